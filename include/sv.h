@@ -1,0 +1,257 @@
+/*
+ * sv.h — C ABI of libsv, the target-model verify step of speculative decoding
+ * on one B300 (sm_103a).
+ *
+ * What the step computes (DSpark summary, "Architecture": the decode round
+ * with an anchor; LFM2.5-DSpark post, "How DSpark works": all drafted tokens
+ * are verified in one forward pass of the target):
+ *   B requests; request r has C_r committed positions in its paged KV cache,
+ *   an anchor token a_r (the last emitted token, not yet cached) and L_r
+ *   drafts d_{r,1..L_r}. The target decoder runs once over the M = sum(L_r+1)
+ *   rows [a_r, d_{r,1}, .., d_{r,L_r}] at absolute positions C_r .. C_r+L_r,
+ *   each row attending to the cached context and to the block rows before
+ *   it. Acceptance then keeps the longest agreeing prefix of the drafts —
+ *   greedy match at temperature 0 (LFM2.5-DSpark post, "Quality parity"),
+ *   rejection sampling above it (DSpark summary, "Problem") — and emits one
+ *   more token: the target's correction at the first rejection, or a bonus
+ *   token when every draft is accepted. The KV rows of the anchor and the
+ *   accepted drafts are committed: seq_len[r] += accepted_len[r] + 1.
+ *
+ * The target is a Llama-style pre-norm decoder (RMSNorm, GQA attention with
+ * rotate-half RoPE, SwiGLU MLP, untied LM head). Its weights are float32,
+ * bf16, or W12: bf16 stored losslessly as three 4-bit planes and rebuilt in
+ * registers inside the matrix kernels (SpecPilot digest, "Reasons").
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers on the current
+ *     device; "host" pointers are ordinary host memory. The library never
+ *     takes ownership of caller memory; the caller keeps it alive until the
+ *     work queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls queue work on it and return without waiting, except
+ *     where a function says it synchronizes.
+ *   - Every function returns an sv_status. Argument errors are detected on
+ *     the host before anything is queued and leave no side effects.
+ *     sv_last_error() gives a message for the last failure on this thread.
+ *   - The library never aborts the process and never traps on the device.
+ *     Device-side checks (token ids, page ids) record a status word that
+ *     sv_model_sync_status() reads back; the offending rows are skipped.
+ */
+#ifndef SV_H
+#define SV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,       /* a size, pointer or option is out of range */
+  SV_ERR_NOT_REPRESENTABLE = 2, /* W12: a value is not a normal number or the exponent window exceeds 16 binades */
+  SV_ERR_KV_CAPACITY = 3,       /* a request's block does not fit its page table */
+  SV_ERR_OUT_OF_MEMORY = 4,     /* workspace allocation failed */
+  SV_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed; see sv_last_error() */
+  SV_ERR_DEVICE_CHECK = 6,      /* a device-side check failed (bad token or page id) */
+  SV_ERR_UNSUPPORTED = 7        /* a configuration this build does not implement */
+} sv_status;
+
+typedef enum {
+  SV_F32 = 0,   /* float32 weights, float32 activations and KV cache */
+  SV_BF16 = 1,  /* bf16 weights, bf16 matrix operands, bf16 KV cache, float32 residual stream */
+  SV_W12 = 2    /* W12 matrices (lossless bf16); otherwise as SV_BF16 */
+} sv_dtype;
+
+/* Model configuration. */
+typedef struct {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t n_heads;       /* query heads */
+  int32_t n_kv_heads;    /* key/value heads; n_heads % n_kv_heads == 0 */
+  int32_t head_dim;      /* 64 or 128 */
+  int32_t ffn;           /* SwiGLU hidden size */
+  int32_t vocab;
+  float rope_theta;      /* RoPE base */
+  float rms_eps;         /* RMSNorm epsilon */
+  int32_t weight_dtype;  /* sv_dtype */
+  int32_t max_batch;     /* largest B passed to sv_verify */
+  int32_t max_gamma;     /* largest L_r (drafts per request, anchor excluded) */
+  int32_t page_size;     /* KV positions per page: 16 */
+  int32_t max_seq_len;   /* largest absolute position + 1 that any row may take */
+  int32_t flags;         /* SV_FLAG_* */
+} sv_config;
+
+/* Also write the full float32 logits [M][vocab] of every verify into the
+ * model's workspace (readable with sv_model_logits). Sampled verifies always
+ * keep them. */
+#define SV_FLAG_KEEP_LOGITS 1
+
+/* A weight matrix [rows][cols] (the output-major layout y = x W^T).
+ * F32/BF16: `data` is a dense row-major device array of that type.
+ * W12: `data` holds plane 0, plane 1, plane 2 back to back, each
+ *      [rows][sv_w12_row_bytes(cols)] bytes (see sv_pack_w12), and `base` is
+ *      the tensor's exponent base. */
+typedef struct {
+  const void* data;
+  int32_t base;
+} sv_matrix;
+
+/* One decoder layer. Norm gains are float32 for SV_F32 models, bf16 otherwise. */
+typedef struct {
+  const void* attn_norm;  /* device [d_model] */
+  sv_matrix wqkv;         /* [(n_heads + 2 n_kv_heads) head_dim][d_model]: q rows, then k rows, then v rows */
+  sv_matrix wo;           /* [d_model][n_heads head_dim] */
+  const void* mlp_norm;   /* device [d_model] */
+  sv_matrix wgu;          /* [2 ffn][d_model]: gate rows, then up rows */
+  sv_matrix wd;           /* [d_model][ffn] */
+} sv_layer_weights;
+
+typedef struct {
+  const void* embed;               /* device [vocab][d_model]; float32 for SV_F32 models, bf16 otherwise */
+  const void* final_norm;          /* device [d_model] */
+  sv_matrix lm_head;               /* [vocab][d_model] */
+  const sv_layer_weights* layers;  /* host array [n_layers]; copied by sv_model_create */
+} sv_weights;
+
+/* Paged KV cache. Pages of all requests come from one pool per layer.
+ * K and V page pools of layer l: device [n_pages][n_kv_heads][page_size][head_dim],
+ * float32 for SV_F32 models, bf16 otherwise. Position p of request r lives in
+ * page page_table[r][p / page_size], slot p % page_size. */
+typedef struct {
+  void* const* k;              /* host array [n_layers] of device pointers */
+  void* const* v;              /* host array [n_layers] of device pointers */
+  int32_t n_pages;
+  const int32_t* page_table;   /* device [batch][max_pages_per_seq] */
+  int32_t max_pages_per_seq;
+  int32_t* seq_len;            /* device [batch]: C_r in, C_r + accepted_len + 1 out */
+} sv_kv;
+
+typedef struct sv_model sv_model;
+
+/* Create a model. The weight pointers are borrowed (not copied) and must
+ * outlive the model; the layer array itself is copied. Allocates the
+ * workspace for max_batch * (1 + max_gamma) rows and the RoPE table on the
+ * current device, and queues their initialization on `stream`. */
+sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void* stream, sv_model** out);
+void sv_model_destroy(sv_model* model);
+
+/*
+ * The verify step.
+ *   batch        B, 1 <= B <= max_batch.
+ *   tokens       device int32 [B][1 + max_gamma]: column 0 the anchor a_r,
+ *                columns 1..L_r the drafts; other columns are ignored.
+ *   verify_lens  HOST int32 [B]: L_r in 0..max_gamma. It is a host array
+ *                because the launch shapes of every kernel depend on
+ *                M = sum(L_r + 1), and the scheduler that chooses L_r runs on
+ *                the host (DSpark summary, "Architecture", the prefix
+ *                scheduler).
+ *   kv           the paged cache; rows C_r..C_r+L_r must have pages.
+ *   draft_probs  device float32 [B][max_gamma][vocab]: q_i, the distribution
+ *                d_i was drawn from. Required when temperature > 0, ignored
+ *                (may be NULL) when temperature == 0.
+ *   temperature  0: greedy match; > 0: rejection sampling with target
+ *                p = softmax(z / temperature): accept d_i iff
+ *                u_i * q_i(d_i) < p_{i-1}(d_i); at the first rejection emit a
+ *                draw from max(0, p_{i-1} - q_i) normalized, else a draw from
+ *                p_{L_r}; draws by inverse CDF in token order.
+ *   seed, request_ids (device int64 [B], or NULL for ids 0..B-1): Philox4x32-10
+ *                key (seed) and counter (position, stream, request id) of the
+ *                uniforms; position = absolute position of the emitted token,
+ *                stream 0 = accept test, 1 = draw.
+ *   accepted_len device int32 [B] out: k_r, the accepted drafts.
+ *   next_token   device int32 [B] out: the correction or bonus token.
+ * Writes the K/V of all M rows into their page slots, then commits
+ * seq_len[r] += k_r + 1 (rows past the accepted prefix are left to be
+ * overwritten). Asynchronous on `stream`.
+ * Errors: SV_ERR_INVALID_ARG (B, L_r, temperature, NULL pointers),
+ *         SV_ERR_CUDA (launch failure).
+ */
+sv_status sv_verify(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
+                    const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
+                    const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream);
+
+/* sv_verify for callers whose per-step inputs and outputs live in host memory:
+ * tokens [B][1 + max_gamma], draft_probs [B][max_gamma][vocab] (or NULL),
+ * request_ids [B] (or NULL), accepted_len [B] and next_token [B] are HOST
+ * pointers; the KV cache stays on the device. Copies the inputs into the
+ * model's workspace, runs the step, copies the outputs back and synchronizes
+ * `stream` before returning. */
+sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
+                         const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
+                         const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream);
+
+/* Copy the float32 logits [M][vocab] of the last verify (rows in request
+ * order, anchor row first) to device `dst`. Valid after a sampled verify, or
+ * after any verify when the model was created with SV_FLAG_KEEP_LOGITS;
+ * otherwise SV_ERR_INVALID_ARG. `rows` must equal that verify's M. */
+sv_status sv_model_logits(sv_model* model, float* dst, int32_t rows, void* stream);
+
+/* Synchronize `stream`, read and clear the device status word. Returns
+ * SV_ERR_DEVICE_CHECK if a kernel saw a token id outside [0, vocab) or a
+ * page id outside [0, n_pages) since the last call; sv_last_error() names it. */
+sv_status sv_model_sync_status(sv_model* model, void* stream);
+
+/* Kernel timing for measurement. When enabled, the library records CUDA
+ * events around its launches on `stream` and accumulates per-kernel-class
+ * device time; sv_model_timing synchronizes on the recorded events, adds
+ * them up, and returns the totals (milliseconds) and launch counts of the
+ * classes below since timing was last enabled. Recording events between
+ * launches adds a little time to each step, so leave it off when timing
+ * whole steps. */
+enum { SV_KC_GEMM = 0, SV_KC_ATTENTION = 1, SV_KC_NORM = 2, SV_KC_LM_HEAD = 3, SV_KC_ACCEPT = 4, SV_KC_COUNT = 5 };
+sv_status sv_model_set_timing(sv_model* model, int32_t enable);
+sv_status sv_model_timing(sv_model* model, double* ms /* [SV_KC_COUNT] */, int64_t* launches /* [SV_KC_COUNT] */);
+
+/*
+ * W12 codec (SpecPilot digest, "Reasons": BF16 split into three 4-bit
+ * bit-planes and rebuilt bit-exactly in the GEMM's registers). The page
+ * fixes no bit layout; this library's:
+ *   bf16 b = s<<15 | E<<7 | m; base = min E over the tensor;
+ *   code c = s<<11 | (E - base)<<7 | m (12 bits);
+ *   plane p holds nibble p of c, row-major [rows][sv_w12_row_bytes(cols)]
+ *   bytes, element k in byte k/2 (low nibble for even k), zero padding.
+ * A tensor is representable iff every element is a normal number (not
+ * +-0, subnormal, inf or NaN) and max E - min E <= 15.
+ */
+int32_t sv_w12_row_bytes(int64_t cols);
+
+/* Pack device bf16 [rows][cols] into device `planes` (3 * rows *
+ * sv_w12_row_bytes(cols) bytes, caller-allocated). Writes the base to
+ * *base_out and the number of offending elements to *n_unrepresentable
+ * (host). Synchronizes `stream`. Returns SV_ERR_NOT_REPRESENTABLE (planes
+ * then undefined) when the tensor is not representable. */
+sv_status sv_pack_w12(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t* planes, int32_t* base_out,
+                      int64_t* n_unrepresentable, void* stream);
+
+/* Rebuild device bf16 [rows][cols] from planes and base. Asynchronous. */
+sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64_t cols, uint16_t* bf16_out,
+                        void* stream);
+
+/*
+ * Skinny weight-streaming matrix product y[M][N] = x[M][K] W^T with the
+ * verify step's own kernels (the path every projection of the step takes):
+ * W [N][K] of `wdtype` (F32, BF16 or W12 as in sv_matrix); x device [M][K]
+ * float32 for F32 weights, bf16 otherwise; y device float32 [M][N].
+ * 1 <= M <= 4096. Uses `workspace` (device, at least sv_linear_workspace_bytes
+ * bytes, caller-allocated, zero-filled before first use and left zeroed by
+ * every call) for split-K partial sums and tile counters. Asynchronous.
+ */
+size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K);
+sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t M, float* y,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Philox4x32-10 uniforms of the verify step: out[i] = u(seed, request_id,
+ * position0 + i, stream_id) for i < n, device float32. Asynchronous. */
+sv_status sv_philox_uniform(uint64_t seed, int64_t request_id, int64_t position0, int32_t stream_id, int32_t n,
+                            float* out, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* sv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_H */

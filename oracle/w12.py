@@ -40,8 +40,10 @@ def representable_mask(bits):
 def pack(bits):
     """Pack a 2-D uint16 array of bf16 patterns.
 
-    Returns (planes uint8 [3, rows, ld], base). Raises NotRepresentable with
-    the count of offending elements when the tensor is not representable.
+    Returns (planes uint8 [3, rows, ld], base). Raises NotRepresentable when
+    the tensor is not representable; its argument counts the offending
+    elements: those that are not normal numbers, plus the normal ones whose
+    exponent exceeds (min exponent over normal elements) + 15.
     """
     bits = np.asarray(bits, dtype=np.uint16)
     if bits.ndim != 2:
@@ -49,12 +51,12 @@ def pack(bits):
     rows, cols = bits.shape
     s, e, m = fields(bits)
     normal = representable_mask(bits)
-    if not normal.all():
-        raise NotRepresentable(int((~normal).sum()))
-    base = int(e.min()) if e.size else 1
+    base = int(e[normal].min()) if normal.any() else 1
     off = e - base
-    if (off > 15).any():
-        raise NotRepresentable(int((off > 15).sum()))
+    # offending elements: the non-normal ones, plus the normal ones above the window
+    bad = int((~normal).sum()) + int(((off > 15) & normal).sum())
+    if bad:
+        raise NotRepresentable(bad)
     code = (s << 11) | (off << 7) | m
     ld = row_bytes(cols)
     planes = np.zeros((3, rows, ld), dtype=np.uint8)

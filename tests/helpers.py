@@ -1,0 +1,89 @@
+"""Test glue: oracle-side references and GPU setup from the same seeded inputs."""
+import numpy as np
+
+import synth
+import synth.device as sd
+from oracle import accept, decoder, spec
+from oracle.decoder import Config, DenseWeights
+
+MARGIN = 0.1        # greedy: a decision may differ only where the oracle's top-1/top-2 gap is <= this
+RATIO_TOL = 1e-3    # sampled: ... or where |u - p/q| <= this
+CDF_TOL = 1e-5      # sampled draws: ... or where u * S lies within this fraction of S of a CDF step
+LOGIT_TOL = {"f32": 1e-4, "bf16": 5e-2}
+
+
+def oracle_config(shape, kind):
+    dt = "f32" if kind == "f32" else "bf16"
+    return Config(**shape, kv_dtype=dt, act_dtype=dt)
+
+
+def oracle_weights(shape, hw, kind):
+    cfg = oracle_config(shape, kind)
+    return cfg, DenseWeights(cfg, hw["layers"], hw["embed"], hw["final_norm"], hw["lm_head"], bf16=(kind != "f32"))
+
+
+def torch_dtype(kind):
+    import torch
+    return torch.float32 if kind == "f32" else torch.bfloat16
+
+
+def build_kv(shape, states, page_size, max_gamma, kind, shuffled=True, extra_pages=0, stream_id=(7, 7)):
+    """Device KV pools holding each oracle state's cache; returns (pools_k, pools_v, table, seq_len)."""
+    import torch
+    lengths = [st.length + max_gamma + 1 for st in states]
+    max_pages = max((n + page_size - 1) // page_size for n in lengths) + 1
+    if shuffled:
+        table, n_pages = synth.shuffled_page_table(lengths, page_size, max_pages, *stream_id)
+    else:
+        table, n_pages = synth.contiguous_page_table(lengths, page_size, max_pages)
+    ks, vs = sd.kv_pools(shape, n_pages + extra_pages, page_size, torch_dtype(kind), fill="zeros")
+    for r, st in enumerate(states):
+        if st.length == 0:
+            continue
+        pos = np.arange(st.length)
+        for l in range(shape["n_layers"]):
+            sd.write_positions(ks[l], table[r], pos, torch.from_numpy(st.k[l]), page_size)
+            sd.write_positions(vs[l], table[r], pos, torch.from_numpy(st.v[l]), page_size)
+    seq = torch.tensor([st.length for st in states], dtype=torch.int32, device="cuda")
+    return ks, vs, table, seq
+
+
+def top2_gap(z):
+    t = np.partition(np.asarray(z), -2)[-2:]
+    return float(t[1] - t[0])
+
+
+def judge_greedy(logits, drafts, k_gpu, next_gpu):
+    """'match', 'near_tie' or 'mismatch' for one request's greedy decision."""
+    k_o, n_o = accept.greedy_accept(logits, drafts)
+    if (k_o, n_o) == (int(k_gpu), int(next_gpu)):
+        return "match"
+    last = min(len(drafts), max(k_o, int(k_gpu)))
+    if any(top2_gap(logits[j]) <= MARGIN for j in range(last + 1)):
+        return "near_tie"
+    return "mismatch"
+
+
+def judge_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, next_gpu):
+    u_acc, u_res = accept.uniforms(seed, req, start, len(drafts))
+    k_o, n_o = accept.sampled_accept(logits, drafts, q, temperature, u_acc, u_res)
+    if (k_o, n_o) == (int(k_gpu), int(next_gpu)):
+        return "match"
+    p = accept.softmax(logits, temperature)
+    q = np.asarray(q, dtype=np.float64)
+    for i in range(1, min(len(drafts), max(k_o, int(k_gpu)) + 1) + 1):
+        d = drafts[i - 1]
+        ratio = p[i - 1, d] / q[i - 1, d] if q[i - 1, d] > 0 else np.inf
+        if abs(u_acc[i - 1] - ratio) <= RATIO_TOL:
+            return "near_tie"
+    if k_o == int(k_gpu):
+        if k_o < len(drafts):
+            w = np.maximum(0.0, p[k_o] - q[k_o])
+            if w.sum() <= 0:
+                w = p[k_o]
+        else:
+            w = p[k_o]
+        cdf = np.cumsum(w)
+        if np.min(np.abs(cdf - u_res[k_o] * cdf[-1])) <= CDF_TOL * cdf[-1]:
+            return "near_tie"
+    return "mismatch"

@@ -1,0 +1,251 @@
+"""Python binding of libsv, the B300 verify step of speculative decoding.
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of libsv.so (built by verify_step_02_b300.build). PyTorch supplies
+device memory and streams. Importing this package loads the library and
+raises ImportError when it has not been built; there is no fallback.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libsv.so is not built ({LIB_PATH}); run python -m verify_step_02_b300.build")
+lib = ctypes.CDLL(LIB_PATH)
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_NOT_REPRESENTABLE, SV_ERR_KV_CAPACITY = 0, 1, 2, 3
+SV_ERR_OUT_OF_MEMORY, SV_ERR_CUDA, SV_ERR_DEVICE_CHECK, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
+SV_F32, SV_BF16, SV_W12 = 0, 1, 2
+SV_FLAG_KEEP_LOGITS = 1
+KERNEL_CLASSES = ("gemm", "attention", "norm", "lm_head", "accept")
+
+
+class SvError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"sv status {status}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab")] + \
+               [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + \
+               [(n, ctypes.c_int32) for n in
+                ("weight_dtype", "max_batch", "max_gamma", "page_size", "max_seq_len", "flags")]
+
+
+class Matrix(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("base", ctypes.c_int32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("attn_norm", ctypes.c_void_p), ("wqkv", Matrix), ("wo", Matrix),
+                ("mlp_norm", ctypes.c_void_p), ("wgu", Matrix), ("wd", Matrix)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p), ("lm_head", Matrix),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class KV(ctypes.Structure):
+    _fields_ = [("k", ctypes.POINTER(ctypes.c_void_p)), ("v", ctypes.POINTER(ctypes.c_void_p)),
+                ("n_pages", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+                ("max_pages_per_seq", ctypes.c_int32), ("seq_len", ctypes.c_void_p)]
+
+
+_vp, _i32, _i64, _u64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                    ctypes.c_float, ctypes.c_size_t)
+_SIGS = {
+    "sv_model_create": (_i32, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _vp, ctypes.POINTER(_vp)]),
+    "sv_model_destroy": (None, [_vp]),
+    "sv_verify": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _f32, _u64, _vp, _vp, _vp, _vp]),
+    "sv_verify_host": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _f32, _u64, _vp, _vp, _vp, _vp]),
+    "sv_model_logits": (_i32, [_vp, _vp, _i32, _vp]),
+    "sv_model_sync_status": (_i32, [_vp, _vp]),
+    "sv_model_set_timing": (_i32, [_vp, _i32]),
+    "sv_model_timing": (_i32, [_vp, _vp, _vp]),
+    "sv_w12_row_bytes": (_i32, [_i64]),
+    "sv_pack_w12": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i64), _vp]),
+    "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+    "sv_linear_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "sv_philox_uniform": (_i32, [_u64, _i64, _i64, _i32, _i32, _vp, _vp]),
+    "sv_last_error": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype, _fn.argtypes = _res, _args
+
+
+def _check(status):
+    if status != SV_OK:
+        raise SvError(status, lib.sv_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_config(shape, weight_dtype, max_batch, max_gamma, max_seq_len, page_size=16, rms_eps=1e-6, flags=0):
+    return Config(shape["n_layers"], shape["d_model"], shape["n_heads"], shape["n_kv_heads"], shape["head_dim"],
+                  shape["ffn"], shape["vocab"], float(shape["rope_theta"]), float(rms_eps), int(weight_dtype),
+                  int(max_batch), int(max_gamma), int(page_size), int(max_seq_len), int(flags))
+
+
+class KVCache:
+    """Paged KV pools (torch tensors [n_pages, n_kv, page_size, head_dim] per layer), page table, seq_len."""
+
+    def __init__(self, k_pools, v_pools, page_table, seq_len):
+        self.k_pools, self.v_pools = list(k_pools), list(v_pools)
+        self.page_table, self.seq_len = page_table, seq_len
+        n = len(self.k_pools)
+        self._k = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.k_pools])
+        self._v = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.v_pools])
+        self.struct = KV(ctypes.cast(self._k, ctypes.POINTER(ctypes.c_void_p)),
+                         ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)),
+                         int(self.k_pools[0].shape[0]), page_table.data_ptr(), int(page_table.shape[1]),
+                         seq_len.data_ptr())
+
+
+class Model:
+    """A verify engine over caller-owned device weights (kept referenced here).
+
+    weights: dict with "layers" (list of dicts: attn_norm, wqkv, wo, mlp_norm, wgu, wd),
+    "embed", "final_norm", "lm_head"; tensors on the current CUDA device. For W12
+    models each matrix entry is a (planes_tensor, base) pair.
+    """
+
+    def __init__(self, config, weights, stream=None):
+        self.config = config
+        self._keep = weights
+
+        def mat(x):
+            if isinstance(x, tuple):
+                return Matrix(x[0].data_ptr(), int(x[1]))
+            return Matrix(x.data_ptr(), 0)
+
+        layers = weights["layers"]
+        self._layers = (LayerWeights * len(layers))(*[
+            LayerWeights(l["attn_norm"].data_ptr(), mat(l["wqkv"]), mat(l["wo"]), l["mlp_norm"].data_ptr(),
+                         mat(l["wgu"]), mat(l["wd"])) for l in layers])
+        self._w = Weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(), mat(weights["lm_head"]),
+                          ctypes.cast(self._layers, ctypes.POINTER(LayerWeights)))
+        h = ctypes.c_void_p()
+        _check(lib.sv_model_create(ctypes.byref(config), ctypes.byref(self._w), _stream(stream), ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.sv_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def verify(self, tokens, verify_lens, kv, accepted_len, next_token, draft_probs=None, temperature=0.0,
+               seed=0, request_ids=None, stream=None):
+        """tokens, draft_probs, request_ids, accepted_len, next_token: device tensors; verify_lens: host ints."""
+        lens = np.ascontiguousarray(np.asarray(verify_lens, dtype=np.int32))
+        _check(lib.sv_verify(self.handle, len(lens), _ptr(tokens), lens.ctypes.data_as(ctypes.c_void_p),
+                             ctypes.byref(kv.struct), _ptr(draft_probs), float(temperature), int(seed),
+                             _ptr(request_ids), _ptr(accepted_len), _ptr(next_token), _stream(stream)))
+
+    def verify_host(self, tokens, verify_lens, kv, draft_probs=None, temperature=0.0, seed=0, request_ids=None,
+                    stream=None, out=None):
+        """Host-memory inputs and outputs (numpy or pinned torch CPU tensors); synchronizes."""
+        lens = np.ascontiguousarray(np.asarray(verify_lens, dtype=np.int32))
+        b = len(lens)
+        if out is None:
+            out = (np.zeros(b, np.int32), np.zeros(b, np.int32))
+
+        def hp(a):
+            if a is None:
+                return None
+            if hasattr(a, "data_ptr"):
+                return ctypes.c_void_p(a.data_ptr())
+            return a.ctypes.data_as(ctypes.c_void_p)
+
+        _check(lib.sv_verify_host(self.handle, b, hp(tokens), lens.ctypes.data_as(ctypes.c_void_p),
+                                  ctypes.byref(kv.struct), hp(draft_probs), float(temperature), int(seed),
+                                  hp(request_ids), hp(out[0]), hp(out[1]), _stream(stream)))
+        return out
+
+    def logits(self, rows, stream=None):
+        import torch
+        out = torch.empty((rows, self.config.vocab), dtype=torch.float32, device="cuda")
+        _check(lib.sv_model_logits(self.handle, _ptr(out), int(rows), _stream(stream)))
+        return out
+
+    def sync_status(self, stream=None):
+        _check(lib.sv_model_sync_status(self.handle, _stream(stream)))
+
+    def set_timing(self, enable):
+        _check(lib.sv_model_set_timing(self.handle, int(bool(enable))))
+
+    def timing(self):
+        ms = (ctypes.c_double * 5)()
+        n = (ctypes.c_int64 * 5)()
+        _check(lib.sv_model_timing(self.handle, ms, n))
+        return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+def w12_row_bytes(cols):
+    return int(lib.sv_w12_row_bytes(int(cols)))
+
+
+def pack_w12(bf16, stream=None):
+    """bf16 device tensor [rows, cols] -> (uint8 planes [3, rows, row_bytes], base). Raises SvError."""
+    import torch
+    rows, cols = bf16.shape
+    planes = torch.empty((3, rows, w12_row_bytes(cols)), dtype=torch.uint8, device=bf16.device)
+    base, bad = ctypes.c_int32(), ctypes.c_int64()
+    st = lib.sv_pack_w12(_ptr(bf16), rows, cols, _ptr(planes), ctypes.byref(base), ctypes.byref(bad),
+                         _stream(stream))
+    if st != SV_OK:
+        err = SvError(st, lib.sv_last_error().decode())
+        err.n_unrepresentable = bad.value
+        raise err
+    return planes, base.value
+
+
+def unpack_w12(planes, base, rows, cols, stream=None):
+    import torch
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=planes.device)
+    _check(lib.sv_unpack_w12(_ptr(planes), int(base), rows, cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def linear(wdtype, w, x, n, k, base=0, stream=None, workspace=None):
+    """y = x W^T with the verify step's GEMM kernels. Returns (y float32 [M, n], workspace)."""
+    import torch
+    m = int(x.shape[0])
+    need = int(lib.sv_linear_workspace_bytes(int(wdtype), m, int(n), int(k)))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=x.device)
+    y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    mat = Matrix(w.data_ptr(), int(base))
+    _check(lib.sv_linear(int(wdtype), ctypes.byref(mat), int(n), int(k), _ptr(x), m, _ptr(y), _ptr(workspace),
+                         workspace.numel(), _stream(stream)))
+    return y, workspace
+
+
+def philox_uniform(seed, request_id, position0, stream_id, n, stream=None):
+    import torch
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    _check(lib.sv_philox_uniform(int(seed), int(request_id), int(position0), int(stream_id), int(n), _ptr(out),
+                                 _stream(stream)))
+    return out

@@ -1,0 +1,183 @@
+// CUDA-core skinny GEMM: y[m][n] = x[m] . W[n] for float32, bf16 or W12 weights.
+//
+// This path serves float32 models (no TF32: float32 products keep the
+// float32 model's accuracy) and bf16/W12 blocks too small for the tensor
+// path. One CTA computes a 128-row x 32-token tile over one K range; the W
+// tile is converted to float32 once into shared memory (W12 rebuilt from its
+// three nibble planes to bf16 on the way, SpecPilot digest, "Reasons") and
+// every thread then runs an 8 x 2 register-blocked FMA loop. K is split
+// across CTAs until the grid covers the GPU; the last split of a tile reduces
+// the partials in a fixed order and runs the projection's epilogue.
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int BN = kGemmBN, BM = kFmaBM, KC = kFmaKC;
+constexpr int WS_LD = BN + 4, XS_LD = BM + 4, YS_LD = BM + 1;
+
+// W row of tile row t, or -1 when the tile row is past the matrix.
+__device__ __forceinline__ int weight_row(const GemmArgs& a, int nt, int t) {
+  if (a.pair == kPairSwiglu) {
+    const int f = nt * (BN / 2) + (t & (BN / 2 - 1));
+    if (f >= a.ffn) return -1;
+    return t < BN / 2 ? f : a.ffn + f;
+  }
+  const int r = nt * BN + t;
+  return r < a.n_rows ? r : -1;
+}
+
+// 16 consecutive weights of row `row` starting at k (k % 16 == 0), as float32.
+template <int WT>
+__device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, float* v) {
+  if (WT == SV_F32) {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.w) + (long long)row * a.K + k);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 f = __ldg(p + j);
+      v[4 * j] = f.x;
+      v[4 * j + 1] = f.y;
+      v[4 * j + 2] = f.z;
+      v[4 * j + 3] = f.w;
+    }
+  } else if (WT == SV_BF16) {
+    const uint4* p =
+        reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.w) + (long long)row * a.K + k);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint4 u = __ldg(p + j);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[8 * j + 2 * q] = __uint_as_float(w[q] << 16);
+        v[8 * j + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+      }
+    }
+  } else {  // W12: bytes k/2 .. k/2+7 of each plane
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(a.w) + (long long)row * a.w12_ld + (k >> 1);
+    const uint2 p0 = __ldg(reinterpret_cast<const uint2*>(base));
+    const uint2 p1 = __ldg(reinterpret_cast<const uint2*>(base + a.w12_plane));
+    const uint2 p2 = __ldg(reinterpret_cast<const uint2*>(base + 2 * a.w12_plane));
+    const uint32_t ebase = static_cast<uint32_t>(a.w12_base) << 7;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t b0 = h ? p0.y : p0.x, b1 = h ? p1.y : p1.x, b2 = h ? p2.y : p2.x;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t c = ((b2 >> (4 * e)) & 0xFu) << 8 | ((b1 >> (4 * e)) & 0xFu) << 4 | ((b0 >> (4 * e)) & 0xFu);
+        const uint32_t bits = ((c & 0x7FFu) + ebase) | ((c & 0x800u) << 4);
+        v[8 * h + e] = __uint_as_float(bits << 16);
+      }
+    }
+  }
+}
+
+template <int WT>
+__global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
+  __shared__ __align__(16) float Ws[KC][WS_LD];
+  __shared__ __align__(16) float Xs[KC][XS_LD];
+  __shared__ __align__(16) float Ys[BN * YS_LD];
+  const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int tr = (tid & 15) * 8, tc = (tid >> 4) * 2;
+  const int m0 = mt * BM;
+  const int kbeg = ks * a.k_chunk, kend = min(a.K, kbeg + a.k_chunk);
+  float acc[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = 0.f;
+
+  const int lrow = tid & (BN - 1), lkk = (tid >> 7) * 16;  // W loader: one row, 16 k
+  const int wrow = weight_row(a, nt, lrow);
+  const int xtok = tid >> 3, xkk = (tid & 7) * 4;          // X loader: one token, 4 k
+  const int xm = m0 + xtok;
+
+  for (int k0 = kbeg; k0 < kend; k0 += KC) {
+    {
+      float v[16];
+      const int k = k0 + lkk;
+      if (wrow >= 0 && k < kend) {
+        load_w16<WT>(a, wrow, k, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) Ws[lkk + i][lrow] = v[i];
+    }
+    {
+      const int k = k0 + xkk;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float xv = 0.f;
+        if (xm < a.M && k + i < kend) {
+          const long long off = (long long)xm * a.K + k + i;
+          xv = WT == SV_F32 ? reinterpret_cast<const float*>(a.x)[off]
+                            : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(a.x)[off] << 16);
+        }
+        Xs[xkk + i][xtok] = xv;
+      }
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < KC; ++k) {
+      const float4 w0 = *reinterpret_cast<const float4*>(&Ws[k][tr]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&Ws[k][tr + 4]);
+      const float2 x = *reinterpret_cast<const float2*>(&Xs[k][tc]);
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i][0] = fmaf(wv[i], x.x, acc[i][0]);
+        acc[i][1] = fmaf(wv[i], x.y, acc[i][1]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    Ys[(tr + i) * YS_LD + tc] = acc[i][0];
+    Ys[(tr + i) * YS_LD + tc + 1] = acc[i][1];
+  }
+  __syncthreads();
+  const int mcount = min(BM, a.M - m0);
+  if (a.k_splits > 1) {
+    if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM)) return;
+  }
+  epilogue_tile(a, nt, Ys, YS_LD, m0, mcount);
+}
+
+}  // namespace
+
+void plan_gemm(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count) {
+  a.M = M;
+  a.K = K;
+  a.pair = pair;
+  a.n_tiles = pair == kPairSwiglu ? (n_units + BN / 2 - 1) / (BN / 2) : (n_units + BN - 1) / BN;
+  a.m_tiles = (M + BM - 1) / BM;
+  const int base = a.n_tiles * a.m_tiles;
+  const int target = 4 * sm_count;
+  const int ksteps = (K + KC - 1) / KC;
+  int splits = (target + base - 1) / base;
+  if (splits > ksteps) splits = ksteps;
+  if (splits < 1) splits = 1;
+  const int steps_per = (ksteps + splits - 1) / splits;
+  a.k_chunk = steps_per * KC;
+  a.k_splits = (K + a.k_chunk - 1) / a.k_chunk;
+}
+
+size_t gemm_partial_floats(const GemmArgs& a) {
+  return a.k_splits > 1 ? (size_t)a.n_tiles * a.m_tiles * a.k_splits * BN * BM : 0;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+  const dim3 grid(a.n_tiles, a.m_tiles, a.k_splits);
+  switch (a.wdtype) {
+    case SV_F32: gemm_fma_kernel<SV_F32><<<grid, 256, 0, s>>>(a); break;
+    case SV_BF16: gemm_fma_kernel<SV_BF16><<<grid, 256, 0, s>>>(a); break;
+    case SV_W12: gemm_fma_kernel<SV_W12><<<grid, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sv

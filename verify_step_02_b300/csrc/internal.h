@@ -1,0 +1,157 @@
+// Internal declarations shared by the kernels and the host engine of libsv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sv.h"
+
+namespace sv {
+
+constexpr int kMaxBatch = 1024;       // largest batch a verify may take
+constexpr int kGemmBN = 128;          // weight rows per GEMM tile (both GEMM paths)
+constexpr int kFmaBM = 32;            // tokens per FMA GEMM tile
+constexpr int kFmaKC = 32;            // K step of the FMA GEMM
+
+// Device status word bits (sv_model_sync_status).
+enum : uint32_t { kStBadToken = 1u, kStBadPage = 2u, kStBadDraftProb = 4u, kStTimeout = 8u, kStBadPos = 16u };
+
+enum EpiKind : int {
+  kEpiStore = 0,   // y[m][n] = value                                  (sv_linear)
+  kEpiQkv = 1,     // RoPE on q,k; q -> q_out; k,v -> paged cache      (QKV projection)
+  kEpiResid = 2,   // h[m][n] += value                                 (O and down projections)
+  kEpiSwiglu = 3,  // act[m][f] = SiLU(gate) * up                      (gate|up projection)
+  kEpiLogits = 4,  // logits and per-tile (max, argmax)                (LM head)
+};
+
+// Row pairing of a GEMM tile. kPairNone: tile rows are W rows nt*BN + t.
+// kPairSwiglu: tile rows t < BN/2 are gate rows f0 + t, rows t >= BN/2 the up
+// rows ffn + f0 + t - BN/2, with f0 = nt * BN/2; the epilogue then sees the
+// gate and up value of a feature in the same tile.
+enum PairKind : int { kPairNone = 0, kPairSwiglu = 1 };
+
+struct Epi {
+  int kind;
+  int act_bf16;            // activations written as bf16 (else float32)
+  // kEpiStore
+  float* y;
+  int ldy;
+  // kEpiQkv
+  const int* row_req;      // [M] request of each row
+  const int* row_pos;      // [M] absolute position of each row
+  const float2* rope;      // [max_seq_len][head_dim/2] (cos, sin)
+  int n_heads, n_kv_heads, head_dim;
+  void* q_out;             // [M][n_heads*head_dim]
+  void* k_cache;           // layer's K pool [n_pages][n_kv][page_size][head_dim]
+  void* v_cache;
+  const int* page_table;
+  int max_pages;
+  int page_size;
+  int n_pages;
+  unsigned* status;
+  // kEpiResid
+  float* h;
+  int ldh;
+  // kEpiSwiglu
+  void* act;
+  int ffn;
+  // kEpiLogits
+  float* logits;           // [M][vocab] or nullptr
+  float2* argmax_part;     // [M][n_tiles]: (max value, index as float bits)
+  int vocab;
+};
+
+struct GemmArgs {
+  int wdtype;              // SV_F32, SV_BF16, SV_W12
+  const void* w;           // weights (W12: planes back to back)
+  int w12_base;
+  int w12_ld;              // W12 bytes per plane row
+  long long w12_plane;     // W12 bytes per plane (rows * ld)
+  int n_rows;              // rows of W
+  int K;
+  const void* x;           // activations [M][K]: float32 for SV_F32, bf16 otherwise
+  int M;
+  int pair;                // PairKind
+  int ffn;                 // kPairSwiglu: gate rows [0, ffn), up rows [ffn, 2 ffn)
+  int n_tiles;             // weight tiles
+  int m_tiles;             // token tiles
+  int k_splits;
+  int k_chunk;             // K range of one split (multiple of the K step)
+  float* partials;         // split-K partial tiles
+  unsigned* counters;      // per tile arrivals (zero between launches)
+  Epi epi;
+};
+
+struct AttnArgs {
+  const void* q;           // [M][n_heads*head_dim], act dtype
+  void* out;               // [M][n_heads*head_dim], act dtype
+  const void* k_cache;
+  const void* v_cache;
+  const int* page_table;
+  int max_pages;
+  int page_size;
+  int n_pages;
+  const int* seq_len;      // [B] committed context C_r (before commit)
+  const int* req_row0;     // [B+1] first block row of each request
+  int n_heads, n_kv_heads, head_dim;
+  int chunk;               // keys per work item
+  int max_chunks;
+  int max_rows;            // (max_gamma + 1) * group
+  int max_seq_len;         // a request whose block ends past this is skipped (status kStBadPos)
+  float* partials;         // [B*n_kv*max_chunks][max_rows][head_dim + 2]
+  unsigned* counters;      // [B*n_kv]
+  unsigned* status;
+  int act_bf16;
+};
+
+struct AcceptArgs {
+  int B;
+  int vocab;
+  int gamma_stride;        // 1 + max_gamma (tokens row stride)
+  const int* tokens;       // [B][gamma_stride]
+  const int* req_row0;     // [B+1]
+  int* seq_len;            // [B] in/out
+  const float* logits;     // [M][vocab] (sampled)
+  const float2* argmax_part;  // [M][n_tiles] (greedy)
+  int n_tiles;
+  const float* draft_probs;   // [B][max_gamma][vocab]
+  int max_gamma;
+  float temperature;
+  unsigned long long seed;
+  const long long* request_ids;
+  int* accepted_len;
+  int* next_token;
+  unsigned* status;
+};
+
+struct PrepParams {
+  int B;
+  int M;
+  int gamma_stride;
+  int req_row0[kMaxBatch + 1];
+};
+
+// ---- launchers (defined in the .cu files) ----
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+void plan_gemm(GemmArgs& a, int M, int n_rows_or_pairs, int K, int pair, int sm_count);
+size_t gemm_partial_floats(const GemmArgs& a);
+cudaError_t launch_attention(const AttnArgs& a, int B, int kv_dtype_bf16, cudaStream_t s);
+void plan_attention(AttnArgs& a, int max_batch, int max_seq_len, int max_gamma);
+size_t attention_partial_floats(const AttnArgs& a, int max_batch);
+cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
+                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, int d, int vocab,
+                        int max_seq_len, float eps, int act_bf16, unsigned* status, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, int M, int d, float eps, int act_bf16,
+                           cudaStream_t s);
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s);
+cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s);
+cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int ld, int base, uint8_t* planes,
+                            cudaStream_t s);
+cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, int ld,
+                              uint16_t* out, cudaStream_t s);
+cudaError_t launch_philox(unsigned long long seed, long long req, long long pos0, int stream_id, int n, float* out,
+                          cudaStream_t s);
+
+}  // namespace sv

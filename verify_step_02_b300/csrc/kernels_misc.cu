@@ -1,0 +1,341 @@
+// Row preparation, RMSNorm, acceptance + commit, RoPE table, W12 codec and
+// Philox kernels of the verify step.
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ float load_gain(const void* g, int k, int act_bf16) { return load_act(g, k, act_bf16); }
+
+// Normalize h[m] (float32, d) into u[m]: u = h / sqrt(mean(h^2) + eps) * g.
+__device__ __forceinline__ void norm_row(const float* hrow, const void* gain, void* u, long long m, int d, float eps,
+                                         int act_bf16, float* red) {
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(hrow[k], hrow[k], ss);
+  const float tot = block_sum(ss, red);
+  const float rstd = rsqrtf(tot / static_cast<float>(d) + eps);
+  for (int k = threadIdx.x; k < d; k += blockDim.x)
+    store_act(u, m * d + k, hrow[k] * rstd * load_gain(gain, k, act_bf16), act_bf16);
+}
+
+// One CTA per block row: find the row's request and offset, gather the token's
+// embedding into the residual stream, and apply the first layer's RMSNorm.
+__global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, const int* tokens, const int* seq_len,
+                                                            int* row_req, int* row_pos, int* req_row0_dev,
+                                                            const void* embed, const void* gain, float* h, void* u,
+                                                            int d, int vocab, int max_seq_len, float eps,
+                                                            int act_bf16, unsigned* status) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  if (m == 0)
+    for (int i = threadIdx.x; i <= p.B; i += blockDim.x) req_row0_dev[i] = p.req_row0[i];
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.req_row0[mid] <= m) lo = mid; else hi = mid - 1;
+  }
+  const int r = lo, j = m - p.req_row0[r];
+  int tok = tokens[(long long)r * p.gamma_stride + j];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) atomicOr(status, kStBadToken);
+    tok = 0;
+  }
+  if (threadIdx.x == 0) {
+    // a row past the RoPE table / page budget gets position -1: the QKV
+    // epilogue then writes nothing for it and the status word records it
+    int pos = seq_len[r] + j;
+    if (seq_len[r] < 0 || pos >= max_seq_len) {
+      atomicOr(status, kStBadPos);
+      pos = -1;
+    }
+    row_req[m] = r;
+    row_pos[m] = pos;
+  }
+  float* hrow = h + (long long)m * d;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) hrow[k] = load_act(embed, (long long)tok * d + k, act_bf16);
+  __syncthreads();
+  norm_row(hrow, gain, u, m, d, eps, act_bf16, red);
+}
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* h, const void* gain, void* u, int d,
+                                                               float eps, int act_bf16) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  norm_row(h + (long long)m * d, gain, u, m, d, eps, act_bf16, red);
+}
+
+// ------------------------------------------------------------------ acceptance
+constexpr int kAccThreads = 512;
+
+struct SoftmaxRow {
+  float mx;   // max of z / T
+  float sum;  // sum of exp(z / T - mx)
+};
+
+__device__ SoftmaxRow softmax_stats(const float* z, int V, float invT, float* red) {
+  float mx = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) mx = fmaxf(mx, z[v] * invT);
+  mx = block_max(mx, red);
+  float s = 0.f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(z[v] * invT - mx);
+  s = block_sum(s, red);
+  return {mx, s};
+}
+
+// Inverse-CDF draw in token order over weights w(v) (v < V): the first v whose
+// inclusive prefix sum exceeds u * total. Each thread owns a contiguous
+// segment; segment sums are scanned across the block.
+template <typename WFn>
+__device__ int inverse_cdf_draw(WFn w, int V, float u, float* red, float* seg_pref, int* s_pick) {
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const int seg = (V + nt - 1) / nt;
+  const int v0 = min(V, tid * seg), v1 = min(V, v0 + seg);
+  float mine = 0.f;
+  for (int v = v0; v < v1; ++v) mine += w(v);
+  seg_pref[tid] = mine;
+  __syncthreads();
+  if (tid == 0) {  // exclusive scan of the segment sums (nt <= 1024 values)
+    float run = 0.f;
+    for (int i = 0; i < nt; ++i) {
+      const float t = seg_pref[i];
+      seg_pref[i] = run;
+      run += t;
+    }
+    red[0] = run;
+    s_pick[0] = 0x7fffffff;
+    s_pick[1] = -1;
+  }
+  __syncthreads();
+  const float total = red[0];
+  const float target = u * total;
+  float run = seg_pref[tid];
+  int last_pos = -1;
+  for (int v = v0; v < v1; ++v) {
+    const float wv = w(v);
+    if (wv > 0.f) last_pos = v;
+    run += wv;
+    if (run > target) {
+      atomicMin(s_pick, v);
+      break;
+    }
+  }
+  if (last_pos >= 0) atomicMax(s_pick + 1, last_pos);
+  __syncthreads();
+  const int pick = s_pick[0] != 0x7fffffff ? s_pick[0] : s_pick[1];
+  __syncthreads();
+  return pick < 0 ? 0 : pick;
+}
+
+__global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a) {
+  __shared__ float red[32];
+  __shared__ float seg_pref[kAccThreads];
+  __shared__ int s_pick[2];
+  __shared__ int s_targ[64];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row0 = a.req_row0[r], L = a.req_row0[r + 1] - row0 - 1;
+  const int C = a.seq_len[r];
+  const int* toks = a.tokens + (long long)r * a.gamma_stride;
+  int k = 0, next = 0;
+  if (a.temperature == 0.f) {
+    // t_j = argmax over the LM head's per-tile partials, one warp per block row
+    for (int j = warp; j <= L; j += blockDim.x >> 5) {
+      const float2* part = a.argmax_part + (long long)(row0 + j) * a.n_tiles;
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int t = lane; t < a.n_tiles; t += 32) {
+        const float2 pv = part[t];
+        argmax_merge(best, bi, pv.x, __float_as_int(pv.y));
+      }
+      warp_argmax(best, bi);
+      if (lane == 0) s_targ[j] = bi;
+    }
+    __syncthreads();
+    while (k < L && toks[1 + k] == s_targ[k]) ++k;
+    next = s_targ[k];
+  } else {
+    const float invT = 1.0f / a.temperature;
+    const long long req = a.request_ids ? a.request_ids[r] : r;
+    bool rejected = false;
+    for (int i = 1; i <= L; ++i) {
+      const float* z = a.logits + (long long)(row0 + i - 1) * a.vocab;
+      const SoftmaxRow st = softmax_stats(z, a.vocab, invT, red);
+      int d = toks[i];
+      if (d < 0 || d >= a.vocab) d = 0;
+      const float* q = a.draft_probs + ((long long)r * a.max_gamma + (i - 1)) * a.vocab;
+      const float pd = expf(z[d] * invT - st.mx) / st.sum;
+      const float qd = q[d];
+      const float u = philox_uniform(a.seed, req, (long long)C + i, 0u);
+      if (u * qd < pd) {
+        ++k;
+        continue;
+      }
+      // residual max(0, p - q); if it is all zero, fall back to p
+      const float invS = 1.0f / st.sum;
+      float rs = 0.f;
+      for (int v = tid; v < a.vocab; v += blockDim.x) rs += fmaxf(0.f, expf(z[v] * invT - st.mx) * invS - q[v]);
+      rs = block_sum(rs, red);
+      const float u2 = philox_uniform(a.seed, req, (long long)C + i, 1u);
+      if (rs > 0.f) {
+        next = inverse_cdf_draw([&](int v) { return fmaxf(0.f, expf(z[v] * invT - st.mx) * invS - q[v]); },
+                                a.vocab, u2, red, seg_pref, s_pick);
+      } else {
+        next = inverse_cdf_draw([&](int v) { return expf(z[v] * invT - st.mx) * invS; }, a.vocab, u2, red,
+                                seg_pref, s_pick);
+      }
+      rejected = true;
+      break;
+    }
+    if (!rejected) {
+      const float* z = a.logits + (long long)(row0 + L) * a.vocab;
+      const SoftmaxRow st = softmax_stats(z, a.vocab, invT, red);
+      const float invS = 1.0f / st.sum;
+      const float u2 = philox_uniform(a.seed, req, (long long)C + L + 1, 1u);
+      next = inverse_cdf_draw([&](int v) { return expf(z[v] * invT - st.mx) * invS; }, a.vocab, u2, red, seg_pref,
+                              s_pick);
+    }
+  }
+  if (tid == 0) {
+    a.accepted_len[r] = k;
+    a.next_token[r] = next;
+    a.seq_len[r] = C + k + 1;  // commit the anchor and the accepted drafts
+  }
+}
+
+// ------------------------------------------------------------------ RoPE table
+__global__ void rope_table_kernel(float2* table, int max_seq_len, int half, int head_dim, double theta) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)max_seq_len * half) return;
+  const int pos = static_cast<int>(idx / half), i = static_cast<int>(idx - (long long)pos * half);
+  const double inv_freq = pow(theta, -2.0 * i / head_dim);
+  double s, c;
+  sincos(pos * inv_freq, &s, &c);
+  table[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+// ------------------------------------------------------------------ W12
+// stats[0]: min exponent over normal numbers, stats[1]: max exponent,
+// stats[2]: elements that are not normal numbers. With base >= 0, stats[3]
+// counts elements whose exponent exceeds base + 15.
+__global__ void w12_scan_kernel(const uint16_t* b, long long n, int base, unsigned* stats) {
+  unsigned emin = 255, emax = 0, bad = 0, wide = 0;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const unsigned e = (b[i] >> 7) & 0xFFu;
+    if (e == 0 || e == 255) {
+      ++bad;
+    } else {
+      emin = min(emin, e);
+      emax = max(emax, e);
+      if (base >= 0 && e > (unsigned)base + 15u) ++wide;
+    }
+  }
+  for (int o = 16; o; o >>= 1) {
+    emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+    emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    wide += __shfl_xor_sync(0xffffffffu, wide, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(stats, emin);
+    atomicMax(stats + 1, emax);
+    atomicAdd(stats + 2, bad);
+    atomicAdd(stats + 3, wide);
+  }
+}
+
+__device__ __forceinline__ unsigned w12_code(uint16_t b, int base) {
+  return (unsigned)(b >> 15) << 11 | (((b >> 7) & 0xFFu) - (unsigned)base) << 7 | (b & 0x7Fu);
+}
+
+// One thread per plane byte column: elements 2c and 2c + 1 of a row.
+__global__ void w12_pack_kernel(const uint16_t* b, long long rows, long long cols, int ld, int base, uint8_t* planes) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * ld) return;
+  const long long row = idx / ld, c = idx - row * ld;
+  const long long k0 = 2 * c, k1 = 2 * c + 1;
+  const unsigned c0 = k0 < cols ? w12_code(b[row * cols + k0], base) : 0u;
+  const unsigned c1 = k1 < cols ? w12_code(b[row * cols + k1], base) : 0u;
+  const long long plane = rows * ld;
+#pragma unroll
+  for (int p = 0; p < 3; ++p)
+    planes[p * plane + idx] = static_cast<uint8_t>(((c0 >> (4 * p)) & 0xFu) | ((c1 >> (4 * p)) & 0xFu) << 4);
+}
+
+__global__ void w12_unpack_kernel(const uint8_t* planes, int base, long long rows, long long cols, int ld,
+                                  uint16_t* out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * cols) return;
+  const long long row = idx / cols, k = idx - row * cols;
+  const long long byte = row * ld + (k >> 1);
+  const int sh = (k & 1) * 4;
+  const long long plane = rows * ld;
+  const unsigned c = ((planes[byte] >> sh) & 0xFu) | ((planes[plane + byte] >> sh) & 0xFu) << 4 |
+                     ((planes[2 * plane + byte] >> sh) & 0xFu) << 8;
+  out[idx] = static_cast<uint16_t>(((c & 0x7FFu) + ((unsigned)base << 7)) | ((c & 0x800u) << 4));
+}
+
+__global__ void philox_kernel(unsigned long long seed, long long req, long long pos0, int stream_id, int n,
+                              float* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = philox_uniform(seed, req, pos0 + i, static_cast<unsigned>(stream_id));
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
+                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, int d, int vocab,
+                        int max_seq_len, float eps, int act_bf16, unsigned* status, cudaStream_t s) {
+  prep_kernel<<<p.M, kNormThreads, 0, s>>>(p, tokens, seq_len, row_req, row_pos, req_row0_dev, embed, gain, h, u, d,
+                                           vocab, max_seq_len, eps, act_bf16, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, int M, int d, float eps, int act_bf16,
+                           cudaStream_t s) {
+  rmsnorm_kernel<<<M, kNormThreads, 0, s>>>(h, gain, u, d, eps, act_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
+  accept_kernel<<<a.B, kAccThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s) {
+  const int half = head_dim / 2;
+  const long long n = (long long)max_seq_len * half;
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(table, max_seq_len, half, head_dim, (double)theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s) {
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  w12_scan_kernel<<<(unsigned)blocks, 256, 0, s>>>(bf16, n, base, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int ld, int base, uint8_t* planes,
+                            cudaStream_t s) {
+  const long long n = rows * ld;
+  w12_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(bf16, rows, cols, ld, base, planes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, int ld, uint16_t* out,
+                              cudaStream_t s) {
+  const long long n = rows * cols;
+  w12_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(planes, base, rows, cols, ld, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_philox(unsigned long long seed, long long req, long long pos0, int stream_id, int n, float* out,
+                          cudaStream_t s) {
+  philox_kernel<<<(n + 255) / 256, 256, 0, s>>>(seed, req, pos0, stream_id, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,656 @@
+// Host engine and C ABI of libsv: argument checks, workspace, and the
+// launch sequence of one verify step (embedding, per layer QKV+RoPE+KV write,
+// block-causal attention, O projection, MLP, then LM head and acceptance).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "internal.h"
+
+using namespace sv;
+
+namespace {
+
+thread_local std::string g_err;
+
+sv_status fail(sv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+sv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define SV_CUDA(call, what)                         \
+  do {                                              \
+    cudaError_t e_ = (call);                        \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+int w12_row_bytes(long long cols) { return static_cast<int>(((cols + 31) / 32) * 16); }
+
+struct Timing {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[SV_KC_COUNT];
+  std::vector<cudaEvent_t> spare;
+  double ms[SV_KC_COUNT] = {};
+  long long launches[SV_KC_COUNT] = {};
+};
+
+}  // namespace
+
+struct sv_model {
+  sv_config cfg;
+  sv_weights w;
+  std::vector<sv_layer_weights> layers;
+  int act_bf16 = 0;
+  int act_bytes = 4;
+  int sm_count = 148;
+  int m_max = 0;
+  int lm_tiles = 0;
+  // workspace
+  float* h = nullptr;
+  void* u = nullptr;
+  void* q = nullptr;
+  void* ao = nullptr;
+  void* act = nullptr;
+  float* logits = nullptr;
+  float2* argmax_part = nullptr;
+  int* row_req = nullptr;
+  int* row_pos = nullptr;
+  int* req_row0 = nullptr;
+  float2* rope = nullptr;
+  float* gemm_part = nullptr;
+  unsigned* gemm_cnt = nullptr;
+  float* attn_part = nullptr;
+  unsigned* attn_cnt = nullptr;
+  unsigned* status = nullptr;
+  // staging for sv_verify_host
+  int* d_tokens = nullptr;
+  float* d_probs = nullptr;
+  long long* d_reqids = nullptr;
+  int* d_out = nullptr;  // accepted_len [max_batch], next_token [max_batch]
+  std::vector<void*> allocs;
+  bool last_logits = false;
+  int last_m = 0;
+  Timing timing;
+};
+
+namespace {
+
+template <typename T>
+sv_status dalloc(sv_model* m, T** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  void* q = nullptr;
+  const cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) return fail(SV_ERR_OUT_OF_MEMORY, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  m->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return SV_OK;
+}
+
+void free_all(sv_model* m) {
+  for (void* p : m->allocs) cudaFree(p);
+  m->allocs.clear();
+  for (auto& v : m->timing.pending)
+    for (auto& pr : v) {
+      cudaEventDestroy(pr.first);
+      cudaEventDestroy(pr.second);
+    }
+  for (cudaEvent_t e : m->timing.spare) cudaEventDestroy(e);
+}
+
+int nqkv(const sv_config& c) { return (c.n_heads + 2 * c.n_kv_heads) * c.head_dim; }
+
+sv_status check_config(const sv_config* c) {
+  if (!c) return fail(SV_ERR_INVALID_ARG, "config is NULL");
+  if (c->n_layers < 1 || c->d_model < 16 || c->n_heads < 1 || c->n_kv_heads < 1 || c->ffn < 16 || c->vocab < 2)
+    return fail(SV_ERR_INVALID_ARG, "model sizes must be positive");
+  if (c->n_heads % c->n_kv_heads) return fail(SV_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(SV_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->d_model % 16 || c->ffn % 16 || (c->n_heads * c->head_dim) % 16)
+    return fail(SV_ERR_UNSUPPORTED, "d_model, ffn and n_heads*head_dim must be multiples of 16");
+  if (c->weight_dtype < SV_F32 || c->weight_dtype > SV_W12) return fail(SV_ERR_INVALID_ARG, "bad weight_dtype");
+  if (c->max_batch < 1 || c->max_batch > kMaxBatch) return fail(SV_ERR_INVALID_ARG, "max_batch must be 1..%d", kMaxBatch);
+  if (c->max_gamma < 0 || c->max_gamma > 63) return fail(SV_ERR_INVALID_ARG, "max_gamma must be 0..63");
+  if (c->page_size < 1 || c->page_size > 256) return fail(SV_ERR_INVALID_ARG, "page_size must be 1..256");
+  if (c->max_seq_len < 1 || c->max_seq_len > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "bad max_seq_len");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(SV_ERR_INVALID_ARG, "bad rms_eps or rope_theta");
+  if ((c->n_heads / c->n_kv_heads) * (c->max_gamma + 1) > 256)
+    return fail(SV_ERR_UNSUPPORTED, "(n_heads / n_kv_heads) * (max_gamma + 1) must be <= 256");
+  return SV_OK;
+}
+
+// ------------------------------------------------------------------ timing
+void timed_begin(sv_model* m, int kc, cudaStream_t s, cudaEvent_t* ev) {
+  *ev = nullptr;
+  if (!m->timing.on) return;
+  cudaEvent_t a, b;
+  if (m->timing.spare.size() >= 2) {
+    a = m->timing.spare.back();
+    m->timing.spare.pop_back();
+    b = m->timing.spare.back();
+    m->timing.spare.pop_back();
+  } else {
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+  }
+  cudaEventRecord(a, s);
+  m->timing.pending[kc].push_back({a, b});
+  ev[0] = a;
+}
+
+void timed_end(sv_model* m, int kc, cudaStream_t s) {
+  if (!m->timing.on) return;
+  cudaEventRecord(m->timing.pending[kc].back().second, s);
+  m->timing.launches[kc]++;
+}
+
+struct Timed {
+  sv_model* m;
+  int kc;
+  cudaStream_t s;
+  Timed(sv_model* m_, int kc_, cudaStream_t s_) : m(m_), kc(kc_), s(s_) {
+    cudaEvent_t e;
+    timed_begin(m, kc, s, &e);
+  }
+  ~Timed() { timed_end(m, kc, s); }
+};
+
+// ------------------------------------------------------------------ GEMM helpers
+GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const void* x) {
+  GemmArgs a;
+  memset(&a, 0, sizeof a);
+  a.wdtype = m->cfg.weight_dtype;
+  a.w = w.data;
+  a.w12_base = w.base;
+  a.w12_ld = w12_row_bytes(K);
+  a.w12_plane = (long long)n_rows * a.w12_ld;
+  a.n_rows = n_rows;
+  a.x = x;
+  a.partials = m->gemm_part;
+  a.counters = m->gemm_cnt;
+  a.epi.act_bf16 = m->act_bf16;
+  a.epi.status = m->status;
+  return a;
+}
+
+// Largest split-K partial buffer and counter array any M in 1..m_max needs for a shape.
+void gemm_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part, size_t* cnt) {
+  for (int M = 1; M <= m_max; ++M) {
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    plan_gemm(a, M, n_units, K, pair, sm);
+    *part = std::max(*part, gemm_partial_floats(a));
+    *cnt = std::max(*cnt, (size_t)a.n_tiles * a.m_tiles);
+  }
+}
+
+sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair, int kc, cudaStream_t s,
+                   const char* what) {
+  plan_gemm(a, M, n_units, K, pair, m->sm_count);
+  Timed t(m, kc, s);
+  SV_CUDA(launch_gemm(a, s), what);
+  return SV_OK;
+}
+
+sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, const sv_kv* kv, const float* probs,
+                     float T, uint64_t seed, const long long* req_ids, int* acc_len, int* next_tok,
+                     cudaStream_t s) {
+  const sv_config& c = m->cfg;
+  if (B < 1 || B > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", B, c.max_batch);
+  if (!tokens || !lens || !kv || !acc_len || !next_tok) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (!kv->k || !kv->v || !kv->page_table || !kv->seq_len || kv->n_pages < 1 || kv->max_pages_per_seq < 1)
+    return fail(SV_ERR_INVALID_ARG, "incomplete sv_kv");
+  if (!(T >= 0.f) || std::isinf(T)) return fail(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (T > 0.f && !probs) return fail(SV_ERR_INVALID_ARG, "draft_probs required when temperature > 0");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!kv->k[l] || !kv->v[l]) return fail(SV_ERR_INVALID_ARG, "NULL KV pool for layer %d", l);
+  static thread_local PrepParams p;
+  p.B = B;
+  p.gamma_stride = c.max_gamma + 1;
+  p.req_row0[0] = 0;
+  for (int r = 0; r < B; ++r) {
+    if (lens[r] < 0 || lens[r] > c.max_gamma)
+      return fail(SV_ERR_INVALID_ARG, "verify_lens[%d] = %d outside 0..%d", r, lens[r], c.max_gamma);
+    p.req_row0[r + 1] = p.req_row0[r] + lens[r] + 1;
+  }
+  const int M = p.req_row0[B];
+  p.M = M;
+  const int d = c.d_model, hd = c.head_dim, nq = c.n_heads * hd, N3 = nqkv(c);
+  const bool keep = T > 0.f || (c.flags & SV_FLAG_KEEP_LOGITS);
+
+  {
+    Timed t(m, SV_KC_NORM, s);
+    SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, m->req_row0, m->w.embed,
+                        m->layers[0].attn_norm, m->h, m->u, d, c.vocab, c.max_seq_len, c.rms_eps, m->act_bf16,
+                        m->status, s),
+            "prep");
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const sv_layer_weights& L = m->layers[l];
+    {  // QKV projection, RoPE, q out, k/v into the page slots
+      GemmArgs a = gemm_base(m, L.wqkv, N3, d, m->u);
+      a.epi.kind = kEpiQkv;
+      a.epi.row_req = m->row_req;
+      a.epi.row_pos = m->row_pos;
+      a.epi.rope = m->rope;
+      a.epi.n_heads = c.n_heads;
+      a.epi.n_kv_heads = c.n_kv_heads;
+      a.epi.head_dim = hd;
+      a.epi.q_out = m->q;
+      a.epi.k_cache = kv->k[l];
+      a.epi.v_cache = kv->v[l];
+      a.epi.page_table = kv->page_table;
+      a.epi.max_pages = kv->max_pages_per_seq;
+      a.epi.page_size = c.page_size;
+      a.epi.n_pages = kv->n_pages;
+      sv_status st = run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm");
+      if (st) return st;
+    }
+    {
+      AttnArgs a;
+      memset(&a, 0, sizeof a);
+      a.q = m->q;
+      a.out = m->ao;
+      a.k_cache = kv->k[l];
+      a.v_cache = kv->v[l];
+      a.page_table = kv->page_table;
+      a.max_pages = kv->max_pages_per_seq;
+      a.page_size = c.page_size;
+      a.n_pages = kv->n_pages;
+      a.seq_len = kv->seq_len;
+      a.req_row0 = m->req_row0;
+      a.n_heads = c.n_heads;
+      a.n_kv_heads = c.n_kv_heads;
+      a.head_dim = hd;
+      plan_attention(a, c.max_batch, c.max_seq_len, c.max_gamma);
+      a.partials = m->attn_part;
+      a.counters = m->attn_cnt;
+      a.status = m->status;
+      a.act_bf16 = m->act_bf16;
+      Timed t(m, SV_KC_ATTENTION, s);
+      SV_CUDA(launch_attention(a, B, m->act_bf16, s), "attention");
+    }
+    {
+      GemmArgs a = gemm_base(m, L.wo, d, nq, m->ao);
+      a.epi.kind = kEpiResid;
+      a.epi.h = m->h;
+      a.epi.ldh = d;
+      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm");
+      if (st) return st;
+    }
+    {
+      Timed t(m, SV_KC_NORM, s);
+      SV_CUDA(launch_rmsnorm(m->h, L.mlp_norm, m->u, M, d, c.rms_eps, m->act_bf16, s), "rmsnorm");
+    }
+    {
+      GemmArgs a = gemm_base(m, L.wgu, 2 * c.ffn, d, m->u);
+      a.ffn = c.ffn;
+      a.epi.kind = kEpiSwiglu;
+      a.epi.act = m->act;
+      a.epi.ffn = c.ffn;
+      sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm");
+      if (st) return st;
+    }
+    {
+      GemmArgs a = gemm_base(m, L.wd, d, c.ffn, m->act);
+      a.epi.kind = kEpiResid;
+      a.epi.h = m->h;
+      a.epi.ldh = d;
+      sv_status st = run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm");
+      if (st) return st;
+    }
+    {
+      const void* g = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
+      Timed t(m, SV_KC_NORM, s);
+      SV_CUDA(launch_rmsnorm(m->h, g, m->u, M, d, c.rms_eps, m->act_bf16, s), "rmsnorm");
+    }
+  }
+  {
+    GemmArgs a = gemm_base(m, m->w.lm_head, c.vocab, d, m->u);
+    a.epi.kind = kEpiLogits;
+    a.epi.logits = keep ? m->logits : nullptr;
+    a.epi.argmax_part = m->argmax_part;
+    a.epi.vocab = c.vocab;
+    sv_status st = run_gemm(m, a, M, c.vocab, d, kPairNone, SV_KC_LM_HEAD, s, "lm head");
+    if (st) return st;
+  }
+  {
+    AcceptArgs a;
+    memset(&a, 0, sizeof a);
+    a.B = B;
+    a.vocab = c.vocab;
+    a.gamma_stride = c.max_gamma + 1;
+    a.tokens = tokens;
+    a.req_row0 = m->req_row0;
+    a.seq_len = kv->seq_len;
+    a.logits = m->logits;
+    a.argmax_part = m->argmax_part;
+    a.n_tiles = m->lm_tiles;
+    a.draft_probs = probs;
+    a.max_gamma = c.max_gamma;
+    a.temperature = T;
+    a.seed = seed;
+    a.request_ids = req_ids;
+    a.accepted_len = acc_len;
+    a.next_token = next_tok;
+    a.status = m->status;
+    Timed t(m, SV_KC_ACCEPT, s);
+    SV_CUDA(launch_accept(a, s), "accept");
+  }
+  m->last_logits = keep;
+  m->last_m = M;
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sv_last_error(void) { return g_err.c_str(); }
+
+int32_t sv_w12_row_bytes(int64_t cols) { return cols < 0 ? 0 : w12_row_bytes(cols); }
+
+sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void* stream, sv_model** out) {
+  if (!out) return fail(SV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  sv_status st = check_config(cfg);
+  if (st) return st;
+  if (!weights || !weights->embed || !weights->final_norm || !weights->lm_head.data || !weights->layers)
+    return fail(SV_ERR_INVALID_ARG, "incomplete sv_weights");
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const sv_layer_weights& L = weights->layers[l];
+    if (!L.attn_norm || !L.mlp_norm || !L.wqkv.data || !L.wo.data || !L.wgu.data || !L.wd.data)
+      return fail(SV_ERR_INVALID_ARG, "incomplete weights for layer %d", l);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  sv_model* m = new sv_model();
+  m->cfg = *cfg;
+  m->w = *weights;
+  m->layers.assign(weights->layers, weights->layers + cfg->n_layers);
+  m->w.layers = nullptr;
+  m->act_bf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
+  m->act_bytes = m->act_bf16 ? 2 : 4;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&m->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  const sv_config& c = *cfg;
+  const int M = c.max_batch * (c.max_gamma + 1);
+  m->m_max = M;
+  m->lm_tiles = (c.vocab + kGemmBN - 1) / kGemmBN;
+  const int d = c.d_model, nq = c.n_heads * c.head_dim;
+  const size_t ab = m->act_bytes;
+#define TRY(x)            \
+  do {                    \
+    st = (x);             \
+    if (st) {             \
+      free_all(m);        \
+      delete m;           \
+      return st;          \
+    }                     \
+  } while (0)
+  TRY(dalloc(m, &m->h, sizeof(float) * M * d));
+  TRY(dalloc(m, &m->u, ab * M * std::max(d, 16)));
+  TRY(dalloc(m, &m->q, ab * M * nq));
+  TRY(dalloc(m, &m->ao, ab * M * nq));
+  TRY(dalloc(m, &m->act, ab * M * c.ffn));
+  TRY(dalloc(m, &m->logits, sizeof(float) * M * (size_t)c.vocab));
+  TRY(dalloc(m, &m->argmax_part, sizeof(float2) * M * (size_t)m->lm_tiles));
+  TRY(dalloc(m, &m->row_req, sizeof(int) * M));
+  TRY(dalloc(m, &m->row_pos, sizeof(int) * M));
+  TRY(dalloc(m, &m->req_row0, sizeof(int) * (c.max_batch + 1)));
+  TRY(dalloc(m, &m->rope, sizeof(float2) * (size_t)c.max_seq_len * (c.head_dim / 2)));
+  size_t part = 0, cnt = 0;
+  gemm_ws_need(m->sm_count, M, nqkv(c), d, kPairNone, &part, &cnt);
+  gemm_ws_need(m->sm_count, M, d, nq, kPairNone, &part, &cnt);
+  gemm_ws_need(m->sm_count, M, c.ffn, d, kPairSwiglu, &part, &cnt);
+  gemm_ws_need(m->sm_count, M, d, c.ffn, kPairNone, &part, &cnt);
+  gemm_ws_need(m->sm_count, M, c.vocab, d, kPairNone, &part, &cnt);
+  TRY(dalloc(m, &m->gemm_part, sizeof(float) * part));
+  TRY(dalloc(m, &m->gemm_cnt, sizeof(unsigned) * cnt));
+  AttnArgs aa;
+  memset(&aa, 0, sizeof aa);
+  aa.n_heads = c.n_heads;
+  aa.n_kv_heads = c.n_kv_heads;
+  aa.head_dim = c.head_dim;
+  plan_attention(aa, c.max_batch, c.max_seq_len, c.max_gamma);
+  TRY(dalloc(m, &m->attn_part, sizeof(float) * attention_partial_floats(aa, c.max_batch)));
+  TRY(dalloc(m, &m->attn_cnt, sizeof(unsigned) * c.max_batch * c.n_kv_heads));
+  TRY(dalloc(m, &m->status, sizeof(unsigned) * 4));
+  TRY(dalloc(m, &m->d_tokens, sizeof(int) * c.max_batch * (c.max_gamma + 1)));
+  TRY(dalloc(m, &m->d_probs, sizeof(float) * (size_t)c.max_batch * std::max(c.max_gamma, 1) * c.vocab));
+  TRY(dalloc(m, &m->d_reqids, sizeof(long long) * c.max_batch));
+  TRY(dalloc(m, &m->d_out, sizeof(int) * 2 * c.max_batch));
+#undef TRY
+  cudaError_t e = cudaMemsetAsync(m->gemm_cnt, 0, sizeof(unsigned) * cnt, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->attn_cnt, 0, sizeof(unsigned) * c.max_batch * c.n_kv_heads, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(unsigned) * 4, s);
+  if (e == cudaSuccess) e = launch_rope_table(m->rope, c.max_seq_len, c.head_dim, c.rope_theta, s);
+  if (e != cudaSuccess) {
+    free_all(m);
+    delete m;
+    return cuda_fail(e, "model init");
+  }
+  *out = m;
+  return SV_OK;
+}
+
+void sv_model_destroy(sv_model* model) {
+  if (!model) return;
+  cudaDeviceSynchronize();
+  free_all(model);
+  delete model;
+}
+
+sv_status sv_verify(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
+                    const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
+                    const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  return run_verify(model, batch, tokens, verify_lens, kv, draft_probs, temperature, seed,
+                    reinterpret_cast<const long long*>(request_ids), accepted_len, next_token,
+                    static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
+                         const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
+                         const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  const sv_config& c = model->cfg;
+  if (batch < 1 || batch > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, c.max_batch);
+  if (!tokens || !accepted_len || !next_token) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (temperature > 0.f && !draft_probs) return fail(SV_ERR_INVALID_ARG, "draft_probs required when temperature > 0");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t tok_bytes = sizeof(int) * batch * (c.max_gamma + 1);
+  SV_CUDA(cudaMemcpyAsync(model->d_tokens, tokens, tok_bytes, cudaMemcpyHostToDevice, s), "copy tokens");
+  const float* dp = nullptr;
+  if (temperature > 0.f) {
+    SV_CUDA(cudaMemcpyAsync(model->d_probs, draft_probs, sizeof(float) * batch * c.max_gamma * (size_t)c.vocab,
+                            cudaMemcpyHostToDevice, s),
+            "copy draft_probs");
+    dp = model->d_probs;
+  }
+  const long long* rid = nullptr;
+  if (request_ids) {
+    SV_CUDA(cudaMemcpyAsync(model->d_reqids, request_ids, sizeof(long long) * batch, cudaMemcpyHostToDevice, s),
+            "copy request_ids");
+    rid = model->d_reqids;
+  }
+  sv_status st = run_verify(model, batch, model->d_tokens, verify_lens, kv, dp, temperature, seed, rid,
+                            model->d_out, model->d_out + c.max_batch, s);
+  if (st) return st;
+  SV_CUDA(cudaMemcpyAsync(accepted_len, model->d_out, sizeof(int) * batch, cudaMemcpyDeviceToHost, s),
+          "copy accepted_len");
+  SV_CUDA(cudaMemcpyAsync(next_token, model->d_out + c.max_batch, sizeof(int) * batch, cudaMemcpyDeviceToHost, s),
+          "copy next_token");
+  SV_CUDA(cudaStreamSynchronize(s), "synchronize");
+  return SV_OK;
+}
+
+sv_status sv_model_logits(sv_model* model, float* dst, int32_t rows, void* stream) {
+  if (!model || !dst) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (!model->last_logits) return fail(SV_ERR_INVALID_ARG, "the last verify kept no logits");
+  if (rows != model->last_m) return fail(SV_ERR_INVALID_ARG, "rows %d != last verify's M %d", rows, model->last_m);
+  SV_CUDA(cudaMemcpyAsync(dst, model->logits, sizeof(float) * rows * (size_t)model->cfg.vocab,
+                          cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)),
+          "copy logits");
+  return SV_OK;
+}
+
+sv_status sv_model_sync_status(sv_model* model, void* stream) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  SV_CUDA(cudaMemcpyAsync(&word, model->status, sizeof word, cudaMemcpyDeviceToHost, s), "read status");
+  SV_CUDA(cudaStreamSynchronize(s), "synchronize");
+  SV_CUDA(cudaMemsetAsync(model->status, 0, sizeof(unsigned), s), "clear status");
+  SV_CUDA(cudaStreamSynchronize(s), "synchronize");
+  if (word)
+    return fail(SV_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s", (word & kStBadToken) ? " token id out of range" : "",
+                (word & kStBadPage) ? " page id out of range" : "", (word & kStTimeout) ? " wait timed out" : "",
+                (word & kStBadPos) ? " a block position reaches max_seq_len" : "");
+  return SV_OK;
+}
+
+sv_status sv_model_set_timing(sv_model* model, int32_t enable) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  Timing& t = model->timing;
+  t.on = enable != 0;
+  for (int k = 0; k < SV_KC_COUNT; ++k) {
+    for (auto& pr : t.pending[k]) {
+      t.spare.push_back(pr.first);
+      t.spare.push_back(pr.second);
+    }
+    t.pending[k].clear();
+    t.ms[k] = 0;
+    t.launches[k] = 0;
+  }
+  return SV_OK;
+}
+
+sv_status sv_model_timing(sv_model* model, double* ms, int64_t* launches) {
+  if (!model || !ms || !launches) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  Timing& t = model->timing;
+  for (int k = 0; k < SV_KC_COUNT; ++k) {
+    for (auto& pr : t.pending[k]) {
+      SV_CUDA(cudaEventSynchronize(pr.second), "event sync");
+      float e = 0.f;
+      SV_CUDA(cudaEventElapsedTime(&e, pr.first, pr.second), "event elapsed");
+      t.ms[k] += e;
+      t.spare.push_back(pr.first);
+      t.spare.push_back(pr.second);
+    }
+    t.pending[k].clear();
+    ms[k] = t.ms[k];
+    launches[k] = t.launches[k];
+  }
+  return SV_OK;
+}
+
+sv_status sv_pack_w12(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t* planes, int32_t* base_out,
+                      int64_t* n_unrepresentable, void* stream) {
+  if (!bf16 || !planes || !base_out || !n_unrepresentable) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (rows < 1 || cols < 1) return fail(SV_ERR_INVALID_ARG, "rows and cols must be positive");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* stats = nullptr;
+  SV_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&stats), 4 * sizeof(unsigned), s), "alloc stats");
+  unsigned h[4] = {255u, 0u, 0u, 0u};
+  sv_status st = SV_OK;
+  cudaError_t e = cudaMemcpyAsync(stats, h, sizeof h, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = launch_w12_scan(bf16, rows * cols, -1, stats, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h, stats, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  long long bad = h[2];
+  const int base = h[0] <= 254u ? static_cast<int>(h[0]) : 1;
+  if (e == cudaSuccess && h[1] > h[0] + 15u && h[0] <= 254u) {
+    unsigned z[4] = {255u, 0u, 0u, 0u};
+    e = cudaMemcpyAsync(stats, z, sizeof z, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = launch_w12_scan(bf16, rows * cols, base, stats, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h, stats, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    bad += h[3];
+  }
+  if (e == cudaSuccess && bad == 0) e = launch_w12_pack(bf16, rows, cols, w12_row_bytes(cols), base, planes, s);
+  cudaFreeAsync(stats, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "pack_w12");
+  *n_unrepresentable = bad;
+  *base_out = base;
+  if (bad) st = fail(SV_ERR_NOT_REPRESENTABLE, "%lld elements are not representable in W12", bad);
+  return st;
+}
+
+sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64_t cols, uint16_t* bf16_out,
+                        void* stream) {
+  if (!planes || !bf16_out) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (rows < 1 || cols < 1 || base < 1 || base > 254) return fail(SV_ERR_INVALID_ARG, "bad sizes or base");
+  SV_CUDA(launch_w12_unpack(planes, base, rows, cols, w12_row_bytes(cols), bf16_out,
+                            static_cast<cudaStream_t>(stream)),
+          "unpack_w12");
+  return SV_OK;
+}
+
+size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K) {
+  (void)wdtype;
+  if (M < 1 || N < 1 || K < 1) return 0;
+  int dev = 0, sm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+  GemmArgs a;
+  memset(&a, 0, sizeof a);
+  plan_gemm(a, M, N, K, kPairNone, sm);
+  const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
+  return cnt + gemm_partial_floats(a) * sizeof(float);
+}
+
+sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t M, float* y,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!w || !w->data || !x || !y || !workspace) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (wdtype < SV_F32 || wdtype > SV_W12) return fail(SV_ERR_INVALID_ARG, "bad wdtype");
+  if (M < 1 || M > 4096 || N < 1 || K < 16 || K % 16) return fail(SV_ERR_INVALID_ARG, "need 1<=M<=4096, N>=1, K%%16==0");
+  if (wdtype == SV_W12 && (w->base < 1 || w->base > 254)) return fail(SV_ERR_INVALID_ARG, "bad W12 base");
+  const size_t need = sv_linear_workspace_bytes(wdtype, M, N, K);
+  if (workspace_bytes < need) return fail(SV_ERR_INVALID_ARG, "workspace %zu < %zu bytes", workspace_bytes, need);
+  int dev = 0, sm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+  GemmArgs a;
+  memset(&a, 0, sizeof a);
+  a.wdtype = wdtype;
+  a.w = w->data;
+  a.w12_base = w->base;
+  a.w12_ld = w12_row_bytes(K);
+  a.w12_plane = (long long)N * a.w12_ld;
+  a.n_rows = N;
+  a.x = x;
+  plan_gemm(a, M, N, K, kPairNone, sm);
+  const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
+  a.counters = static_cast<unsigned*>(workspace);
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + cnt);
+  a.epi.kind = kEpiStore;
+  a.epi.y = y;
+  a.epi.ldy = N;
+  SV_CUDA(launch_gemm(a, static_cast<cudaStream_t>(stream)), "linear");
+  return SV_OK;
+}
+
+sv_status sv_philox_uniform(uint64_t seed, int64_t request_id, int64_t position0, int32_t stream_id, int32_t n,
+                            float* out, void* stream) {
+  if (!out || n < 0) return fail(SV_ERR_INVALID_ARG, "bad arguments");
+  if (n == 0) return SV_OK;
+  SV_CUDA(launch_philox(seed, request_id, position0, stream_id, n, out, static_cast<cudaStream_t>(stream)),
+          "philox");
+  return SV_OK;
+}
+
+}  // extern "C"
