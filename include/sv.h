@@ -60,7 +60,7 @@ typedef enum {
 
 typedef enum {
   SV_F32 = 0,   /* float32 weights, float32 activations and KV cache */
-  SV_BF16 = 1,  /* bf16 weights, bf16 matrix operands, bf16 KV cache, float32 residual stream */
+  SV_BF16 = 1,  /* bf16 weights and KV cache; activations near float32 (hi/lo bf16 operand pairs) */
   SV_W12 = 2    /* W12 matrices (lossless bf16); otherwise as SV_BF16 */
 } sv_dtype;
 
@@ -232,15 +232,19 @@ sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64
 /*
  * Skinny weight-streaming matrix product y[M][N] = x[M][K] W^T with the
  * verify step's own kernels (the path every projection of the step takes):
- * W [N][K] of `wdtype` (F32, BF16 or W12 as in sv_matrix); x device [M][K]
- * float32 for F32 weights, bf16 otherwise; y device float32 [M][N].
- * 1 <= M <= 4096. Uses `workspace` (device, at least sv_linear_workspace_bytes
- * bytes, caller-allocated, zero-filled before first use and left zeroed by
- * every call) for split-K partial sums and tile counters. Asynchronous.
+ * W [N][K] of `wdtype` (F32, BF16 or W12 as in sv_matrix); y device float32
+ * [M][N]; 1 <= M <= 4096, K a multiple of 16.
+ * x (device): for F32 weights float32 [M][K] (x_planes = 1). For BF16/W12
+ * weights bf16: x_planes = 1 gives one plane [M][K]; x_planes = 2 gives a hi
+ * plane [M][K] followed by a lo plane [M][K] and the product uses hi + lo
+ * (the verify step carries its activations this way, near float32 precision).
+ * Uses `workspace` (device, at least sv_linear_workspace_bytes bytes,
+ * caller-allocated, zero-filled before first use and left zeroed by every
+ * call) for split-K partial sums and tile counters. Asynchronous.
  */
 size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K);
-sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t M, float* y,
-                    void* workspace, size_t workspace_bytes, void* stream);
+sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t x_planes,
+                    int32_t M, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Philox4x32-10 uniforms of the verify step: out[i] = u(seed, request_id,
  * position0 + i, stream_id) for i < n, device float32. Asynchronous. */

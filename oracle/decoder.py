@@ -25,10 +25,10 @@ RMSNorm(x) = x / sqrt(mean(x^2) + eps). SiLU(x) = x / (1 + e^-x).
 RoPE at position p rotates the pair (x_i, x_{i+hd/2}) by p * theta^(-2i/hd).
 
 A bf16 target (the pages' targets run in BF16, LFM2.5-DSpark post, "CPU &
-GPU speed") feeds bf16 operands to its matrix products: with act_dtype
-"bf16" the normed activations, the rotated queries, the attention output,
-the SwiGLU product and the final normed state are rounded to bf16 (ties to
-even) before they are multiplied; sums and the residual stream stay float64.
+GPU speed") has bf16 weights and a bf16 KV cache: every key and value is
+rounded to the cache's storage type (ties to even) when it is stored. The
+pages fix no activation precision; activations are not rounded here, so this
+is the exact forward of the stored weights and cache.
 
 With rowwise=True every block row goes through its own matrix-vector
 products in a fixed order, so a row's logits are bit-identical whether it is
@@ -53,7 +53,6 @@ class Config:
     rope_theta: float
     rms_eps: float = 1e-6
     kv_dtype: str = "f32"      # storage type of the KV cache: "f32" or "bf16"
-    act_dtype: str = "f32"     # operand type of the matrix products: "f32" or "bf16"
 
 
 def bf16_bits_to_f64(bits):
@@ -81,10 +80,6 @@ def round_to_cache(x, kv_dtype):
     if kv_dtype == "f32":
         return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
     raise ValueError(kv_dtype)
-
-
-def round_act(x, act_dtype):
-    return round_to_bf16(x) if act_dtype == "bf16" else np.asarray(x, dtype=np.float64)
 
 
 def rmsnorm(x, g, eps):
@@ -182,33 +177,55 @@ def forward_block(cfg, weights, ctx_k, ctx_v, tokens, start_pos, rowwise=True, l
     block's keys/values [M, hkv, hd] as the cache stores them. If layers_out
     is a list, the residual stream after each layer is appended to it.
     """
+    (out,) = forward_blocks(cfg, weights, [(ctx_k, ctx_v, tokens, start_pos)], rowwise, layers_out)
+    return out
+
+
+def forward_blocks(cfg, weights, requests, rowwise=True, layers_out=None):
+    """forward_block for several independent requests, sharing each layer's weights.
+
+    requests: list of (ctx_k, ctx_v, tokens, start_pos); ctx_k / ctx_v only
+    need to support indexing by layer. The layer loop is outermost so a
+    layer's weights are fetched once; each request's arithmetic is exactly
+    that of forward_block (requests never mix). Returns a list of
+    (logits, new_k, new_v).
+    """
     c = cfg
-    tokens = np.asarray(tokens, dtype=np.int64)
-    m = tokens.shape[0]
-    pos = start_pos + np.arange(m)
-    h = weights.embed(tokens)
-    new_k, new_v = [], []
+    state = []
+    for ctx_k, ctx_v, tokens, start_pos in requests:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        m = tokens.shape[0]
+        state.append({"m": m, "pos": start_pos + np.arange(m), "h": weights.embed(tokens), "k": [], "v": [],
+                      "ctx_k": ctx_k, "ctx_v": ctx_v})
     for l in range(c.n_layers):
         p = weights.layer(l)
-        u = round_act(rmsnorm(h, p["attn_norm"], c.rms_eps), c.act_dtype)
-        q = linear(u, p["wq"], rowwise).reshape(m, c.n_heads, c.head_dim)
-        k = linear(u, p["wk"], rowwise).reshape(m, c.n_kv_heads, c.head_dim)
-        v = linear(u, p["wv"], rowwise).reshape(m, c.n_kv_heads, c.head_dim)
-        q = round_act(rope(q, pos, c.rope_theta), c.act_dtype)
-        k = round_to_cache(rope(k, pos, c.rope_theta), c.kv_dtype)
-        v = round_to_cache(v, c.kv_dtype)
-        keys = np.concatenate([ctx_k[l], k], axis=0)
-        vals = np.concatenate([ctx_v[l], v], axis=0)
-        n_ctx = ctx_k[l].shape[0]
-        o = np.stack([attention_row(q[j], keys[:n_ctx + j + 1], vals[:n_ctx + j + 1]) for j in range(m)])
-        o = round_act(o.reshape(m, c.n_heads * c.head_dim), c.act_dtype)
-        h = h + linear(o, p["wo"], rowwise)
-        u = round_act(rmsnorm(h, p["mlp_norm"], c.rms_eps), c.act_dtype)
-        a = round_act(silu(linear(u, p["wg"], rowwise)) * linear(u, p["wu"], rowwise), c.act_dtype)
-        h = h + linear(a, p["wd"], rowwise)
-        new_k.append(k)
-        new_v.append(v)
-        if layers_out is not None:
-            layers_out.append(h.copy())
-    hf = round_act(rmsnorm(h, weights.final_norm(), c.rms_eps), c.act_dtype)
-    return weights.logits(hf, rowwise), new_k, new_v
+        for st in state:
+            m, pos, h = st["m"], st["pos"], st["h"]
+            u = rmsnorm(h, p["attn_norm"], c.rms_eps)
+            q = linear(u, p["wq"], rowwise).reshape(m, c.n_heads, c.head_dim)
+            k = linear(u, p["wk"], rowwise).reshape(m, c.n_kv_heads, c.head_dim)
+            v = linear(u, p["wv"], rowwise).reshape(m, c.n_kv_heads, c.head_dim)
+            q = rope(q, pos, c.rope_theta)
+            k = round_to_cache(rope(k, pos, c.rope_theta), c.kv_dtype)
+            v = round_to_cache(v, c.kv_dtype)
+            ck, cv = st["ctx_k"][l], st["ctx_v"][l]
+            keys = np.concatenate([ck, k], axis=0)
+            vals = np.concatenate([cv, v], axis=0)
+            n_ctx = ck.shape[0]
+            o = np.stack([attention_row(q[j], keys[:n_ctx + j + 1], vals[:n_ctx + j + 1]) for j in range(m)])
+            o = o.reshape(m, c.n_heads * c.head_dim)
+            h = h + linear(o, p["wo"], rowwise)
+            u = rmsnorm(h, p["mlp_norm"], c.rms_eps)
+            a = silu(linear(u, p["wg"], rowwise)) * linear(u, p["wu"], rowwise)
+            h = h + linear(a, p["wd"], rowwise)
+            st["h"] = h
+            st["k"].append(k)
+            st["v"].append(v)
+        if layers_out is not None and len(state) == 1:
+            layers_out.append(state[0]["h"].copy())
+        del p
+    out = []
+    for st in state:
+        hf = rmsnorm(st["h"], weights.final_norm(), c.rms_eps)
+        out.append((weights.logits(hf, rowwise), st["k"], st["v"]))
+    return out

@@ -13,8 +13,7 @@ LOGIT_TOL = {"f32": 1e-4, "bf16": 5e-2}
 
 
 def oracle_config(shape, kind):
-    dt = "f32" if kind == "f32" else "bf16"
-    return Config(**shape, kv_dtype=dt, act_dtype=dt)
+    return Config(**shape, kv_dtype="f32" if kind == "f32" else "bf16")
 
 
 def oracle_weights(shape, hw, kind):
@@ -87,3 +86,46 @@ def judge_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, next_
         if np.min(np.abs(cdf - u_res[k_o] * cdf[-1])) <= CDF_TOL * cdf[-1]:
             return "near_tie"
     return "mismatch"
+
+
+class DeviceLayers:
+    """Per-layer host copies (bf16 patterns) of device weights, fetched when the oracle asks."""
+
+    def __init__(self, wdev):
+        self.w = wdev
+
+    def __getitem__(self, l):
+        return {k: sd.bf16_to_bits(v) for k, v in self.w["layers"][l].items()}
+
+    def __len__(self):
+        return len(self.w["layers"])
+
+
+class DeviceRows:
+    """Row access (index array or slice) to a device bf16 matrix, as host bf16 patterns."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, idx):
+        import torch
+        if isinstance(idx, slice):
+            return sd.bf16_to_bits(self.t[idx])
+        return sd.bf16_to_bits(self.t[torch.as_tensor(np.asarray(idx), device=self.t.device)])
+
+
+class DeviceContext:
+    """ctx[l] = the first C cached positions of one request, layer l, as float64 [C, n_kv, hd]."""
+
+    def __init__(self, pools, table_row, length, page_size):
+        self.pools, self.row, self.n, self.page = pools, table_row, length, page_size
+
+    def __getitem__(self, l):
+        return sd.read_positions(self.pools[l], self.row, np.arange(self.n), self.page).float().cpu().numpy() \
+            .astype(np.float64)
+
+
+def device_oracle_weights(shape, wdev):
+    cfg = oracle_config(shape, "bf16")
+    return cfg, DenseWeights(cfg, DeviceLayers(wdev), DeviceRows(wdev["embed"]), sd.bf16_to_bits(wdev["final_norm"]),
+                             DeviceRows(wdev["lm_head"]), bf16=True)

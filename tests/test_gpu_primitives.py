@@ -87,3 +87,11 @@ def test_linear_matches_float64(kind, m):
         scale = np.sqrt((np.abs(x64) ** 2) @ (np.abs(w64) ** 2).T) + 1e-30
         err = np.abs(y.cpu().numpy() - want) / scale
         assert err.max() < 1e-5, (n, k, err.max())
+        if kind != "f32":   # activations as a hi/lo bf16 pair: the product uses hi + lo
+            xf = torch.from_numpy(x.astype(np.float32)).cuda()
+            hi = xf.to(torch.bfloat16)
+            lo = (xf - hi.float()).to(torch.bfloat16)
+            y2, _ = vs.linear(wdtype, w_dev, torch.stack([hi, lo]), n, k, base=base)
+            x2 = (hi.double() + lo.double()).cpu().numpy()
+            err2 = np.abs(y2.cpu().numpy() - x2 @ w64.T) / scale
+            assert err2.max() < 1e-5, (n, k, err2.max())

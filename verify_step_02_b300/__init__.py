@@ -73,7 +73,7 @@ _SIGS = {
     "sv_pack_w12": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i64), _vp]),
     "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "sv_linear_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
-    "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sv_philox_uniform": (_i32, [_u64, _i64, _i64, _i32, _i32, _vp, _vp]),
     "sv_last_error": (ctypes.c_char_p, []),
 }
@@ -230,16 +230,20 @@ def unpack_w12(planes, base, rows, cols, stream=None):
 
 
 def linear(wdtype, w, x, n, k, base=0, stream=None, workspace=None):
-    """y = x W^T with the verify step's GEMM kernels. Returns (y float32 [M, n], workspace)."""
+    """y = x W^T with the verify step's GEMM kernels. Returns (y float32 [M, n], workspace).
+
+    x: float32 [M, k] for float32 weights; bf16 [M, k], or a hi/lo pair [2, M, k], otherwise.
+    """
     import torch
-    m = int(x.shape[0])
+    planes = 2 if x.dim() == 3 else 1
+    m = int(x.shape[-2])
     need = int(lib.sv_linear_workspace_bytes(int(wdtype), m, int(n), int(k)))
     if workspace is None or workspace.numel() < need:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=x.device)
     y = torch.empty((m, n), dtype=torch.float32, device=x.device)
     mat = Matrix(w.data_ptr(), int(base))
-    _check(lib.sv_linear(int(wdtype), ctypes.byref(mat), int(n), int(k), _ptr(x), m, _ptr(y), _ptr(workspace),
-                         workspace.numel(), _stream(stream)))
+    _check(lib.sv_linear(int(wdtype), ctypes.byref(mat), int(n), int(k), _ptr(x), planes, m, _ptr(y),
+                         _ptr(workspace), workspace.numel(), _stream(stream)))
     return y, workspace
 
 

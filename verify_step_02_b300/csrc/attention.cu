@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
   for (int idx = tid; idx < R * hd; idx += blockDim.x) {
     const int rho = idx / hd, d = idx - rho * hd;
     const int j = rho / group, g = rho - j * group;
-    Qs[idx] = load_act(a.q, (long long)(row0 + j) * nq + (h * group + g) * hd + d, a.act_bf16) * scale;
+    Qs[idx] = a.q[(long long)(row0 + j) * nq + (h * group + g) * hd + d] * scale;
     Os[idx] = 0.f;
   }
   for (int rho = tid; rho < R; rho += blockDim.x) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
         const float mc = __ldcg(base + c * cstride + rho * stride);
         if (mc != -INFINITY) o += __ldcg(base + c * cstride + rho * stride + 2 + d) * expf(mc - M);
       }
-      store_act(a.out, orow + d, o / L, a.act_bf16);
+      store_x(a.out, a.out_plane, orow + d, o / L, a.x_pair);
     }
   }
   if (tid == 0) a.counters[item] = 0u;

@@ -25,6 +25,26 @@ __device__ __forceinline__ float load_act(const void* base, long long idx, int a
   return reinterpret_cast<const float*>(base)[idx];
 }
 
+// x tensors: float32, or hi/lo bf16 planes (hi at i, lo at plane + i).
+__device__ __forceinline__ void store_x(void* base, long long plane, long long idx, float v, int pair) {
+  if (pair) {
+    const uint16_t hi = f32_to_bf16_bits(v);
+    const uint16_t lo = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
+    reinterpret_cast<uint16_t*>(base)[idx] = hi;
+    reinterpret_cast<uint16_t*>(base)[plane + idx] = lo;
+  } else {
+    reinterpret_cast<float*>(base)[idx] = v;
+  }
+}
+
+// kind 0: float32; 1: one bf16 plane; 2: hi/lo bf16 planes (see XKind).
+__device__ __forceinline__ float load_x(const void* base, long long plane, long long idx, int kind) {
+  if (kind == 0) return reinterpret_cast<const float*>(base)[idx];
+  const uint16_t* p = reinterpret_cast<const uint16_t*>(base);
+  const float hi = bf16_bits_to_f32(p[idx]);
+  return kind == 2 ? hi + bf16_bits_to_f32(p[plane + idx]) : hi;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

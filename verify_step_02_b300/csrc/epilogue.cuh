@@ -45,7 +45,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
       const int f = nt * HB + t;
       if (f >= e.ffn) continue;
       const float g = ys[t * ldys + c], u = ys[(t + HB) * ldys + c];
-      store_act(e.act, (long long)(m0 + c) * e.ffn + f, silu(g) * u, e.act_bf16);
+      store_x(e.act, e.act_plane, (long long)(m0 + c) * e.ffn + f, silu(g) * u, e.x_pair);
     }
   } else if (e.kind == kEpiQkv) {
     const int hd = e.head_dim, half = hd >> 1;
@@ -71,7 +71,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
         }
       }
       if (n < nq) {
-        store_act(e.q_out, (long long)m * nq + n, v, e.act_bf16);
+        e.q_out[(long long)m * nq + n] = v;
       } else {
         const bool is_k = head < e.n_heads + e.n_kv_heads;
         const int kvh = head - e.n_heads - (is_k ? 0 : e.n_kv_heads);
@@ -84,7 +84,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
         }
         const long long off = (((long long)page * e.n_kv_heads + kvh) * e.page_size + (pos - pidx * e.page_size)) *
                                   hd + i;
-        store_act(is_k ? e.k_cache : e.v_cache, off, v, e.act_bf16);
+        store_act(is_k ? e.k_cache : e.v_cache, off, v, e.kv_bf16);
       }
     }
   } else if (e.kind == kEpiLogits) {

@@ -5,7 +5,8 @@
 // path. One CTA computes a 128-row x 32-token tile over one K range; the W
 // tile is converted to float32 once into shared memory (W12 rebuilt from its
 // three nibble planes to bf16 on the way, SpecPilot digest, "Reasons") and
-// every thread then runs an 8 x 2 register-blocked FMA loop. K is split
+// every thread then runs an 8 x 2 register-blocked FMA loop. Activations are
+// read as float32 (a hi/lo pair is summed on load). K is split
 // across CTAs until the grid covers the GPU; the last split of a tile reduces
 // the partials in a fixed order and runs the projection's epilogue.
 #include "epilogue.cuh"
@@ -111,9 +112,7 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
       for (int i = 0; i < 4; ++i) {
         float xv = 0.f;
         if (xm < a.M && k + i < kend) {
-          const long long off = (long long)xm * a.K + k + i;
-          xv = WT == SV_F32 ? reinterpret_cast<const float*>(a.x)[off]
-                            : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(a.x)[off] << 16);
+          xv = load_x(a.x, a.x_plane, (long long)xm * a.K + k + i, a.x_kind);
         }
         Xs[xkk + i][xtok] = xv;
       }

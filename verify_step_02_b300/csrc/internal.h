@@ -31,9 +31,19 @@ enum EpiKind : int {
 // gate and up value of a feature in the same tile.
 enum PairKind : int { kPairNone = 0, kPairSwiglu = 1 };
 
+enum XKind : int { kXF32 = 0, kXBf16 = 1, kXPair = 2 };
+
+// Activations that feed a matrix product ("x tensors": the normed residual,
+// the attention output, the SwiGLU product) are float32 for float32 models.
+// For bf16/W12 models they are a pair of bf16 planes, hi = bf16(x) and
+// lo = bf16(x - hi), so that x = hi + lo to about 16 significant bits: the
+// tensor-core product then runs on bf16 operands (hi and lo rows of one B
+// tile) while keeping the activations near float32. A pair tensor stores hi
+// at element i and lo at element plane + i.
 struct Epi {
   int kind;
-  int act_bf16;            // activations written as bf16 (else float32)
+  int x_pair;              // x outputs (SwiGLU product) as hi/lo pairs (else float32)
+  int kv_bf16;             // KV cache stored as bf16 (else float32)
   // kEpiStore
   float* y;
   int ldy;
@@ -42,7 +52,7 @@ struct Epi {
   const int* row_pos;      // [M] absolute position of each row
   const float2* rope;      // [max_seq_len][head_dim/2] (cos, sin)
   int n_heads, n_kv_heads, head_dim;
-  void* q_out;             // [M][n_heads*head_dim]
+  float* q_out;            // [M][n_heads*head_dim], float32
   void* k_cache;           // layer's K pool [n_pages][n_kv][page_size][head_dim]
   void* v_cache;
   const int* page_table;
@@ -55,6 +65,7 @@ struct Epi {
   int ldh;
   // kEpiSwiglu
   void* act;
+  long long act_plane;     // element offset of the lo plane (x_pair)
   int ffn;
   // kEpiLogits
   float* logits;           // [M][vocab] or nullptr
@@ -70,7 +81,9 @@ struct GemmArgs {
   long long w12_plane;     // W12 bytes per plane (rows * ld)
   int n_rows;              // rows of W
   int K;
-  const void* x;           // activations [M][K]: float32 for SV_F32, bf16 otherwise
+  const void* x;           // activations [M][K]
+  int x_kind;              // kXF32, kXBf16 (one bf16 plane) or kXPair (hi/lo bf16 planes)
+  long long x_plane;       // element offset of the lo plane (kXPair)
   int M;
   int pair;                // PairKind
   int ffn;                 // kPairSwiglu: gate rows [0, ffn), up rows [ffn, 2 ffn)
@@ -84,8 +97,9 @@ struct GemmArgs {
 };
 
 struct AttnArgs {
-  const void* q;           // [M][n_heads*head_dim], act dtype
-  void* out;               // [M][n_heads*head_dim], act dtype
+  const float* q;          // [M][n_heads*head_dim], float32
+  void* out;               // [M][n_heads*head_dim], float32 or hi/lo pair
+  long long out_plane;     // element offset of the lo plane (x_pair)
   const void* k_cache;
   const void* v_cache;
   const int* page_table;
@@ -102,7 +116,8 @@ struct AttnArgs {
   float* partials;         // [B*n_kv*max_chunks][max_rows][head_dim + 2]
   unsigned* counters;      // [B*n_kv]
   unsigned* status;
-  int act_bf16;
+  int x_pair;
+  int kv_bf16;
 };
 
 struct AcceptArgs {
@@ -139,11 +154,13 @@ size_t gemm_partial_floats(const GemmArgs& a);
 cudaError_t launch_attention(const AttnArgs& a, int B, int kv_dtype_bf16, cudaStream_t s);
 void plan_attention(AttnArgs& a, int max_batch, int max_seq_len, int max_gamma);
 size_t attention_partial_floats(const AttnArgs& a, int max_batch);
+// prep / rmsnorm: weights_bf16 selects the embedding and gain type; x_pair the u output form.
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
-                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, int d, int vocab,
-                        int max_seq_len, float eps, int act_bf16, unsigned* status, cudaStream_t s);
-cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, int M, int d, float eps, int act_bf16,
-                           cudaStream_t s);
+                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
+                        int d, int vocab, int max_seq_len, float eps, int weights_bf16, int x_pair, unsigned* status,
+                        cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, long long u_plane, int M, int d, float eps,
+                           int weights_bf16, int x_pair, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s);

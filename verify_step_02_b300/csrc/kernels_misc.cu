@@ -8,17 +8,15 @@ namespace {
 
 constexpr int kNormThreads = 256;
 
-__device__ __forceinline__ float load_gain(const void* g, int k, int act_bf16) { return load_act(g, k, act_bf16); }
-
 // Normalize h[m] (float32, d) into u[m]: u = h / sqrt(mean(h^2) + eps) * g.
-__device__ __forceinline__ void norm_row(const float* hrow, const void* gain, void* u, long long m, int d, float eps,
-                                         int act_bf16, float* red) {
+__device__ __forceinline__ void norm_row(const float* hrow, const void* gain, void* u, long long u_plane, long long m,
+                                         int d, float eps, int weights_bf16, int x_pair, float* red) {
   float ss = 0.f;
   for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(hrow[k], hrow[k], ss);
   const float tot = block_sum(ss, red);
   const float rstd = rsqrtf(tot / static_cast<float>(d) + eps);
   for (int k = threadIdx.x; k < d; k += blockDim.x)
-    store_act(u, m * d + k, hrow[k] * rstd * load_gain(gain, k, act_bf16), act_bf16);
+    store_x(u, u_plane, m * d + k, hrow[k] * rstd * load_act(gain, k, weights_bf16), x_pair);
 }
 
 // One CTA per block row: find the row's request and offset, gather the token's
@@ -26,8 +24,9 @@ __device__ __forceinline__ void norm_row(const float* hrow, const void* gain, vo
 __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, const int* tokens, const int* seq_len,
                                                             int* row_req, int* row_pos, int* req_row0_dev,
                                                             const void* embed, const void* gain, float* h, void* u,
-                                                            int d, int vocab, int max_seq_len, float eps,
-                                                            int act_bf16, unsigned* status) {
+                                                            long long u_plane, int d, int vocab, int max_seq_len,
+                                                            float eps, int weights_bf16, int x_pair,
+                                                            unsigned* status) {
   __shared__ float red[32];
   const int m = blockIdx.x;
   if (m == 0)
@@ -55,16 +54,17 @@ __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, 
     row_pos[m] = pos;
   }
   float* hrow = h + (long long)m * d;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) hrow[k] = load_act(embed, (long long)tok * d + k, act_bf16);
+  for (int k = threadIdx.x; k < d; k += blockDim.x) hrow[k] = load_act(embed, (long long)tok * d + k, weights_bf16);
   __syncthreads();
-  norm_row(hrow, gain, u, m, d, eps, act_bf16, red);
+  norm_row(hrow, gain, u, u_plane, m, d, eps, weights_bf16, x_pair, red);
 }
 
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* h, const void* gain, void* u, int d,
-                                                               float eps, int act_bf16) {
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* h, const void* gain, void* u,
+                                                               long long u_plane, int d, float eps, int weights_bf16,
+                                                               int x_pair) {
   __shared__ float red[32];
   const int m = blockIdx.x;
-  norm_row(h + (long long)m * d, gain, u, m, d, eps, act_bf16, red);
+  norm_row(h + (long long)m * d, gain, u, u_plane, m, d, eps, weights_bf16, x_pair, red);
 }
 
 // ------------------------------------------------------------------ acceptance
@@ -285,16 +285,17 @@ __global__ void philox_kernel(unsigned long long seed, long long req, long long 
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
-                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, int d, int vocab,
-                        int max_seq_len, float eps, int act_bf16, unsigned* status, cudaStream_t s) {
-  prep_kernel<<<p.M, kNormThreads, 0, s>>>(p, tokens, seq_len, row_req, row_pos, req_row0_dev, embed, gain, h, u, d,
-                                           vocab, max_seq_len, eps, act_bf16, status);
+                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
+                        int d, int vocab, int max_seq_len, float eps, int weights_bf16, int x_pair, unsigned* status,
+                        cudaStream_t s) {
+  prep_kernel<<<p.M, kNormThreads, 0, s>>>(p, tokens, seq_len, row_req, row_pos, req_row0_dev, embed, gain, h, u,
+                                           u_plane, d, vocab, max_seq_len, eps, weights_bf16, x_pair, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, int M, int d, float eps, int act_bf16,
-                           cudaStream_t s) {
-  rmsnorm_kernel<<<M, kNormThreads, 0, s>>>(h, gain, u, d, eps, act_bf16);
+cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, long long u_plane, int M, int d, float eps,
+                           int weights_bf16, int x_pair, cudaStream_t s) {
+  rmsnorm_kernel<<<M, kNormThreads, 0, s>>>(h, gain, u, u_plane, d, eps, weights_bf16, x_pair);
   return cudaGetLastError();
 }
 

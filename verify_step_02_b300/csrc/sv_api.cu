@@ -53,8 +53,8 @@ struct sv_model {
   sv_config cfg;
   sv_weights w;
   std::vector<sv_layer_weights> layers;
-  int act_bf16 = 0;
-  int act_bytes = 4;
+  int wbf16 = 0;    // embedding, gains, KV cache in bf16 (else float32)
+  int x_pair = 0;   // x tensors as hi/lo bf16 pairs (else float32)
   int sm_count = 148;
   int m_max = 0;
   int lm_tiles = 0;
@@ -64,6 +64,7 @@ struct sv_model {
   void* q = nullptr;
   void* ao = nullptr;
   void* act = nullptr;
+  long long u_plane = 0, ao_plane = 0, act_plane = 0;  // lo-plane offsets of the x tensors
   float* logits = nullptr;
   float2* argmax_part = nullptr;
   int* row_req = nullptr;
@@ -168,7 +169,7 @@ struct Timed {
 };
 
 // ------------------------------------------------------------------ GEMM helpers
-GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const void* x) {
+GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const void* x, long long x_plane) {
   GemmArgs a;
   memset(&a, 0, sizeof a);
   a.wdtype = m->cfg.weight_dtype;
@@ -178,9 +179,12 @@ GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const voi
   a.w12_plane = (long long)n_rows * a.w12_ld;
   a.n_rows = n_rows;
   a.x = x;
+  a.x_plane = x_plane;
   a.partials = m->gemm_part;
   a.counters = m->gemm_cnt;
-  a.epi.act_bf16 = m->act_bf16;
+  a.x_kind = m->x_pair ? kXPair : kXF32;
+  a.epi.x_pair = m->x_pair;
+  a.epi.kv_bf16 = m->wbf16;
   a.epi.status = m->status;
   return a;
 }
@@ -233,14 +237,14 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   {
     Timed t(m, SV_KC_NORM, s);
     SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, m->req_row0, m->w.embed,
-                        m->layers[0].attn_norm, m->h, m->u, d, c.vocab, c.max_seq_len, c.rms_eps, m->act_bf16,
-                        m->status, s),
+                        m->layers[0].attn_norm, m->h, m->u, m->u_plane, d, c.vocab, c.max_seq_len, c.rms_eps,
+                        m->wbf16, m->x_pair, m->status, s),
             "prep");
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const sv_layer_weights& L = m->layers[l];
     {  // QKV projection, RoPE, q out, k/v into the page slots
-      GemmArgs a = gemm_base(m, L.wqkv, N3, d, m->u);
+      GemmArgs a = gemm_base(m, L.wqkv, N3, d, m->u, m->u_plane);
       a.epi.kind = kEpiQkv;
       a.epi.row_req = m->row_req;
       a.epi.row_pos = m->row_pos;
@@ -248,7 +252,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.n_heads = c.n_heads;
       a.epi.n_kv_heads = c.n_kv_heads;
       a.epi.head_dim = hd;
-      a.epi.q_out = m->q;
+      a.epi.q_out = static_cast<float*>(m->q);
       a.epi.k_cache = kv->k[l];
       a.epi.v_cache = kv->v[l];
       a.epi.page_table = kv->page_table;
@@ -261,8 +265,9 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     {
       AttnArgs a;
       memset(&a, 0, sizeof a);
-      a.q = m->q;
+      a.q = static_cast<const float*>(m->q);
       a.out = m->ao;
+      a.out_plane = m->ao_plane;
       a.k_cache = kv->k[l];
       a.v_cache = kv->v[l];
       a.page_table = kv->page_table;
@@ -278,12 +283,13 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.partials = m->attn_part;
       a.counters = m->attn_cnt;
       a.status = m->status;
-      a.act_bf16 = m->act_bf16;
+      a.x_pair = m->x_pair;
+      a.kv_bf16 = m->wbf16;
       Timed t(m, SV_KC_ATTENTION, s);
-      SV_CUDA(launch_attention(a, B, m->act_bf16, s), "attention");
+      SV_CUDA(launch_attention(a, B, m->wbf16, s), "attention");
     }
     {
-      GemmArgs a = gemm_base(m, L.wo, d, nq, m->ao);
+      GemmArgs a = gemm_base(m, L.wo, d, nq, m->ao, m->ao_plane);
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
@@ -292,19 +298,21 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     }
     {
       Timed t(m, SV_KC_NORM, s);
-      SV_CUDA(launch_rmsnorm(m->h, L.mlp_norm, m->u, M, d, c.rms_eps, m->act_bf16, s), "rmsnorm");
+      SV_CUDA(launch_rmsnorm(m->h, L.mlp_norm, m->u, m->u_plane, M, d, c.rms_eps, m->wbf16, m->x_pair, s),
+              "rmsnorm");
     }
     {
-      GemmArgs a = gemm_base(m, L.wgu, 2 * c.ffn, d, m->u);
+      GemmArgs a = gemm_base(m, L.wgu, 2 * c.ffn, d, m->u, m->u_plane);
       a.ffn = c.ffn;
       a.epi.kind = kEpiSwiglu;
       a.epi.act = m->act;
+      a.epi.act_plane = m->act_plane;
       a.epi.ffn = c.ffn;
       sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm");
       if (st) return st;
     }
     {
-      GemmArgs a = gemm_base(m, L.wd, d, c.ffn, m->act);
+      GemmArgs a = gemm_base(m, L.wd, d, c.ffn, m->act, m->act_plane);
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
@@ -314,11 +322,11 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     {
       const void* g = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
       Timed t(m, SV_KC_NORM, s);
-      SV_CUDA(launch_rmsnorm(m->h, g, m->u, M, d, c.rms_eps, m->act_bf16, s), "rmsnorm");
+      SV_CUDA(launch_rmsnorm(m->h, g, m->u, m->u_plane, M, d, c.rms_eps, m->wbf16, m->x_pair, s), "rmsnorm");
     }
   }
   {
-    GemmArgs a = gemm_base(m, m->w.lm_head, c.vocab, d, m->u);
+    GemmArgs a = gemm_base(m, m->w.lm_head, c.vocab, d, m->u, m->u_plane);
     a.epi.kind = kEpiLogits;
     a.epi.logits = keep ? m->logits : nullptr;
     a.epi.argmax_part = m->argmax_part;
@@ -380,8 +388,8 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->w = *weights;
   m->layers.assign(weights->layers, weights->layers + cfg->n_layers);
   m->w.layers = nullptr;
-  m->act_bf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
-  m->act_bytes = m->act_bf16 ? 2 : 4;
+  m->wbf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
+  m->x_pair = m->wbf16;
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&m->sm_count, cudaDevAttrMultiProcessorCount, dev);
@@ -390,7 +398,11 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->m_max = M;
   m->lm_tiles = (c.vocab + kGemmBN - 1) / kGemmBN;
   const int d = c.d_model, nq = c.n_heads * c.head_dim;
-  const size_t ab = m->act_bytes;
+  // x tensors: float32, or two bf16 planes of M rows each (the same bytes)
+  const size_t ab = 4;
+  m->u_plane = m->x_pair ? (long long)M * d : 0;
+  m->ao_plane = m->x_pair ? (long long)M * nq : 0;
+  m->act_plane = m->x_pair ? (long long)M * c.ffn : 0;
 #define TRY(x)            \
   do {                    \
     st = (x);             \
@@ -402,7 +414,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   } while (0)
   TRY(dalloc(m, &m->h, sizeof(float) * M * d));
   TRY(dalloc(m, &m->u, ab * M * std::max(d, 16)));
-  TRY(dalloc(m, &m->q, ab * M * nq));
+  TRY(dalloc(m, &m->q, sizeof(float) * M * nq));
   TRY(dalloc(m, &m->ao, ab * M * nq));
   TRY(dalloc(m, &m->act, ab * M * c.ffn));
   TRY(dalloc(m, &m->logits, sizeof(float) * M * (size_t)c.vocab));
@@ -613,10 +625,12 @@ size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K
   return cnt + gemm_partial_floats(a) * sizeof(float);
 }
 
-sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t M, float* y,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t x_planes,
+                    int32_t M, float* y, void* workspace, size_t workspace_bytes, void* stream) {
   if (!w || !w->data || !x || !y || !workspace) return fail(SV_ERR_INVALID_ARG, "NULL argument");
   if (wdtype < SV_F32 || wdtype > SV_W12) return fail(SV_ERR_INVALID_ARG, "bad wdtype");
+  if (x_planes != 1 && !(x_planes == 2 && wdtype != SV_F32))
+    return fail(SV_ERR_INVALID_ARG, "x_planes must be 1, or 2 for bf16/W12 weights");
   if (M < 1 || M > 4096 || N < 1 || K < 16 || K % 16) return fail(SV_ERR_INVALID_ARG, "need 1<=M<=4096, N>=1, K%%16==0");
   if (wdtype == SV_W12 && (w->base < 1 || w->base > 254)) return fail(SV_ERR_INVALID_ARG, "bad W12 base");
   const size_t need = sv_linear_workspace_bytes(wdtype, M, N, K);
@@ -633,6 +647,8 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   a.w12_plane = (long long)N * a.w12_ld;
   a.n_rows = N;
   a.x = x;
+  a.x_kind = wdtype == SV_F32 ? kXF32 : (x_planes == 2 ? kXPair : kXBf16);
+  a.x_plane = (long long)M * K;
   plan_gemm(a, M, N, K, kPairNone, sm);
   const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
   a.counters = static_cast<unsigned*>(workspace);
