@@ -246,6 +246,31 @@ size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K
 sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t x_planes,
                     int32_t M, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sv_linear without any device allocation. The pages have no counterpart to
+ * this entry point: it exists for callers that must not allocate device
+ * memory while they run (cudaMalloc can synchronize the whole device and
+ * stall other streams, and some hosts, such as inference servers with fixed
+ * memory pools or plugins whose host owns every allocation, forbid it).
+ * Same arguments and result as sv_linear, without the workspace: the split-K
+ * scratch (partial tiles and tile counters) lives in a 16 MiB static device
+ * array inside the library, which every GPU that loads the library keeps
+ * until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current. Make that first call
+ *     before any stream capture.
+ *   - A shape whose scratch would exceed 16 MiB is rejected with
+ *     SV_ERR_INVALID_ARG; sv_last_error() gives the bytes it would need.
+ *   - Each call clears the tile counters (cudaMemsetAsync on `stream`)
+ *     before its launch. No call allocates or frees memory.
+ *   - All calls share the one array, and it keeps the last call's contents:
+ *     calls whose work overlaps on the GPU (several streams, or several host
+ *     threads) race on it and produce wrong results. Serialize them, for
+ *     example on one stream.
+ */
+sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x,
+                            int32_t x_planes, int32_t M, float* y, void* stream);
+
 /* Philox4x32-10 uniforms of the verify step: out[i] = u(seed, request_id,
  * position0 + i, stream_id) for i < n, device float32. Asynchronous. */
 sv_status sv_philox_uniform(uint64_t seed, int64_t request_id, int64_t position0, int32_t stream_id, int32_t n,

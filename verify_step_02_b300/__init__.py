@@ -74,6 +74,7 @@ _SIGS = {
     "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "sv_linear_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "sv_linear_noalloc": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp]),
     "sv_philox_uniform": (_i32, [_u64, _i64, _i64, _i32, _i32, _vp, _vp]),
     "sv_last_error": (ctypes.c_char_p, []),
 }

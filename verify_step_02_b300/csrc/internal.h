@@ -147,6 +147,9 @@ struct PrepParams {
   int req_row0[kMaxBatch + 1];
 };
 
+// Set the message sv_last_error() returns on this thread.
+void record_error(const char* msg);
+
 // ---- launchers (defined in the .cu files) ----
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 void plan_gemm(GemmArgs& a, int M, int n_rows_or_pairs, int K, int pair, int sm_count);

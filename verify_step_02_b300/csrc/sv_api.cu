@@ -49,6 +49,8 @@ struct Timing {
 
 }  // namespace
 
+void sv::record_error(const char* msg) { g_err = msg; }
+
 struct sv_model {
   sv_config cfg;
   sv_weights w;
