@@ -7,5 +7,11 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
+    # the binding loads libsv.so at import; build it (incrementally) before collection
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_sv_build", os.path.join(ROOT, "verify_step_02_b300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300) and the built library")
     config.addinivalue_line("markers", "slow: full-size workload; takes minutes")
