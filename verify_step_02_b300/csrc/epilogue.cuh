@@ -20,11 +20,11 @@ namespace sv {
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // ys: tile values, element (t, c) at ys[t * ldys + c] for tile row t < kGemmBN and
-// token c < mcount (global token m0 + c). nt: the weight tile index.
+// token c < mcount (global token m0 + c). nt: the weight tile index. The tile
+// is shared by threads tid = 0 .. nthr-1 (nthr a multiple of 32).
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const float* ys, int ldys, int m0,
-                                              int mcount) {
+                                              int mcount, int tid, int nthr) {
   const Epi& e = a.epi;
-  const int tid = threadIdx.x, nthr = blockDim.x;
   constexpr int BN = kGemmBN;
   if (e.kind == kEpiStore || e.kind == kEpiResid) {
     for (int idx = tid; idx < BN * mcount; idx += nthr) {

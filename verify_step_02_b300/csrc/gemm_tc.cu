@@ -1,0 +1,385 @@
+// Weight-streaming skinny GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// y[m][n] = x[m] . W[n] for bf16 weights W [rows][K] and bf16 activations, one
+// plane or a hi/lo pair (x = hi + lo: both planes are multiplied into the same
+// float32 accumulator). The verify block has M = sum(L_r + 1) rows, a few to a
+// few hundred, so W is the big operand: it is the MMA's A operand (128 weight
+// rows per tile, the MMA's M), and the block's tokens are its N (32 .. 256
+// columns). Every weight byte is read from HBM exactly once per launch.
+//
+// Work split ("stream-K"): the launch has P <= #SM CTAs and U = tiles x K
+// blocks of 64 units of work; CTA c takes units [c U / P, (c+1) U / P), so
+// every SM streams the same number of weight bytes. A tile whose K range is
+// shared by several CTAs is finished by the last of them to arrive, which sums
+// the partial tiles in CTA order (a fixed order: results do not depend on
+// timing) and runs the projection's epilogue. No CTA waits on another.
+//
+// Roles inside a CTA (256 threads):
+//   warp 0     one thread issues TMA loads of the weight tile (two 64-row
+//              boxes) and the x tile (32-row boxes per plane) into an S-stage
+//              shared-memory ring;
+//   warp 1     allocates the TMEM accumulators (two buffers of NT columns) and
+//              one thread issues tcgen05.mma (M 128, N NT, K 16) per stage;
+//   warps 4-7  read finished accumulators out of TMEM (warp w reads lanes
+//              32 (w % 4) ..), and write partial tiles or run the epilogue.
+// Every wait is bounded; a wait that runs out sets the status word's timeout
+// bit and the whole CTA winds down (waits for its copies and MMAs in flight,
+// frees TMEM, returns).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace sv {
+namespace {
+
+using namespace tc;
+
+constexpr int kTcThreads = 256;
+constexpr int kYsLd = 33;                       // Ys row stride (floats)
+constexpr int kABytes = kGemmBN * 128;          // weight tile of one stage: 128 rows x 64 bf16
+constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s
+constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
+constexpr int kSmemBudget = 225 * 1024;
+
+__host__ __device__ constexpr int stage_bytes(int nt, bool pair) { return kABytes + nt * 128 * (pair ? 2 : 1); }
+
+__host__ __device__ constexpr uint32_t tmem_cols(int nt) {
+  return 2 * nt <= 32 ? 32u : 2 * nt <= 64 ? 64u : 2 * nt <= 128 ? 128u : 2 * nt <= 256 ? 256u : 512u;
+}
+
+// First CTA whose unit range contains unit x: the largest c with floor(c U / P) <= x.
+__device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
+  return static_cast<int>(((x + 1) * P + U - 1) / U - 1);
+}
+
+template <int NT, bool PAIR>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
+                   const GemmArgs a) {
+  constexpr int BX = NT * 128;  // bytes of one x plane per stage
+  constexpr int STAGE = stage_bytes(NT, PAIR);
+  constexpr uint32_t TCOLS = tmem_cols(NT);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.tc_stages;
+  float* Ys = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(Ys + kGemmBN * kYsLd);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = a.grid_p, c = blockIdx.x;
+  const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
+  const long long u0 = c * U / P, u1 = (c + 1) * U / P;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(acc_full + i, 1);
+      mbar_init(acc_empty + i, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmw);
+    prefetch_tmap(&tmx);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TCOLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (long long u = u0; u < u1; ++u) {
+        const long long t = u / a.kb;
+        const int kb = static_cast<int>(u - t * a.kb);
+        const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
+        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
+        uint8_t* sa = smem + static_cast<size_t>(stage) * STAGE;
+        uint8_t* sb = sa + kABytes;
+        mbar_arrive_expect_tx(full + stage, STAGE);
+        const int k = kb * 64;
+        const int r0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
+        const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : r0 + kGemmBN / 2;
+        tma_load_2d(sa, &tmw, k, r0, full + stage, pw);
+        tma_load_2d(sa + kABytes / 2, &tmw, k, r1, full + stage, pw);
+#pragma unroll
+        for (int j = 0; j < NT / 32; ++j) {
+          tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, full + stage, px);
+          if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, full + stage, px);
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*abort_flag) {
+        // let the copies still in flight land before the CTA's shared memory goes away
+        volatile int never = 0;
+        const long long n = issued < S ? issued : S;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;  // issue number
+          mbar_wait(full + (q % S), static_cast<uint32_t>((q / S) & 1), &never, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBN, NT);
+      int stage = 0, seg = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1 && ok;) {
+        const long long t = u / a.kb;
+        const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+        const int b = seg & 1;
+        if (!mbar_wait(acc_empty + b, ((seg >> 1) & 1) ^ 1u, abort_flag, kWaitNs)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * NT;
+        for (long long v = u; v < uend; ++v) {
+          if (!mbar_wait(full + stage, phase, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * STAGE), sb = sa + kABytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = smem_desc_sw128(sa + k * 32);
+            mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || k > 0) ? 1u : 0u);
+            if (PAIR) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
+          }
+          mma_commit(empty + stage);  // frees the stage once these MMAs have read it
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(acc_full + b);
+        ++seg;
+        u = uend;
+      }
+      // every MMA issued above has completed once `drain` flips
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, kDrainNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 128;  // tile row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int slot0_tile = static_cast<int>(u0 / a.kb);
+    int seg = 0;
+    for (long long u = u0; u < u1;) {
+      const long long t = u / a.kb;
+      const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+      const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
+      const int b = seg & 1;
+      // one thread waits and broadcasts, so all 128 threads agree on the outcome
+      if (et == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
+      named_bar(1, 128);
+      const bool ok = *s_flag != 0;
+      named_bar(1, 128);
+      if (!ok) break;
+      tc_fence_after();
+      const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
+      const bool alone = cf == cl;
+      const int m_base = mt * NT;
+      const int mtot = a.M - m_base < NT ? a.M - m_base : NT;
+      const int slot = static_cast<int>(t) == slot0_tile ? 0 : 1;
+      float* mine = a.partials + ((static_cast<size_t>(c) * 2 + slot) * kGemmBN + et) * NT;
+      for (int ch = 0; ch * 32 < mtot; ++ch) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + b * NT + ch * 32, v);
+        if (alone) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
+          named_bar(1, 128);
+          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128);
+          named_bar(1, 128);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(mine + ch * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty + b);
+      if (!alone) {
+        __threadfence();
+        named_bar(1, 128);
+        if (et == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
+        named_bar(1, 128);
+        const bool last = *s_flag != 0;
+        named_bar(1, 128);
+        if (last) {
+          __threadfence();
+          for (int ch = 0; ch * 32 < mtot; ++ch) {
+            float s[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[i] = 0.f;
+            for (int cc = cf; cc <= cl; ++cc) {
+              const int sl = static_cast<long long>(cc) * U / P / a.kb == t ? 0 : 1;
+              const float4* src = reinterpret_cast<const float4*>(
+                  a.partials + ((static_cast<size_t>(cc) * 2 + sl) * kGemmBN + et) * NT + ch * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 p = __ldcg(src + i);
+                s[4 * i] += p.x;
+                s[4 * i + 1] += p.y;
+                s[4 * i + 2] += p.z;
+                s[4 * i + 3] += p.w;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = s[i];
+            named_bar(1, 128);
+            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128);
+            named_bar(1, 128);
+          }
+          if (et == 0) a.counters[t] = 0u;
+        }
+      }
+      ++seg;
+      u = uend;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TCOLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag && a.epi.status) atomicOr(a.epi.status, kStTimeout);
+}
+
+size_t tc_smem_bytes(int nt, bool pair, int stages) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair) + sizeof(float) * kGemmBN * kYsLd +
+         sizeof(uint64_t) * (2 * stages + 5) + 16;
+}
+
+int tc_stages_for(int nt, bool pair) {
+  const size_t fixed = tc_smem_bytes(nt, pair, 0) + 16 * sizeof(uint64_t);
+  int s = static_cast<int>((kSmemBudget - fixed) / stage_bytes(nt, pair));
+  if (s > 8) s = 8;
+  return s;
+}
+
+template <int NT, bool PAIR>
+cudaError_t launch_nt(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  const size_t smem = tc_smem_bytes(NT, PAIR, a.tc_stages);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<NT, PAIR><<<a.grid_p, kTcThreads, smem, s>>>(w, x, a);
+  return cudaGetLastError();
+}
+
+template <bool PAIR>
+cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  switch (a.tc_nt) {
+    case 32: return launch_nt<32, PAIR>(a, w, x, s);
+    case 64: return launch_nt<64, PAIR>(a, w, x, s);
+    case 96: return launch_nt<96, PAIR>(a, w, x, s);
+    case 128: return launch_nt<128, PAIR>(a, w, x, s);
+    case 160: return launch_nt<160, PAIR>(a, w, x, s);
+    case 192: return launch_nt<192, PAIR>(a, w, x, s);
+    case 224: return launch_nt<224, PAIR>(a, w, x, s);
+    case 256: return launch_nt<256, PAIR>(a, w, x, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t encode_bf16_map(CUtensorMap* m, const void* p, long long rows, int K, int box_rows) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  if ((reinterpret_cast<uintptr_t>(p) & 15) || (K % 8) || rows < 1) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t tc_encode_weight_map(CUtensorMap* m, const void* w, long long rows, int K) {
+  return encode_bf16_map(m, w, rows, K, kGemmBN / 2);
+}
+
+cudaError_t tc_encode_x_map(CUtensorMap* m, const void* x, long long rows, int K) {
+  return encode_bf16_map(m, x, rows, K, 32);
+}
+
+void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count) {
+  a.M = M;
+  a.K = K;
+  a.pair = pair;
+  a.n_tiles = pair == kPairSwiglu ? (n_units + kGemmBN / 2 - 1) / (kGemmBN / 2) : (n_units + kGemmBN - 1) / kGemmBN;
+  a.m_tiles = (M + 255) / 256;
+  const int per = (M + a.m_tiles - 1) / a.m_tiles;
+  a.tc_nt = (per + 31) / 32 * 32;
+  a.kb = (K + 63) / 64;
+  const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
+  a.grid_p = static_cast<int>(U < sm_count ? U : sm_count);
+  a.tc_stages = tc_stages_for(a.tc_nt, a.x_kind == kXPair);
+  a.k_splits = 1;
+  a.k_chunk = K;
+}
+
+size_t gemm_tc_partial_floats(const GemmArgs& a) {
+  return static_cast<size_t>(a.grid_p) * 2 * kGemmBN * a.tc_nt;
+}
+
+size_t gemm_tc_counter_count(const GemmArgs& a) { return static_cast<size_t>(a.n_tiles) * a.m_tiles; }
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  if (a.wdtype != SV_BF16 || a.tc_stages < 2) return cudaErrorInvalidValue;
+  return a.x_kind == kXPair ? launch_pair<true>(a, w, x, s) : launch_pair<false>(a, w, x, s);
+}
+
+}  // namespace sv

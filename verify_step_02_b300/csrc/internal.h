@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the host engine of libsv.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -93,6 +94,12 @@ struct GemmArgs {
   int k_chunk;             // K range of one split (multiple of the K step)
   float* partials;         // split-K partial tiles
   unsigned* counters;      // per tile arrivals (zero between launches)
+  // tensor path (gemm_tc.cu)
+  int tc_nt;               // token columns of one accumulator (multiple of 32, <= 256)
+  int kb;                  // K blocks of 64 per tile
+  int grid_p;              // CTAs; CTA c owns units [c U / P, (c+1) U / P), U = n_tiles m_tiles kb
+  int tc_stages;           // shared-memory pipeline depth
+  int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
   Epi epi;
 };
 
@@ -152,6 +159,15 @@ void record_error(const char* msg);
 
 // ---- launchers (defined in the .cu files) ----
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+// Tensor path (tcgen05, gemm_tc.cu) for bf16 weights with bf16 or hi/lo-pair x.
+// Weight maps: bf16 [rows][K], 64 x 64 boxes; x maps: bf16 [rows][K], 64 x 32
+// boxes; both 128-byte swizzled, zero fill outside the tensor.
+void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count);
+size_t gemm_tc_partial_floats(const GemmArgs& a);
+size_t gemm_tc_counter_count(const GemmArgs& a);
+cudaError_t tc_encode_weight_map(CUtensorMap* m, const void* w, long long rows, int K);
+cudaError_t tc_encode_x_map(CUtensorMap* m, const void* x, long long rows, int K);
+cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s);
 void plan_gemm(GemmArgs& a, int M, int n_rows_or_pairs, int K, int pair, int sm_count);
 size_t gemm_partial_floats(const GemmArgs& a);
 cudaError_t launch_attention(const AttnArgs& a, int B, int kv_dtype_bf16, cudaStream_t s);

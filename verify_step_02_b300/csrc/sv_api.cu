@@ -84,6 +84,10 @@ struct sv_model {
   long long* d_reqids = nullptr;
   int* d_out = nullptr;  // accepted_len [max_batch], next_token [max_batch]
   std::vector<void*> allocs;
+  // tensor path (bf16 weights): TMA maps of every weight matrix and of the x tensors
+  bool use_tc = false;
+  std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
+  CUtensorMap map_lm, map_u, map_ao, map_act;
   bool last_logits = false;
   int last_m = 0;
   Timing timing;
@@ -202,11 +206,29 @@ void gemm_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part,
   }
 }
 
+void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part, size_t* cnt) {
+  for (int M = 1; M <= m_max; ++M) {
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.x_kind = kXPair;
+    plan_gemm_tc(a, M, n_units, K, pair, sm);
+    *part = std::max(*part, gemm_tc_partial_floats(a));
+    *cnt = std::max(*cnt, gemm_tc_counter_count(a));
+  }
+}
+
+// wmap / xmap: the tensor maps of the weight and the x tensor (tensor path only).
 sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair, int kc, cudaStream_t s,
-                   const char* what) {
-  plan_gemm(a, M, n_units, K, pair, m->sm_count);
+                   const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr) {
   Timed t(m, kc, s);
-  SV_CUDA(launch_gemm(a, s), what);
+  if (m->use_tc) {
+    plan_gemm_tc(a, M, n_units, K, pair, m->sm_count);
+    a.x_lo_row = m->m_max;
+    SV_CUDA(launch_gemm_tc(a, *wmap, *xmap, s), what);
+  } else {
+    plan_gemm(a, M, n_units, K, pair, m->sm_count);
+    SV_CUDA(launch_gemm(a, s), what);
+  }
   return SV_OK;
 }
 
@@ -261,7 +283,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.max_pages = kv->max_pages_per_seq;
       a.epi.page_size = c.page_size;
       a.epi.n_pages = kv->n_pages;
-      sv_status st = run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm");
+      sv_status st = run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm", &m->map_qkv[l], &m->map_u);
       if (st) return st;
     }
     {
@@ -295,7 +317,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
-      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm");
+      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao);
       if (st) return st;
     }
     {
@@ -310,7 +332,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.act = m->act;
       a.epi.act_plane = m->act_plane;
       a.epi.ffn = c.ffn;
-      sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm");
+      sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm", &m->map_gu[l], &m->map_u);
       if (st) return st;
     }
     {
@@ -318,7 +340,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
-      sv_status st = run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm");
+      sv_status st = run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act);
       if (st) return st;
     }
     {
@@ -333,7 +355,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     a.epi.logits = keep ? m->logits : nullptr;
     a.epi.argmax_part = m->argmax_part;
     a.epi.vocab = c.vocab;
-    sv_status st = run_gemm(m, a, M, c.vocab, d, kPairNone, SV_KC_LM_HEAD, s, "lm head");
+    sv_status st = run_gemm(m, a, M, c.vocab, d, kPairNone, SV_KC_LM_HEAD, s, "lm head", &m->map_lm, &m->map_u);
     if (st) return st;
   }
   {
@@ -426,11 +448,13 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->req_row0, sizeof(int) * (c.max_batch + 1)));
   TRY(dalloc(m, &m->rope, sizeof(float2) * (size_t)c.max_seq_len * (c.head_dim / 2)));
   size_t part = 0, cnt = 0;
-  gemm_ws_need(m->sm_count, M, nqkv(c), d, kPairNone, &part, &cnt);
-  gemm_ws_need(m->sm_count, M, d, nq, kPairNone, &part, &cnt);
-  gemm_ws_need(m->sm_count, M, c.ffn, d, kPairSwiglu, &part, &cnt);
-  gemm_ws_need(m->sm_count, M, d, c.ffn, kPairNone, &part, &cnt);
-  gemm_ws_need(m->sm_count, M, c.vocab, d, kPairNone, &part, &cnt);
+  m->use_tc = cfg->weight_dtype == SV_BF16;
+  auto need = m->use_tc ? gemm_tc_ws_need : gemm_ws_need;
+  need(m->sm_count, M, nqkv(c), d, kPairNone, &part, &cnt);
+  need(m->sm_count, M, d, nq, kPairNone, &part, &cnt);
+  need(m->sm_count, M, c.ffn, d, kPairSwiglu, &part, &cnt);
+  need(m->sm_count, M, d, c.ffn, kPairNone, &part, &cnt);
+  need(m->sm_count, M, c.vocab, d, kPairNone, &part, &cnt);
   TRY(dalloc(m, &m->gemm_part, sizeof(float) * part));
   TRY(dalloc(m, &m->gemm_cnt, sizeof(unsigned) * cnt));
   AttnArgs aa;
@@ -447,6 +471,33 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->d_reqids, sizeof(long long) * c.max_batch));
   TRY(dalloc(m, &m->d_out, sizeof(int) * 2 * c.max_batch));
 #undef TRY
+  if (m->use_tc) {
+    cudaError_t me = cudaSuccess;
+    auto enc_w = [&](CUtensorMap* mp, const sv_matrix& w, long long rows, int K) {
+      if (me == cudaSuccess) me = tc_encode_weight_map(mp, w.data, rows, K);
+    };
+    const int L = c.n_layers;
+    m->map_qkv.resize(L);
+    m->map_o.resize(L);
+    m->map_gu.resize(L);
+    m->map_d.resize(L);
+    for (int l = 0; l < L; ++l) {
+      enc_w(&m->map_qkv[l], m->layers[l].wqkv, nqkv(c), d);
+      enc_w(&m->map_o[l], m->layers[l].wo, d, nq);
+      enc_w(&m->map_gu[l], m->layers[l].wgu, 2LL * c.ffn, d);
+      enc_w(&m->map_d[l], m->layers[l].wd, d, c.ffn);
+    }
+    enc_w(&m->map_lm, m->w.lm_head, c.vocab, d);
+    if (me == cudaSuccess) me = tc_encode_x_map(&m->map_u, m->u, 2LL * M, d);
+    if (me == cudaSuccess) me = tc_encode_x_map(&m->map_ao, m->ao, 2LL * M, nq);
+    if (me == cudaSuccess) me = tc_encode_x_map(&m->map_act, m->act, 2LL * M, c.ffn);
+    if (me != cudaSuccess) {
+      free_all(m);
+      delete m;
+      return fail(SV_ERR_INVALID_ARG, "tensor map encoding failed (weights must be 16-byte aligned): %s",
+                  cudaGetErrorString(me));
+    }
+  }
   cudaError_t e = cudaMemsetAsync(m->gemm_cnt, 0, sizeof(unsigned) * cnt, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->attn_cnt, 0, sizeof(unsigned) * c.max_batch * c.n_kv_heads, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(unsigned) * 4, s);
@@ -615,13 +666,18 @@ sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64
 }
 
 size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K) {
-  (void)wdtype;
   if (M < 1 || N < 1 || K < 1) return 0;
   int dev = 0, sm = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
   GemmArgs a;
   memset(&a, 0, sizeof a);
+  if (wdtype == SV_BF16) {  // tensor path; the pair plan needs the most scratch
+    a.x_kind = kXPair;
+    plan_gemm_tc(a, M, N, K, kPairNone, sm);
+    const size_t cnt = (gemm_tc_counter_count(a) * sizeof(unsigned) + 255) & ~(size_t)255;
+    return cnt + gemm_tc_partial_floats(a) * sizeof(float);
+  }
   plan_gemm(a, M, N, K, kPairNone, sm);
   const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
   return cnt + gemm_partial_floats(a) * sizeof(float);
@@ -651,13 +707,25 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   a.x = x;
   a.x_kind = wdtype == SV_F32 ? kXF32 : (x_planes == 2 ? kXPair : kXBf16);
   a.x_plane = (long long)M * K;
+  a.epi.kind = kEpiStore;
+  a.epi.y = y;
+  a.epi.ldy = N;
+  if (wdtype == SV_BF16) {
+    plan_gemm_tc(a, M, N, K, kPairNone, sm);
+    const size_t cnt = (gemm_tc_counter_count(a) * sizeof(unsigned) + 255) & ~(size_t)255;
+    a.counters = static_cast<unsigned*>(workspace);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + cnt);
+    a.x_lo_row = M;
+    CUtensorMap wm, xm;
+    SV_CUDA(tc_encode_weight_map(&wm, w->data, N, K), "weight tensor map");
+    SV_CUDA(tc_encode_x_map(&xm, x, (long long)x_planes * M, K), "x tensor map");
+    SV_CUDA(launch_gemm_tc(a, wm, xm, static_cast<cudaStream_t>(stream)), "linear");
+    return SV_OK;
+  }
   plan_gemm(a, M, N, K, kPairNone, sm);
   const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
   a.counters = static_cast<unsigned*>(workspace);
   a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + cnt);
-  a.epi.kind = kEpiStore;
-  a.epi.y = y;
-  a.epi.ldy = N;
   SV_CUDA(launch_gemm(a, static_cast<cudaStream_t>(stream)), "linear");
   return SV_OK;
 }
