@@ -52,9 +52,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", choices=["none", "gemm"], default="none")
-    ap.add_argument("--sweep-m", type=int, default=17)
+    ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
     ap.add_argument("--sweep-dtype", choices=["bf16", "w12"], default="bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=36,
+                    help="decoder layers of the 8B-class model (36; fewer only for small profiling runs, "
+                         "which the JSON line's config then names)")
     return ap.parse_args()
 
 
@@ -167,14 +170,14 @@ def traffic_record(kernel, workload, files):
 
 
 # ------------------------------------------------------------------ workload
-def build_workload(steps_total):
+def build_workload(steps_total, layers=36):
     import torch
 
     import synth
     import synth.device as sd
     import verify_step_02_b300 as vs
 
-    shape = synth.SHAPES["8b"]
+    shape = dict(synth.SHAPES["8b"], n_layers=layers)
     max_seq = CONTEXT + (steps_total + 2) * (GAMMA + 1) + 64
     max_seq = (max_seq + PAGE - 1) // PAGE * PAGE
     wdev = sd.random_bf16_model(shape)
@@ -237,7 +240,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     steps_total = args.warmup + args.steps
-    shape, wdev, kv, model, table = build_workload(3 * steps_total)
+    shape, wdev, kv, model, table = build_workload(3 * steps_total, args.layers)
     vocab = shape["vocab"]
     anchor = int(np.random.default_rng(20261202).integers(0, vocab))
     n_ref = int(steps_total * (1 + sum(P_KEEP ** (i + 1) for i in range(GAMMA))) * 1.5) + GAMMA + 8
@@ -326,7 +329,7 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random N(0,0.02) weights, random N(0,1) KV context, greedy-mix drafts)",
             "config": {"workload": "8B-class bf16 single-request verify, gamma 16 (M=17), context 4096, T=0",
-                       "batch": 1, "gamma": GAMMA, "context": CONTEXT, "layers": 36, "d_model": 4096,
+                       "batch": 1, "gamma": GAMMA, "context": CONTEXT, "layers": args.layers, "d_model": 4096,
                        "vocab": 151936, "l2": "inputs larger than L2 (15.1 GB of weights per step)",
                        "parallelism": f"replicas x{world}"},
             "verify_us": {"median": round(1e3 * statistics.median(per_step), 1),
@@ -485,7 +488,14 @@ def run_reference(args, world, rank, local):
 
 # ------------------------------------------------------------------ GEMM sweep
 def run_sweep(args, local):
-    """The skinny GEMM alone on the 8B-class projection shapes (rotating weight copies > L2)."""
+    """The skinny GEMM alone (sv_linear) on the 8B-class projection and LM-head shapes.
+
+    Activations are a hi/lo bf16 pair, as the verify step passes them. Each shape
+    rotates enough weight copies to exceed L2, and the timed launches replay from
+    a CUDA graph, so the time is the kernels' alone (no host work between them).
+    """
+    import ctypes
+
     import torch
 
     import synth
@@ -494,42 +504,67 @@ def run_sweep(args, local):
     s = synth.SHAPES["8b"]
     shapes = {"qkv": ((s["n_heads"] + 2 * s["n_kv_heads"]) * s["head_dim"], s["d_model"]),
               "o": (s["d_model"], s["n_heads"] * s["head_dim"]), "gate_up": (2 * s["ffn"], s["d_model"]),
-              "down": (s["d_model"], s["ffn"])}
+              "down": (s["d_model"], s["ffn"]), "lm_head": (s["vocab"], s["d_model"])}
     peak, peak_kind = measured_peaks()
+    ms = [int(v) for v in str(args.sweep_m).split(",")]
     out = {}
-    m = args.sweep_m
+    stream = torch.cuda.Stream()
     for name, (n, k) in shapes.items():
-        copies = max(2, int(np.ceil(512e6 / (n * k * 2))))
+        copies = max(1, int(np.ceil(512e6 / (n * k * 2))))
         ws = [synth.device_bf16_normal((n, k), 0.02, (900 + i, 0), "cuda") for i in range(copies)]
-        wdtype, base = vs.SV_BF16, 0
-        bpe = 2.0
+        wdtype, bases, bpe = vs.SV_BF16, [0] * copies, 2.0
         if args.sweep_dtype == "w12":
             wdtype, bpe = vs.SV_W12, 1.5
-            packed = []
+            packed, bases = [], []
             for w in ws:
                 bits = torch.randint(0, 2, w.shape, device="cuda", dtype=torch.int32) << 15 | \
                     torch.randint(111, 127, w.shape, device="cuda", dtype=torch.int32) << 7 | \
                     torch.randint(0, 128, w.shape, device="cuda", dtype=torch.int32)
                 planes, base = vs.pack_w12(bits.to(torch.int16).view(torch.bfloat16))
                 packed.append(planes)
+                bases.append(base)
             ws = packed
-        x = torch.randn((m, k), device="cuda").to(torch.bfloat16)
-        y, wsp = vs.linear(wdtype, ws[0], x, n, k, base=base)
-        for i in range(3):
-            vs.linear(wdtype, ws[i % copies], x, n, k, base=base, workspace=wsp)
-        reps = 20
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record()
-        for i in range(reps):
-            vs.linear(wdtype, ws[i % copies], x, n, k, base=base, workspace=wsp)
-        e1.record()
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) / reps * 1e3
-        gbs = n * k * bpe / (us * 1e-6) / 1e9
-        out[name] = {"n": n, "k": k, "us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
-    return {"sweep": "gemm", "m": m, "dtype": args.sweep_dtype, "peak_gbs": peak, "peak_kind": peak_kind,
-            "shapes": out}
+        for m in ms:
+            xf = torch.randn((m, k), device="cuda")
+            hi = xf.to(torch.bfloat16)
+            x = torch.stack([hi, (xf - hi.float()).to(torch.bfloat16)]).contiguous()
+            y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+            need = int(vs.lib.sv_linear_workspace_bytes(wdtype, m, n, k))
+            wsp = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+            mats = [vs.Matrix(w.data_ptr(), int(b)) for w, b in zip(ws, bases)]
+            reps = max(4, min(40, int(4e9 / (n * k * bpe))))
+
+            def launch(i):
+                st = vs.lib.sv_linear(wdtype, ctypes.byref(mats[i % copies]), n, k, ctypes.c_void_p(x.data_ptr()),
+                                      2, m, ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(wsp.data_ptr()),
+                                      wsp.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                assert st == vs.SV_OK, vs.lib.sv_last_error()
+
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    launch(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    launch(i)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record()
+                g.replay()
+                e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / reps * 1e3
+            gbs = n * k * bpe / (us * 1e-6) / 1e9
+            out[f"{name}@M{m}"] = {"n": n, "k": k, "m": m, "us": round(us, 2), "gbs": round(gbs, 1),
+                                   "frac": round(gbs / peak, 4)}
+            del g
+        del ws
+        torch.cuda.empty_cache()
+    return {"sweep": "gemm", "dtype": args.sweep_dtype, "x": "hi/lo bf16 pair", "peak_gbs": peak,
+            "peak_kind": peak_kind, "timing": "CUDA-graph replay of back-to-back launches", "shapes": out}
 
 
 def main():

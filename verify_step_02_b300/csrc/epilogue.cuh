@@ -7,9 +7,17 @@
 //   QKV   rotate q and k by RoPE at the row's absolute position (rotate-half
 //         pairing i <-> i + hd/2, both halves of a head are in one tile),
 //         write q for attention and k, v into the row's page slot;
-//   O, down  add into the float32 residual stream;
+//   O, down  add into the float32 residual stream h, then write the next
+//         projection's x tensor h * gain and the tile's sums of h^2 per token
+//         (the statistics of the next RMSNorm);
 //   gate|up  SiLU(gate) * up, both rows of a feature in one tile;
 //   LM head  write logits and each token's (max, argmax) over the tile.
+// RMSNorm is folded in: y = W (h * g / rms) = (W (h * g)) / rms, so the
+// products consume x = h * g and their epilogues scale token m by
+// 1 / rms_m = rsqrt(sum of the tiles' h^2 / d + eps), summed in tile order.
+//
+// Thread layout: thread tid owns tile row t = tid % kGemmBN and tokens
+// tid / kGemmBN, + nthr / kGemmBN, ... (nthr a multiple of kGemmBN).
 #pragma once
 
 #include "device_util.cuh"
@@ -20,91 +28,155 @@ namespace sv {
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // ys: tile values, element (t, c) at ys[t * ldys + c] for tile row t < kGemmBN and
-// token c < mcount (global token m0 + c). nt: the weight tile index. The tile
-// is shared by threads tid = 0 .. nthr-1 (nthr a multiple of 32).
+// token c < mcount <= 32 (global token m0 + c). nt: the weight tile index.
+// sync(): a barrier over the nthr threads that run the epilogue.
+template <class Sync>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const float* ys, int ldys, int m0,
-                                              int mcount, int tid, int nthr) {
+                                              int mcount, int tid, int nthr, EpiSmem& sm, Sync sync) {
   const Epi& e = a.epi;
   constexpr int BN = kGemmBN;
-  if (e.kind == kEpiStore || e.kind == kEpiResid) {
-    for (int idx = tid; idx < BN * mcount; idx += nthr) {
-      const int c = idx / BN, t = idx - c * BN;
-      const int n = nt * BN + t;
-      if (n >= a.n_rows) continue;
-      const long long m = m0 + c;
-      const float v = ys[t * ldys + c];
-      if (e.kind == kEpiStore)
-        e.y[m * e.ldy + n] = v;
-      else
-        e.h[m * e.ldh + n] += v;
+  const int t = tid % BN, cg = tid / BN, ng = nthr / BN;
+  const int lane = tid & 31, rg = t >> 5;
+
+  // ---- per-token data, once per tile
+  if (tid < mcount) {
+    const int m = m0 + tid;
+    float rs = 1.f;
+    if (e.ss_in) {
+      const float* p = e.ss_in + static_cast<long long>(m) * e.n_ss;
+      float s = 0.f;
+      for (int i = 0; i < e.n_ss; ++i) s += p[i];
+      rs = rsqrtf(s / static_cast<float>(e.d_model) + e.eps);
+    }
+    sm.rstd[tid] = rs;
+    if (e.kind == kEpiQkv) {
+      const int pos = e.row_pos[m];
+      long long kvo = -1;
+      if (pos >= 0) {
+        const int r = e.row_req[m], pidx = pos / e.page_size;
+        const int page = pidx < e.max_pages ? e.page_table[static_cast<long long>(r) * e.max_pages + pidx] : -1;
+        if (page < 0 || page >= e.n_pages)
+          atomicOr(e.status, kStBadPage);
+        else
+          kvo = static_cast<long long>(page) * e.n_kv_heads * e.page_size + (pos - pidx * e.page_size);
+      }
+      sm.pos[tid] = pos;
+      sm.kv[tid] = kvo;
+    }
+  }
+  sync();
+
+  if (e.kind == kEpiStore) {
+    const int n = nt * BN + t;
+    if (n < a.n_rows)
+      for (int c = cg; c < mcount; c += ng) e.y[static_cast<long long>(m0 + c) * e.ldy + n] = ys[t * ldys + c];
+  } else if (e.kind == kEpiResid) {
+    const int n = nt * BN + t;
+    const bool valid = n < a.n_rows;
+    const float g = (valid && e.next_gain) ? load_act(e.next_gain, n, e.gain_bf16) : 0.f;
+    for (int c0 = cg; c0 < mcount; c0 += 8 * ng) {
+      float hv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + i * ng;
+        hv[i] = (valid && c < mcount) ? e.h[static_cast<long long>(m0 + c) * e.ldh + n] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + i * ng;
+        const bool live = valid && c < mcount;
+        const float hn = live ? hv[i] + ys[t * ldys + c] : 0.f;
+        if (live) {
+          e.h[static_cast<long long>(m0 + c) * e.ldh + n] = hn;
+          if (e.next_gain)
+            store_x(e.x_out, e.x_out_plane, static_cast<long long>(m0 + c) * e.d_model + n, hn * g, e.x_pair);
+        }
+        if (e.ss_out) {
+          const float sq = warp_sum(hn * hn);
+          if (lane == 0 && c < mcount) sm.red[rg][c] = sq;
+        }
+      }
+    }
+    if (e.ss_out) {
+      sync();
+      if (tid < mcount)
+        e.ss_out[static_cast<long long>(m0 + tid) * e.n_ss + nt] =
+            sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
     }
   } else if (e.kind == kEpiSwiglu) {
     constexpr int HB = BN / 2;
-    for (int idx = tid; idx < HB * mcount; idx += nthr) {
-      const int c = idx / HB, t = idx - c * HB;
-      const int f = nt * HB + t;
-      if (f >= e.ffn) continue;
-      const float g = ys[t * ldys + c], u = ys[(t + HB) * ldys + c];
-      store_x(e.act, e.act_plane, (long long)(m0 + c) * e.ffn + f, silu(g) * u, e.x_pair);
+    const int f = nt * HB + t;
+    if (t < HB && f < e.ffn) {
+      for (int c = cg; c < mcount; c += ng) {
+        const float rs = sm.rstd[c];
+        const float gv = ys[t * ldys + c] * rs, uv = ys[(t + HB) * ldys + c] * rs;
+        store_x(e.act, e.act_plane, static_cast<long long>(m0 + c) * e.ffn + f, silu(gv) * uv, e.x_pair);
+      }
     }
   } else if (e.kind == kEpiQkv) {
     const int hd = e.head_dim, half = hd >> 1;
     const int nq = e.n_heads * hd;
-    for (int idx = tid; idx < BN * mcount; idx += nthr) {
-      const int c = idx / BN, t = idx - c * BN;
-      const int n = nt * BN + t;
-      if (n >= a.n_rows) continue;
+    const int n = nt * BN + t;
+    if (n < a.n_rows) {
       const int head = n / hd, i = n - head * hd;
-      const int m = m0 + c;
-      const int pos = e.row_pos[m];
-      if (pos < 0) continue;  // flagged by the row preparation
-      float v = ys[t * ldys + c];
-      if (head < e.n_heads + e.n_kv_heads) {  // q or k: rotate
-        const int ii = i < half ? i : i - half;
-        const float2 cs = e.rope[(long long)pos * half + ii];
-        if (i < half) {
-          const float p = ys[(t + half) * ldys + c];
-          v = v * cs.x - p * cs.y;
-        } else {
-          const float p = ys[(t - half) * ldys + c];
-          v = v * cs.x + p * cs.y;
+      const bool rot = head < e.n_heads + e.n_kv_heads;  // q or k
+      const int ii = i < half ? i : i - half;
+      const int tp = i < half ? t + half : t - half;       // partner row of the rotation
+      const float sgn = i < half ? -1.f : 1.f;
+      const bool is_q = n < nq;
+      const int kvh = is_q ? 0 : head - e.n_heads - (rot ? 0 : e.n_kv_heads);
+      for (int c0 = cg; c0 < mcount; c0 += 8 * ng) {
+        float2 cs[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j * ng;
+          const int pos = c < mcount ? sm.pos[c] : -1;
+          cs[j] = (rot && pos >= 0) ? __ldg(e.rope + static_cast<long long>(pos) * half + ii) : make_float2(1.f, 0.f);
         }
-      }
-      if (n < nq) {
-        e.q_out[(long long)m * nq + n] = v;
-      } else {
-        const bool is_k = head < e.n_heads + e.n_kv_heads;
-        const int kvh = head - e.n_heads - (is_k ? 0 : e.n_kv_heads);
-        const int r = e.row_req[m];
-        const int pidx = pos / e.page_size;
-        const int page = pidx < e.max_pages ? e.page_table[(long long)r * e.max_pages + pidx] : -1;
-        if (page < 0 || page >= e.n_pages) {
-          atomicOr(e.status, kStBadPage);
-          continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j * ng;
+          if (c >= mcount) continue;
+          const int pos = sm.pos[c];
+          if (pos < 0) continue;  // flagged by the row preparation
+          const float rs = sm.rstd[c];
+          float v = ys[t * ldys + c] * rs;
+          if (rot) v = v * cs[j].x + sgn * (ys[tp * ldys + c] * rs) * cs[j].y;
+          const long long m = m0 + c;
+          if (is_q) {
+            if (e.q_pair)
+              store_x(e.q_pair, e.q_plane, m * nq + n, v * e.q_scale, 1);
+            else
+              e.q_out[m * nq + n] = v;
+          } else {
+            const long long kvo = sm.kv[c];
+            if (kvo < 0) continue;
+            const long long off = (kvo + static_cast<long long>(kvh) * e.page_size) * hd + i;
+            store_act(rot ? e.k_cache : e.v_cache, off, v, e.kv_bf16);
+          }
         }
-        const long long off = (((long long)page * e.n_kv_heads + kvh) * e.page_size + (pos - pidx * e.page_size)) *
-                                  hd + i;
-        store_act(is_k ? e.k_cache : e.v_cache, off, v, e.kv_bf16);
       }
     }
   } else if (e.kind == kEpiLogits) {
-    if (e.logits) {
-      for (int idx = tid; idx < BN * mcount; idx += nthr) {
-        const int c = idx / BN, t = idx - c * BN;
-        const int n = nt * BN + t;
-        if (n < e.vocab) e.logits[(long long)(m0 + c) * e.vocab + n] = ys[t * ldys + c];
+    const int n = nt * BN + t;
+    const bool valid = n < e.vocab;
+    for (int c = cg; c < mcount; c += ng) {
+      const float v = valid ? ys[t * ldys + c] * sm.rstd[c] : -INFINITY;
+      if (e.logits && valid) e.logits[static_cast<long long>(m0 + c) * e.vocab + n] = v;
+      float best = v;
+      int bi = valid ? n : 0x7fffffff;
+      warp_argmax(best, bi);
+      if (lane == 0) {
+        sm.red[rg][c] = best;
+        sm.redi[rg][c] = bi;
       }
     }
-    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    for (int c = warp; c < mcount; c += nw) {
-      float best = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int t = lane; t < BN; t += 32) {
-        const int n = nt * BN + t;
-        if (n < e.vocab) argmax_merge(best, bi, ys[t * ldys + c], n);
-      }
-      warp_argmax(best, bi);
-      if (lane == 0) e.argmax_part[(long long)(m0 + c) * a.n_tiles + nt] = make_float2(best, __int_as_float(bi));
+    sync();
+    if (tid < mcount) {
+      float best = sm.red[0][tid];
+      int bi = sm.redi[0][tid];
+      for (int g = 1; g < 4; ++g) argmax_merge(best, bi, sm.red[g][tid], sm.redi[g][tid]);
+      e.argmax_part[static_cast<long long>(m0 + tid) * a.n_tiles + nt] = make_float2(best, __int_as_float(bi));
     }
   }
 }

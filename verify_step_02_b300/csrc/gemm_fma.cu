@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   if (a.k_splits > 1) {
     if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM)) return;
   }
-  epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x);
+  __shared__ EpiSmem esm;
+  epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x, esm, [] { __syncthreads(); });
 }
 
 }  // namespace

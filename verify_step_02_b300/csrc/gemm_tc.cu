@@ -27,6 +27,7 @@
 // frees TMEM, returns).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "epilogue.cuh"
@@ -45,7 +46,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 constexpr int kSmemBudget = 225 * 1024;
 
-__host__ __device__ constexpr int stage_bytes(int nt, bool pair) { return kABytes + nt * 128 * (pair ? 2 : 1); }
+// One pipeline stage covers ks K-elements (ks / 64 swizzled sub-tiles of 64).
+__host__ __device__ constexpr int stage_bytes(int nt, bool pair, int ks) {
+  return (ks / 64) * (kABytes + nt * 128 * (pair ? 2 : 1));
+}
 
 __host__ __device__ constexpr uint32_t tmem_cols(int nt) {
   return 2 * nt <= 32 ? 32u : 2 * nt <= 64 ? 64u : 2 * nt <= 128 ? 128u : 2 * nt <= 256 ? 256u : 512u;
@@ -56,18 +60,21 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
   return static_cast<int>(((x + 1) * P + U - 1) / U - 1);
 }
 
-template <int NT, bool PAIR>
+template <int NT, bool PAIR, int KS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                    const GemmArgs a) {
-  constexpr int BX = NT * 128;  // bytes of one x plane per stage
-  constexpr int STAGE = stage_bytes(NT, PAIR);
+  constexpr int BX = NT * 128;              // bytes of one x plane per 64-wide sub-tile
+  constexpr int SUB = kABytes + BX * (PAIR ? 2 : 1);  // one 64-wide sub-tile: weights, then x
+  constexpr int NSUB = KS / 64;
+  constexpr int STAGE = stage_bytes(NT, PAIR, KS);
   constexpr uint32_t TCOLS = tmem_cols(NT);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.tc_stages;
   float* Ys = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(Ys + kGemmBN * kYsLd);
+  EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * kYsLd);
+  uint64_t* full = reinterpret_cast<uint64_t*>(esm + 1);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
@@ -116,18 +123,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int kb = static_cast<int>(u - t * a.kb);
         const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
         if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
-        uint8_t* sa = smem + static_cast<size_t>(stage) * STAGE;
-        uint8_t* sb = sa + kABytes;
+        uint8_t* st = smem + static_cast<size_t>(stage) * STAGE;
         mbar_arrive_expect_tx(full + stage, STAGE);
-        const int k = kb * 64;
         const int r0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
         const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : r0 + kGemmBN / 2;
-        tma_load_2d(sa, &tmw, k, r0, full + stage, pw);
-        tma_load_2d(sa + kABytes / 2, &tmw, k, r1, full + stage, pw);
+        // weight boxes first, all sub-tiles back to back: each row's KS elements
+        // are requested together (contiguous bytes in HBM)
 #pragma unroll
-        for (int j = 0; j < NT / 32; ++j) {
-          tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, full + stage, px);
-          if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, full + stage, px);
+        for (int q = 0; q < NSUB; ++q) {
+          tma_load_2d(st + q * SUB, &tmw, kb * KS + q * 64, r0, full + stage, pw);
+          tma_load_2d(st + q * SUB + kABytes / 2, &tmw, kb * KS + q * 64, r1, full + stage, pw);
+        }
+#pragma unroll
+        for (int q = 0; q < NSUB; ++q) {
+          uint8_t* sb = st + q * SUB + kABytes;
+          const int k = kb * KS + q * 64;
+#pragma unroll
+          for (int j = 0; j < NT / 32; ++j) {
+            tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, full + stage, px);
+            if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, full + stage, px);
+          }
         }
         ++issued;
         if (++stage == S) {
@@ -165,12 +180,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * STAGE), sb = sa + kABytes;
+          const uint32_t st = smem_u32(smem + static_cast<size_t>(stage) * STAGE);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = smem_desc_sw128(sa + k * 32);
-            mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || k > 0) ? 1u : 0u);
-            if (PAIR) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
+          for (int q = 0; q < NSUB; ++q) {
+            const uint32_t sa = st + q * SUB, sb = sa + kABytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc_sw128(sa + k * 32);
+              mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || q > 0 || k > 0) ? 1u : 0u);
+              if (PAIR) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
+            }
           }
           mma_commit(empty + stage);  // frees the stage once these MMAs have read it
           if (++stage == S) {
@@ -219,7 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
           named_bar(1, 128);
-          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128);
+          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128, *esm,
+                        [] { named_bar(1, 128); });
           named_bar(1, 128);
         } else {
           float4* dst = reinterpret_cast<float4*>(mine + ch * 32);
@@ -258,7 +278,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = s[i];
             named_bar(1, 128);
-            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128);
+            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128, *esm,
+                        [] { named_bar(1, 128); });
             named_bar(1, 128);
           }
           if (et == 0) a.counters[t] = 0u;
@@ -278,26 +299,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && *abort_flag && a.epi.status) atomicOr(a.epi.status, kStTimeout);
 }
 
-size_t tc_smem_bytes(int nt, bool pair, int stages) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair) + sizeof(float) * kGemmBN * kYsLd +
-         sizeof(uint64_t) * (2 * stages + 5) + 16;
+size_t tc_smem_bytes(int nt, bool pair, int ks, int stages) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair, ks) + sizeof(float) * kGemmBN * kYsLd +
+         sizeof(EpiSmem) + sizeof(uint64_t) * (2 * stages + 5) + 16;
 }
 
-int tc_stages_for(int nt, bool pair) {
-  const size_t fixed = tc_smem_bytes(nt, pair, 0) + 16 * sizeof(uint64_t);
-  int s = static_cast<int>((kSmemBudget - fixed) / stage_bytes(nt, pair));
+int tc_stages_for(int nt, bool pair, int ks) {
+  const size_t fixed = tc_smem_bytes(nt, pair, ks, 0) + 16 * sizeof(uint64_t);
+  int s = static_cast<int>((kSmemBudget - fixed) / stage_bytes(nt, pair, ks));
   if (s > 8) s = 8;
   return s;
 }
 
-template <int NT, bool PAIR>
-cudaError_t launch_nt(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
-  const size_t smem = tc_smem_bytes(NT, PAIR, a.tc_stages);
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+// K elements per pipeline stage for a token tile of nt columns: the widest of
+// 256 / 128 / 64 that still leaves three stages (two at the widest token tiles).
+int tc_ks_for(int nt, bool pair) {
+  if (const char* env = getenv("SV_GEMM_KS")) {
+    const int v = atoi(env);
+    if ((v == 64 || v == 128 || v == 256) && tc_stages_for(nt, pair, v) >= 2) return v;
+  }
+  for (int ks = 256; ks >= 64; ks /= 2)
+    if (tc_stages_for(nt, pair, ks) >= 3) return ks;
+  return 64;
+}
+
+template <int NT, bool PAIR, int KS>
+cudaError_t launch_ks(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  const size_t smem = tc_smem_bytes(NT, PAIR, KS, a.tc_stages);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<NT, PAIR><<<a.grid_p, kTcThreads, smem, s>>>(w, x, a);
+  gemm_tc_kernel<NT, PAIR, KS><<<a.grid_p, kTcThreads, smem, s>>>(w, x, a);
   return cudaGetLastError();
+}
+
+template <int NT, bool PAIR>
+cudaError_t launch_nt(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  switch (a.tc_ks) {
+    case 64: return launch_ks<NT, PAIR, 64>(a, w, x, s);
+    case 128: return launch_ks<NT, PAIR, 128>(a, w, x, s);
+    case 256: return launch_ks<NT, PAIR, 256>(a, w, x, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <bool PAIR>
@@ -355,6 +398,29 @@ cudaError_t tc_encode_x_map(CUtensorMap* m, const void* x, long long rows, int K
   return encode_bf16_map(m, x, rows, K, 32);
 }
 
+cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim) {
+  return encode_bf16_map(m, pool, static_cast<long long>(n_pages) * n_kv * 16, head_dim, 16);
+}
+
+cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,
+                            int rows) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (head_dim % 64) || group < 1 || group > 256 || rows < 1 ||
+      rows > 256)
+    return cudaErrorInvalidValue;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(n_heads),
+                              static_cast<cuuint64_t>(2) * m_max};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(n_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count) {
   a.M = M;
   a.K = K;
@@ -363,10 +429,11 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
   a.m_tiles = (M + 255) / 256;
   const int per = (M + a.m_tiles - 1) / a.m_tiles;
   a.tc_nt = (per + 31) / 32 * 32;
-  a.kb = (K + 63) / 64;
+  a.tc_ks = tc_ks_for(a.tc_nt, a.x_kind == kXPair);
+  a.kb = (K + a.tc_ks - 1) / a.tc_ks;
   const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
   a.grid_p = static_cast<int>(U < sm_count ? U : sm_count);
-  a.tc_stages = tc_stages_for(a.tc_nt, a.x_kind == kXPair);
+  a.tc_stages = tc_stages_for(a.tc_nt, a.x_kind == kXPair, a.tc_ks);
   a.k_splits = 1;
   a.k_chunk = K;
 }

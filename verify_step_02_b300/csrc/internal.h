@@ -61,9 +61,26 @@ struct Epi {
   int page_size;
   int n_pages;
   unsigned* status;
-  // kEpiResid
+  // RMSNorm folded into the projections: the x tensors of the QKV, gate|up and
+  // LM-head products hold h * gain (no 1/rms); their epilogues multiply each
+  // token's results by rsqrt(sum_i ss_in[m][i] / d_model + eps), the sums of
+  // squares that the producer of h left per 128-column tile.
+  const float* ss_in;      // [M][n_ss] or nullptr (no scaling)
+  int n_ss;                // ceil(d_model / 128)
+  int d_model;
+  float eps;
+  // kEpiResid: h += value; then x_out = h * next_gain and ss_out[m][tile] = sum of h^2
   float* h;
   int ldh;
+  const void* next_gain;   // [d_model], bf16 when gain_bf16 else float32; nullptr: no x_out
+  int gain_bf16;
+  void* x_out;             // x tensor [M][d_model] (float32 or hi/lo pair, x_pair)
+  long long x_out_plane;
+  float* ss_out;           // [M][n_ss]
+  // kEpiQkv: q for the tensor-core attention as hi/lo bf16 planes, pre-scaled
+  void* q_pair;            // [2][M][n_heads*head_dim] or nullptr (float32 q_out)
+  long long q_plane;
+  float q_scale;
   // kEpiSwiglu
   void* act;
   long long act_plane;     // element offset of the lo plane (x_pair)
@@ -72,6 +89,15 @@ struct Epi {
   float* logits;           // [M][vocab] or nullptr
   float2* argmax_part;     // [M][n_tiles]: (max value, index as float bits)
   int vocab;
+};
+
+// Per-token scratch of a GEMM tile epilogue (shared memory).
+struct EpiSmem {
+  float rstd[32];
+  int pos[32];
+  long long kv[32];        // page-pool row of the token's slot for kv head 0, or -1
+  float red[4][32];
+  int redi[4][32];
 };
 
 struct GemmArgs {
@@ -96,7 +122,8 @@ struct GemmArgs {
   unsigned* counters;      // per tile arrivals (zero between launches)
   // tensor path (gemm_tc.cu)
   int tc_nt;               // token columns of one accumulator (multiple of 32, <= 256)
-  int kb;                  // K blocks of 64 per tile
+  int tc_ks;               // K elements per pipeline stage (64, 128 or 256)
+  int kb;                  // K blocks of tc_ks per tile
   int grid_p;              // CTAs; CTA c owns units [c U / P, (c+1) U / P), U = n_tiles m_tiles kb
   int tc_stages;           // shared-memory pipeline depth
   int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
@@ -120,7 +147,9 @@ struct AttnArgs {
   int max_chunks;
   int max_rows;            // (max_gamma + 1) * group
   int max_seq_len;         // a request whose block ends past this is skipped (status kStBadPos)
-  float* partials;         // [B*n_kv*max_chunks][max_rows][head_dim + 2]
+  float* partials;         // chunk partials (layout per kernel; max_batch*n_kv*max_chunks*max_rows*(head_dim+2) floats)
+  long long ml_offset;     // tensor-core kernel: float offset of the (m, l) pairs after the O partials
+  int q_lo_row;            // tensor-core kernel: first token row of q's lo plane in the q tensor map
   unsigned* counters;      // [B*n_kv]
   unsigned* status;
   int x_pair;
@@ -168,18 +197,26 @@ size_t gemm_tc_counter_count(const GemmArgs& a);
 cudaError_t tc_encode_weight_map(CUtensorMap* m, const void* w, long long rows, int K);
 cudaError_t tc_encode_x_map(CUtensorMap* m, const void* x, long long rows, int K);
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s);
+// Tensor-core attention (attention_tc.cu) for bf16 KV caches with 16-position
+// pages and at most 128 query rows per (request, kv head); KV maps: a layer's
+// pool as bf16 [n_pages * n_kv * 16][head_dim], 64 x 16 boxes.
+bool attention_tc_supported(int head_dim, int page_size, int max_rows);
+cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
+// q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
+cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,
+                            int rows);
+cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
+                                const CUtensorMap& v, cudaStream_t s);
 void plan_gemm(GemmArgs& a, int M, int n_rows_or_pairs, int K, int pair, int sm_count);
 size_t gemm_partial_floats(const GemmArgs& a);
 cudaError_t launch_attention(const AttnArgs& a, int B, int kv_dtype_bf16, cudaStream_t s);
 void plan_attention(AttnArgs& a, int max_batch, int max_seq_len, int max_gamma);
 size_t attention_partial_floats(const AttnArgs& a, int max_batch);
-// prep / rmsnorm: weights_bf16 selects the embedding and gain type; x_pair the u output form.
+// prep: weights_bf16 selects the embedding and gain type; x_pair the u output form.
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
                         int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
-                        int d, int vocab, int max_seq_len, float eps, int weights_bf16, int x_pair, unsigned* status,
-                        cudaStream_t s);
-cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, long long u_plane, int M, int d, float eps,
-                           int weights_bf16, int x_pair, cudaStream_t s);
+                        float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16, int x_pair,
+                        unsigned* status, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s);

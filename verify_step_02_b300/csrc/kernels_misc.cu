@@ -1,5 +1,5 @@
-// Row preparation, RMSNorm, acceptance + commit, RoPE table, W12 codec and
-// Philox kernels of the verify step.
+// Row preparation (embedding + the first RMSNorm statistics), acceptance +
+// commit, RoPE table, W12 codec and Philox kernels of the verify step.
 #include "device_util.cuh"
 #include "internal.h"
 
@@ -8,24 +8,16 @@ namespace {
 
 constexpr int kNormThreads = 256;
 
-// Normalize h[m] (float32, d) into u[m]: u = h / sqrt(mean(h^2) + eps) * g.
-__device__ __forceinline__ void norm_row(const float* hrow, const void* gain, void* u, long long u_plane, long long m,
-                                         int d, float eps, int weights_bf16, int x_pair, float* red) {
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(hrow[k], hrow[k], ss);
-  const float tot = block_sum(ss, red);
-  const float rstd = rsqrtf(tot / static_cast<float>(d) + eps);
-  for (int k = threadIdx.x; k < d; k += blockDim.x)
-    store_x(u, u_plane, m * d + k, hrow[k] * rstd * load_act(gain, k, weights_bf16), x_pair);
-}
-
 // One CTA per block row: find the row's request and offset, gather the token's
-// embedding into the residual stream, and apply the first layer's RMSNorm.
+// embedding into the residual stream h, and write the first projection's x
+// tensor h * g (the first layer's attention-norm gain) with the row's sum of
+// squares in ss[m][0] (the other tiles' slots zero): the QKV epilogue turns
+// that into the RMSNorm scale.
 __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, const int* tokens, const int* seq_len,
                                                             int* row_req, int* row_pos, int* req_row0_dev,
                                                             const void* embed, const void* gain, float* h, void* u,
-                                                            long long u_plane, int d, int vocab, int max_seq_len,
-                                                            float eps, int weights_bf16, int x_pair,
+                                                            long long u_plane, float* ss, int n_ss, int d, int vocab,
+                                                            int max_seq_len, int weights_bf16, int x_pair,
                                                             unsigned* status) {
   __shared__ float red[32];
   const int m = blockIdx.x;
@@ -54,17 +46,15 @@ __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, 
     row_pos[m] = pos;
   }
   float* hrow = h + (long long)m * d;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) hrow[k] = load_act(embed, (long long)tok * d + k, weights_bf16);
-  __syncthreads();
-  norm_row(hrow, gain, u, u_plane, m, d, eps, weights_bf16, x_pair, red);
-}
-
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* h, const void* gain, void* u,
-                                                               long long u_plane, int d, float eps, int weights_bf16,
-                                                               int x_pair) {
-  __shared__ float red[32];
-  const int m = blockIdx.x;
-  norm_row(h + (long long)m * d, gain, u, u_plane, m, d, eps, weights_bf16, x_pair, red);
+  float sq = 0.f;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    const float x = load_act(embed, (long long)tok * d + k, weights_bf16);
+    hrow[k] = x;
+    sq = fmaf(x, x, sq);
+    store_x(u, u_plane, (long long)m * d + k, x * load_act(gain, k, weights_bf16), x_pair);
+  }
+  const float tot = block_sum(sq, red);
+  for (int i = threadIdx.x; i < n_ss; i += blockDim.x) ss[(long long)m * n_ss + i] = i == 0 ? tot : 0.f;
 }
 
 // ------------------------------------------------------------------ acceptance
@@ -286,16 +276,10 @@ __global__ void philox_kernel(unsigned long long seed, long long req, long long 
 
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
                         int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
-                        int d, int vocab, int max_seq_len, float eps, int weights_bf16, int x_pair, unsigned* status,
-                        cudaStream_t s) {
+                        float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16, int x_pair,
+                        unsigned* status, cudaStream_t s) {
   prep_kernel<<<p.M, kNormThreads, 0, s>>>(p, tokens, seq_len, row_req, row_pos, req_row0_dev, embed, gain, h, u,
-                                           u_plane, d, vocab, max_seq_len, eps, weights_bf16, x_pair, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_rmsnorm(const float* h, const void* gain, void* u, long long u_plane, int M, int d, float eps,
-                           int weights_bf16, int x_pair, cudaStream_t s) {
-  rmsnorm_kernel<<<M, kNormThreads, 0, s>>>(h, gain, u, u_plane, d, eps, weights_bf16, x_pair);
+                                           u_plane, ss, n_ss, d, vocab, max_seq_len, weights_bf16, x_pair, status);
   return cudaGetLastError();
 }
 

@@ -62,6 +62,8 @@ struct sv_model {
   int lm_tiles = 0;
   // workspace
   float* h = nullptr;
+  float* ss = nullptr;   // [m_max][n_ss] per-tile sums of h^2 (RMSNorm statistics)
+  int n_ss = 1;
   void* u = nullptr;
   void* q = nullptr;
   void* ao = nullptr;
@@ -88,6 +90,13 @@ struct sv_model {
   bool use_tc = false;
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
   CUtensorMap map_lm, map_u, map_ao, map_act;
+  // tensor-core attention (bf16 KV): per-layer maps of the K and V page pools,
+  // re-encoded when the caller passes other pools
+  bool use_tc_attn = false;
+  std::vector<CUtensorMap> map_k, map_v;
+  std::vector<const void*> map_k_ptr, map_v_ptr;
+  std::vector<int> map_kv_pages;
+  CUtensorMap map_q;
   bool last_logits = false;
   int last_m = 0;
   Timing timing;
@@ -192,6 +201,10 @@ GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const voi
   a.epi.x_pair = m->x_pair;
   a.epi.kv_bf16 = m->wbf16;
   a.epi.status = m->status;
+  a.epi.n_ss = m->n_ss;
+  a.epi.d_model = m->cfg.d_model;
+  a.epi.eps = m->cfg.rms_eps;
+  a.epi.gain_bf16 = m->wbf16;
   return a;
 }
 
@@ -261,7 +274,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   {
     Timed t(m, SV_KC_NORM, s);
     SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, m->req_row0, m->w.embed,
-                        m->layers[0].attn_norm, m->h, m->u, m->u_plane, d, c.vocab, c.max_seq_len, c.rms_eps,
+                        m->layers[0].attn_norm, m->h, m->u, m->u_plane, m->ss, m->n_ss, d, c.vocab, c.max_seq_len,
                         m->wbf16, m->x_pair, m->status, s),
             "prep");
   }
@@ -277,6 +290,12 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.n_kv_heads = c.n_kv_heads;
       a.epi.head_dim = hd;
       a.epi.q_out = static_cast<float*>(m->q);
+      if (m->use_tc_attn) {  // q as pre-scaled hi/lo bf16 planes for the tensor-core attention
+        a.epi.q_pair = m->q;
+        a.epi.q_plane = (long long)m->m_max * nq;
+        a.epi.q_scale = 1.0f / std::sqrt(static_cast<float>(hd));
+      }
+      a.epi.ss_in = m->ss;
       a.epi.k_cache = kv->k[l];
       a.epi.v_cache = kv->v[l];
       a.epi.page_table = kv->page_table;
@@ -309,21 +328,34 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.status = m->status;
       a.x_pair = m->x_pair;
       a.kv_bf16 = m->wbf16;
-      Timed t(m, SV_KC_ATTENTION, s);
-      SV_CUDA(launch_attention(a, B, m->wbf16, s), "attention");
+      if (m->use_tc_attn) {
+        if (m->map_k_ptr[l] != kv->k[l] || m->map_v_ptr[l] != kv->v[l] || m->map_kv_pages[l] != kv->n_pages) {
+          SV_CUDA(tc_encode_kv_map(&m->map_k[l], kv->k[l], kv->n_pages, c.n_kv_heads, hd), "K pool tensor map");
+          SV_CUDA(tc_encode_kv_map(&m->map_v[l], kv->v[l], kv->n_pages, c.n_kv_heads, hd), "V pool tensor map");
+          m->map_k_ptr[l] = kv->k[l];
+          m->map_v_ptr[l] = kv->v[l];
+          m->map_kv_pages[l] = kv->n_pages;
+        }
+        a.q_lo_row = m->m_max;
+        a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
+        Timed t(m, SV_KC_ATTENTION, s);
+        SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
+      } else {
+        Timed t(m, SV_KC_ATTENTION, s);
+        SV_CUDA(launch_attention(a, B, m->wbf16, s), "attention");
+      }
     }
     {
       GemmArgs a = gemm_base(m, L.wo, d, nq, m->ao, m->ao_plane);
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
+      a.epi.next_gain = L.mlp_norm;
+      a.epi.x_out = m->u;
+      a.epi.x_out_plane = m->u_plane;
+      a.epi.ss_out = m->ss;
       sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao);
       if (st) return st;
-    }
-    {
-      Timed t(m, SV_KC_NORM, s);
-      SV_CUDA(launch_rmsnorm(m->h, L.mlp_norm, m->u, m->u_plane, M, d, c.rms_eps, m->wbf16, m->x_pair, s),
-              "rmsnorm");
     }
     {
       GemmArgs a = gemm_base(m, L.wgu, 2 * c.ffn, d, m->u, m->u_plane);
@@ -332,6 +364,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.act = m->act;
       a.epi.act_plane = m->act_plane;
       a.epi.ffn = c.ffn;
+      a.epi.ss_in = m->ss;
       sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm", &m->map_gu[l], &m->map_u);
       if (st) return st;
     }
@@ -340,18 +373,18 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.kind = kEpiResid;
       a.epi.h = m->h;
       a.epi.ldh = d;
+      a.epi.next_gain = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
+      a.epi.x_out = m->u;
+      a.epi.x_out_plane = m->u_plane;
+      a.epi.ss_out = m->ss;
       sv_status st = run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act);
       if (st) return st;
-    }
-    {
-      const void* g = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
-      Timed t(m, SV_KC_NORM, s);
-      SV_CUDA(launch_rmsnorm(m->h, g, m->u, m->u_plane, M, d, c.rms_eps, m->wbf16, m->x_pair, s), "rmsnorm");
     }
   }
   {
     GemmArgs a = gemm_base(m, m->w.lm_head, c.vocab, d, m->u, m->u_plane);
     a.epi.kind = kEpiLogits;
+    a.epi.ss_in = m->ss;
     a.epi.logits = keep ? m->logits : nullptr;
     a.epi.argmax_part = m->argmax_part;
     a.epi.vocab = c.vocab;
@@ -437,6 +470,8 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
     }                     \
   } while (0)
   TRY(dalloc(m, &m->h, sizeof(float) * M * d));
+  m->n_ss = (d + kGemmBN - 1) / kGemmBN;
+  TRY(dalloc(m, &m->ss, sizeof(float) * M * m->n_ss));
   TRY(dalloc(m, &m->u, ab * M * std::max(d, 16)));
   TRY(dalloc(m, &m->q, sizeof(float) * M * nq));
   TRY(dalloc(m, &m->ao, ab * M * nq));
@@ -471,6 +506,21 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->d_reqids, sizeof(long long) * c.max_batch));
   TRY(dalloc(m, &m->d_out, sizeof(int) * 2 * c.max_batch));
 #undef TRY
+  m->use_tc_attn = m->wbf16 && attention_tc_supported(c.head_dim, c.page_size, aa.max_rows);
+  if (m->use_tc_attn) {
+    m->map_k.resize(c.n_layers);
+    m->map_v.resize(c.n_layers);
+    m->map_k_ptr.assign(c.n_layers, nullptr);
+    m->map_v_ptr.assign(c.n_layers, nullptr);
+    m->map_kv_pages.assign(c.n_layers, 0);
+    const cudaError_t qe = tc_encode_q_map(&m->map_q, m->q, M, c.n_heads, c.head_dim, c.n_heads / c.n_kv_heads,
+                                           c.max_gamma + 1);
+    if (qe != cudaSuccess) {
+      free_all(m);
+      delete m;
+      return fail(SV_ERR_CUDA, "q tensor map: %s", cudaGetErrorString(qe));
+    }
+  }
   if (m->use_tc) {
     cudaError_t me = cudaSuccess;
     auto enc_w = [&](CUtensorMap* mp, const sv_matrix& w, long long rows, int K) {
