@@ -32,6 +32,8 @@ __device__ __forceinline__ float kv_load(const KVT* p, long long i) {
 template <typename KVT>
 __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) float sm[];
+  pdl_trigger();
+  pdl_wait();
   const int hd = a.head_dim, nkv = a.n_kv_heads, group = a.n_heads / nkv;
   const int r = blockIdx.x / nkv, h = blockIdx.x - r * nkv, chunk = blockIdx.y;
   const int C = a.seq_len[r];
@@ -203,14 +205,13 @@ cudaError_t launch_attention(const AttnArgs& a, int B, int kv_bf16, cudaStream_t
     cudaError_t e = cudaFuncSetAttribute(attn_fma_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    attn_fma_kernel<uint16_t><<<grid, 256, smem, s>>>(a);
+    return launch_k(attn_fma_kernel<uint16_t>, grid, dim3(256), smem, s, a.pdl != 0, a);
   } else {
     cudaError_t e =
         cudaFuncSetAttribute(attn_fma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_fma_kernel<float><<<grid, 256, smem, s>>>(a);
+    return launch_k(attn_fma_kernel<float>, grid, dim3(256), smem, s, a.pdl != 0, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace sv

@@ -35,7 +35,9 @@ namespace {
 using namespace tc;
 
 constexpr int kChunk = 256;
-constexpr int kAttnThreads = 192;
+constexpr int kRowWarps = 16;                         // softmax warps: 4 lane groups x 4 column groups
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kAttnThreads = kRowThreads + 64;        // + TMA warp + MMA warp
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr uint32_t kTile = 16384;  // 128 rows x 128 bytes
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* s_flag = abort_flag + 1;
   volatile uint32_t* valid_mask = reinterpret_cast<volatile uint32_t*>(abort_flag + 2);
 
+  pdl_trigger();
+  pdl_wait();
   const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
   const int r = blockIdx.x / nkv, h = blockIdx.x - r * nkv, chunk = blockIdx.y;
   const int C = a.seq_len[r];
@@ -105,68 +109,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     mbar_init(kv_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, kRowThreads);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, 512);
+  if (warp == kRowWarps + 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tO = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == kRowWarps) {
     // ------------------------------------------------------------ TMA producer
+    // lane p < 16 looks up page p of the chunk (all lookups in flight at once)
+    const int key = k0 + 16 * lane;
+    int page = -1;
+    if (lane < 16 && key < T) {
+      const int pidx = key >> 4;
+      page = pidx < a.max_pages ? a.page_table[static_cast<long long>(r) * a.max_pages + pidx] : -1;
+      if (page < 0 || page >= a.n_pages) {
+        atomicOr(a.status, kStBadPage);
+        page = -1;
+      }
+    }
+    const uint32_t mask = __ballot_sync(0xffffffffu, page >= 0);
     if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
-      const int* ptab = a.page_table + static_cast<long long>(r) * a.max_pages;
-      int pages[16];
-      uint32_t mask = 0;
-      int n_valid = 0;
-      for (int p = 0; p < 16; ++p) {
-        const int key = k0 + 16 * p;
-        pages[p] = -1;
-        if (key >= T) continue;
-        const int pidx = key >> 4;
-        const int page = pidx < a.max_pages ? ptab[pidx] : -1;
-        if (page < 0 || page >= a.n_pages) {
-          atomicOr(a.status, kStBadPage);
-          continue;
-        }
-        pages[p] = page;
-        mask |= 1u << p;
-        ++n_valid;
-      }
       *valid_mask = mask;
       const uint32_t qbox = 128u * group * (a.max_rows / group);
-      mbar_arrive_expect_tx(kv_full, static_cast<uint32_t>(n_valid) * NH * 2 * 2048u + 2 * NH * qbox);
-      const uint64_t pol = policy_evict_first(), polq = policy_evict_last();
+      mbar_arrive_expect_tx(kv_full, static_cast<uint32_t>(__popc(mask)) * NH * 2 * 2048u + 2 * NH * qbox);
+      const uint64_t polq = policy_evict_last();
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh)
           tma_load_3d(smem + Q_OFF + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0,
                       kv_full, polq);
-      for (int p = 0; p < 16; ++p) {
-        if (pages[p] < 0) continue;
-        const int row = (pages[p] * nkv + h) * 16;
+    }
+    __syncwarp();
+    if (page >= 0) {  // the transaction count was raised above, before any of these copies
+      const uint64_t pol = policy_evict_first();
+      const int row = (page * nkv + h) * 16;
 #pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-          tma_load_2d(smem + K_OFF + hh * 2 * kTile + p * 2048, &tmk, hh * 64, row, kv_full, pol);
-          tma_load_2d(smem + V_OFF + hh * 2 * kTile + p * 2048, &tmv, hh * 64, row, kv_full, pol);
-        }
-      }
-      {  // the copies land before the CTA can leave
-        volatile int never = 0;
-        mbar_wait(kv_full, 0, &never, kWaitNs);
+      for (int hh = 0; hh < NH; ++hh) {
+        tma_load_2d(smem + K_OFF + hh * 2 * kTile + lane * 2048, &tmk, hh * 64, row, kv_full, pol);
+        tma_load_2d(smem + V_OFF + hh * 2 * kTile + lane * 2048, &tmv, hh * 64, row, kv_full, pol);
       }
     }
-  } else if (warp == 5) {
+    if (lane == 0) {  // the copies land before the CTA can leave
+      volatile int never = 0;
+      mbar_wait(kv_full, 0, &never, kWaitNs);
+    }
+    __syncwarp();
+  } else if (warp == kRowWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(kv_full, 0, abort_flag, kWaitNs);
@@ -205,56 +205,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ rows: softmax, output
-    const int rho = tid;  // 0..127
+    // warp w reads TMEM lanes 32 (w % 4) .. (its rows) and columns of group
+    // cg = w / 4: keys cg*64 .. cg*64+63 of S, dims cg*32 .. cg*32+31 of O
+    const int lg = warp & 3, cg = warp >> 2;
+    const int rho = lg * 32 + lane;
     const bool live = rho < R;
     const int j = live ? rho / group : 0;
-    // softmax of the chunk's scores, one row per thread (waiting on kv_full too
-    // makes the producer's page mask visible here)
+    float* red = reinterpret_cast<float*>(bars + 8);  // [2][4][128]: partial max, partial sum
+    auto sync = [] { named_bar(1, kRowThreads); };
+    // (waiting on kv_full too makes the producer's page mask visible here)
     if (tid == 0)
       *s_flag = mbar_wait(kv_full, 0, abort_flag, kWaitNs) && mbar_wait(s_full, 0, abort_flag, kWaitNs) ? 1 : 0;
-    named_bar(1, 128);
+    sync();
     const bool ok = *s_flag != 0;
-    named_bar(1, 128);
+    sync();
     float m = -INFINITY, l = 0.f;
     if (ok) {
       tc_fence_after();
-      const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+      const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
       const uint32_t vmask = *valid_mask;
       const int lim = live ? C + j : -1;  // last key this row may see
-      for (int ch = 0; ch < kChunk / 32; ++ch) {
-        float v[32];
-        tmem_ld32(tS + lane_base + ch * 32, v);
+      float v[64];
+      tmem_ld32(tS + lane_base + cg * 64, v);
+      tmem_ld32(tS + lane_base + cg * 64 + 32, v + 32);
+      float mp = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + ch * 32 + i;
-          const bool vis = key <= lim && ((vmask >> ((ch * 32 + i) >> 4)) & 1u);
-          if (vis) m = fmaxf(m, v[i]);
-        }
+      for (int i = 0; i < 64; ++i) {
+        const int kk = cg * 64 + i;  // key within the chunk
+        const bool vis = k0 + kk <= lim && ((vmask >> (kk >> 4)) & 1u);
+        v[i] = vis ? v[i] : -INFINITY;
+        mp = fmaxf(mp, v[i]);
       }
-      for (int ch = 0; ch < kChunk / 32; ++ch) {
-        float v[32];
-        tmem_ld32(tS + lane_base + ch * 32, v);
+      red[cg * 128 + rho] = mp;
+      sync();
+      m = fmaxf(fmaxf(red[rho], red[128 + rho]), fmaxf(red[256 + rho], red[384 + rho]));
+      float lp = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + ch * 32 + i;
-          const bool vis = key <= lim && ((vmask >> ((ch * 32 + i) >> 4)) & 1u);
-          v[i] = vis ? expf(v[i] - m) : 0.f;
-          l += v[i];
-        }
-        // keys ch*32 .. +31 are chunks 4*(ch&1) .. +3 of key block ch/2
-        const int kb = ch >> 1;
+      for (int i = 0; i < 64; ++i) {
+        v[i] = v[i] == -INFINITY ? 0.f : expf(v[i] - m);
+        lp += v[i];
+      }
+      red[512 + cg * 128 + rho] = lp;
+      // keys cg*64 .. +63 are key block cg of P: 8 16-byte chunks per plane
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint4 hi, lo;
-          split8(v + 8 * q8, hi, lo);
-          const int c16 = (ch & 1) * 4 + q8;
-          *reinterpret_cast<uint4*>(smem + kb * kTile + sw128(rho, c16)) = hi;
-          *reinterpret_cast<uint4*>(smem + (4 + kb) * kTile + sw128(rho, c16)) = lo;
-        }
+      for (int c16 = 0; c16 < 8; ++c16) {
+        uint4 hi, lo;
+        split8(v + 8 * c16, hi, lo);
+        *reinterpret_cast<uint4*>(smem + cg * kTile + sw128(rho, c16)) = hi;
+        *reinterpret_cast<uint4*>(smem + (4 + cg) * kTile + sw128(rho, c16)) = lo;
       }
       // V rows of keys past the request's end or on unloaded pages hold stale
       // bytes (possibly not finite); zero them so P = 0 there contributes 0
-      for (int idx = tid; idx < kChunk * NH * 8; idx += 128) {
+      for (int idx = tid; idx < kChunk * NH * 8; idx += kRowThreads) {
         const int key_i = idx / (NH * 8), rem = idx - key_i * (NH * 8);
         const int hh = rem >> 3, c16 = rem & 7;
         if (k0 + key_i >= T || !((vmask >> (key_i >> 4)) & 1u))
@@ -266,29 +268,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_arrive(p_ready);
 
     if (tid == 0) *s_flag = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
-    named_bar(1, 128);
+    sync();
     const bool ok2 = *s_flag != 0;
     if (ok2) {
       tc_fence_after();
-      const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+      const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
       const long long slot = (static_cast<long long>(blockIdx.x) * a.max_chunks + chunk) * a.max_rows + rho;
-      float4* po = reinterpret_cast<float4*>(a.partials + slot * HD);
-      for (int ch = 0; ch < HD / 32; ++ch) {
-        float v[32];
-        tmem_ld32(tO + lane_base + ch * 32, v);
+      if (cg < HD / 32) {  // O dims cg*32 .. +31 (hd 64: column groups 0 and 1)
+        float4* po = reinterpret_cast<float4*>(a.partials + slot * HD + cg * 32);
+        float o[32];
+        tmem_ld32(tO + lane_base + cg * 32, o);
         if (live) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            __stcg(po + ch * 8 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          for (int i = 0; i < 8; ++i) __stcg(po + i, make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
         }
       }
-      if (live) __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(m, l));
+      if (live && cg == 0) {
+        l = red[512 + rho] + red[640 + rho] + red[768 + rho] + red[896 + rho];
+        __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(m, l));
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kRowWarps + 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -296,14 +300,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // One warp per (request, kv head, row): merge the row's chunk partials. Lanes
-// take the chunks' (m, l) for the maxima and the denominator, then each lane
-// sums its hd / 32 output dims over the chunks.
+// read the chunks' (m, l) once, form the weights e^(m_c - M) in shared memory
+// and the denominator; then each lane sums its hd / 32 output dims over the
+// chunks.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   constexpr int D = HD / 32;
+  extern __shared__ float s_w[];  // [8 warps][max_chunks]
   const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
   const int item = blockIdx.x, r = item / nkv, h = item - r * nkv;
-  const int rho = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rho = blockIdx.y * 8 + warp;
+  pdl_trigger();
+  pdl_wait();
   const int C = a.seq_len[r];
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
@@ -311,34 +320,41 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   const int nchunks = (T + kChunk - 1) / kChunk;
   const long long slot0 = static_cast<long long>(item) * a.max_chunks * a.max_rows + rho;
   const float2* ml = reinterpret_cast<const float2*>(a.partials + a.ml_offset) + slot0;
+  float* w = s_w + warp * a.max_chunks;
   float M = -INFINITY;
-  for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, __ldcg(ml + static_cast<long long>(c) * a.max_rows).x);
+  for (int c = lane; c < nchunks; c += 32) {
+    const float2 v = __ldcg(ml + static_cast<long long>(c) * a.max_rows);
+    w[c] = v.x;
+    M = fmaxf(M, v.x);
+  }
   M = warp_max(M);
   float L = 0.f;
   for (int c = lane; c < nchunks; c += 32) {
-    const float2 v = __ldcg(ml + static_cast<long long>(c) * a.max_rows);
-    if (v.x != -INFINITY) L += v.y * expf(v.x - M);
+    const float mc = w[c];
+    const float wc = mc == -INFINITY ? 0.f : expf(mc - M);
+    L += __ldcg(ml + static_cast<long long>(c) * a.max_rows).y * wc;
+    w[c] = wc;
   }
   L = warp_sum(L);
+  __syncwarp();
   float o[D];
 #pragma unroll
   for (int i = 0; i < D; ++i) o[i] = 0.f;
   const float* po = a.partials + slot0 * HD + lane * D;
 #pragma unroll 4
   for (int c = 0; c < nchunks; ++c) {
-    const float mc = __ldcg(ml + static_cast<long long>(c) * a.max_rows).x;
-    const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+    const float wc = w[c];
     const float* p = po + static_cast<long long>(c) * a.max_rows * HD;
     if constexpr (D == 4) {
       const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
-      o[0] = fmaf(w, v.x, o[0]);
-      o[1] = fmaf(w, v.y, o[1]);
-      o[2] = fmaf(w, v.z, o[2]);
-      o[3] = fmaf(w, v.w, o[3]);
+      o[0] = fmaf(wc, v.x, o[0]);
+      o[1] = fmaf(wc, v.y, o[1]);
+      o[2] = fmaf(wc, v.z, o[2]);
+      o[3] = fmaf(wc, v.w, o[3]);
     } else {
       const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
-      o[0] = fmaf(w, v.x, o[0]);
-      o[1] = fmaf(w, v.y, o[1]);
+      o[0] = fmaf(wc, v.x, o[0]);
+      o[1] = fmaf(wc, v.y, o[1]);
     }
   }
   const int j = rho / group, g = rho - j * group;
@@ -350,32 +366,43 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
 
 size_t attn_tc_smem(int hd) {
   const int nh = hd / 64;
-  return 1024 + 8 * kTile + static_cast<size_t>(nh) * 2 * kTile + 6 * 8 + 16 + 64;
+  return 1024 + 8 * kTile + static_cast<size_t>(nh) * 2 * kTile + 8 * 8 + sizeof(float) * 2 * 4 * 128;
 }
 
 template <int HD>
 cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       cudaStream_t s) {
   const size_t smem = attn_tc_smem(HD);
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = cudaSuccess;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_merge_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  e = launch_k(attn_tc_kernel<HD>, dim3(B * a.n_kv_heads, a.max_chunks), dim3(kAttnThreads), smem, s, a.pdl != 0, q,
+               k, v, a);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<HD><<<dim3(B * a.n_kv_heads, a.max_chunks), kAttnThreads, smem, s>>>(q, k, v, a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_merge_kernel<HD><<<dim3(B * a.n_kv_heads, (a.max_rows + 7) / 8), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  const size_t msmem = sizeof(float) * 8 * a.max_chunks;
+  return launch_k(attn_merge_kernel<HD>, dim3(B * a.n_kv_heads, (a.max_rows + 7) / 8), dim3(256), msmem, s,
+                  a.pdl != 0, a);
 }
 
 }  // namespace
 
-bool attention_tc_supported(int head_dim, int page_size, int max_rows) {
-  return (head_dim == 64 || head_dim == 128) && page_size == 16 && max_rows <= 128;
+bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len) {
+  const long long max_chunks = (static_cast<long long>(max_seq_len) + kChunk - 1) / kChunk;
+  return (head_dim == 64 || head_dim == 128) && page_size == 16 && max_rows <= 128 &&
+         max_chunks * 8 * sizeof(float) <= 200 * 1024;
 }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
                                 const CUtensorMap& v, cudaStream_t s) {
-  if (a.chunk != kChunk || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows))
+  if (a.chunk != kChunk || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
     return cudaErrorInvalidValue;
   return a.head_dim == 128 ? launch_hd<128>(a, B, q, k, v, s) : launch_hd<64>(a, B, q, k, v, s);
 }

@@ -8,6 +8,13 @@ namespace sv {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Programmatic dependent launch. pdl_trigger: this CTA lets the next kernel in
+// the stream start its independent prologue. pdl_wait: block until the
+// kernels before this one have completed and their writes are visible. Both
+// are no-ops for a kernel launched without the programmatic attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }

@@ -27,41 +27,60 @@ namespace sv {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// Per-token data of block row m: the RMSNorm scale 1 / rms (1 when the
+// product's input is not a normed x), and for the QKV product the row's
+// position and the page-pool row of its slot (kv head 0), or -1.
+__device__ __forceinline__ void token_data(const Epi& e, int m, float& rs, int& pos, long long& kvo) {
+  rs = 1.f;
+  if (e.ss_in) {
+    const float* p = e.ss_in + static_cast<long long>(m) * e.n_ss;
+    float s = 0.f;
+    for (int i0 = 0; i0 < e.n_ss; i0 += 8) {  // loads in flight together, sums in tile order
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = i0 + i < e.n_ss ? __ldcg(p + i0 + i) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[i];
+    }
+    rs = rsqrtf(s / static_cast<float>(e.d_model) + e.eps);
+  }
+  pos = -1;
+  kvo = -1;
+  if (e.kind == kEpiQkv) {
+    pos = e.row_pos[m];
+    if (pos >= 0) {
+      const int r = e.row_req[m], pidx = pos / e.page_size;
+      const int page = pidx < e.max_pages ? e.page_table[static_cast<long long>(r) * e.max_pages + pidx] : -1;
+      if (page < 0 || page >= e.n_pages)
+        atomicOr(e.status, kStBadPage);
+      else
+        kvo = static_cast<long long>(page) * e.n_kv_heads * e.page_size + (pos - pidx * e.page_size);
+    }
+  }
+}
+
 // ys: tile values, element (t, c) at ys[t * ldys + c] for tile row t < kGemmBN and
 // token c < mcount <= 32 (global token m0 + c). nt: the weight tile index.
+// td: the launch's per-token data, or nullptr (computed here, per tile).
 // sync(): a barrier over the nthr threads that run the epilogue.
 template <class Sync>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const float* ys, int ldys, int m0,
-                                              int mcount, int tid, int nthr, EpiSmem& sm, Sync sync) {
+                                              int mcount, int tid, int nthr, EpiSmem& sm, const TokData* td,
+                                              Sync sync) {
   const Epi& e = a.epi;
   constexpr int BN = kGemmBN;
   const int t = tid % BN, cg = tid / BN, ng = nthr / BN;
   const int lane = tid & 31, rg = t >> 5;
 
-  // ---- per-token data, once per tile
+  // ---- per-token data of the tile's tokens
   if (tid < mcount) {
     const int m = m0 + tid;
-    float rs = 1.f;
-    if (e.ss_in) {
-      const float* p = e.ss_in + static_cast<long long>(m) * e.n_ss;
-      float s = 0.f;
-      for (int i = 0; i < e.n_ss; ++i) s += p[i];
-      rs = rsqrtf(s / static_cast<float>(e.d_model) + e.eps);
-    }
-    sm.rstd[tid] = rs;
-    if (e.kind == kEpiQkv) {
-      const int pos = e.row_pos[m];
-      long long kvo = -1;
-      if (pos >= 0) {
-        const int r = e.row_req[m], pidx = pos / e.page_size;
-        const int page = pidx < e.max_pages ? e.page_table[static_cast<long long>(r) * e.max_pages + pidx] : -1;
-        if (page < 0 || page >= e.n_pages)
-          atomicOr(e.status, kStBadPage);
-        else
-          kvo = static_cast<long long>(page) * e.n_kv_heads * e.page_size + (pos - pidx * e.page_size);
-      }
-      sm.pos[tid] = pos;
-      sm.kv[tid] = kvo;
+    if (td) {
+      sm.rstd[tid] = td->rstd[m];
+      sm.pos[tid] = td->pos[m];
+      sm.kv[tid] = td->kv[m];
+    } else {
+      token_data(e, m, sm.rstd[tid], sm.pos[tid], sm.kv[tid]);
     }
   }
   sync();
@@ -74,15 +93,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
     const int n = nt * BN + t;
     const bool valid = n < a.n_rows;
     const float g = (valid && e.next_gain) ? load_act(e.next_gain, n, e.gain_bf16) : 0.f;
-    for (int c0 = cg; c0 < mcount; c0 += 8 * ng) {
-      float hv[8];
+    for (int c0 = cg; c0 < mcount; c0 += 16 * ng) {
+      float hv[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const int c = c0 + i * ng;
         hv[i] = (valid && c < mcount) ? e.h[static_cast<long long>(m0 + c) * e.ldh + n] : 0.f;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const int c = c0 + i * ng;
         const bool live = valid && c < mcount;
         const float hn = live ? hv[i] + ys[t * ldys + c] : 0.f;
@@ -125,16 +144,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
       const float sgn = i < half ? -1.f : 1.f;
       const bool is_q = n < nq;
       const int kvh = is_q ? 0 : head - e.n_heads - (rot ? 0 : e.n_kv_heads);
-      for (int c0 = cg; c0 < mcount; c0 += 8 * ng) {
-        float2 cs[8];
+      for (int c0 = cg; c0 < mcount; c0 += 16 * ng) {
+        float2 cs[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           const int c = c0 + j * ng;
           const int pos = c < mcount ? sm.pos[c] : -1;
           cs[j] = (rot && pos >= 0) ? __ldg(e.rope + static_cast<long long>(pos) * half + ii) : make_float2(1.f, 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           const int c = c0 + j * ng;
           if (c >= mcount) continue;
           const int pos = sm.pos[c];

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   __shared__ __align__(16) float Ws[KC][WS_LD];
   __shared__ __align__(16) float Xs[KC][XS_LD];
   __shared__ __align__(16) float Ys[BN * YS_LD];
+  pdl_trigger();
+  pdl_wait();
   const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
   const int tid = threadIdx.x;
   const int tr = (tid & 15) * 8, tc = (tid >> 4) * 2;
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
     if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM)) return;
   }
   __shared__ EpiSmem esm;
-  epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x, esm, [] { __syncthreads(); });
+  epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x, esm, nullptr, [] { __syncthreads(); });
 }
 
 }  // namespace
@@ -172,12 +174,11 @@ size_t gemm_partial_floats(const GemmArgs& a) {
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   const dim3 grid(a.n_tiles, a.m_tiles, a.k_splits);
   switch (a.wdtype) {
-    case SV_F32: gemm_fma_kernel<SV_F32><<<grid, 256, 0, s>>>(a); break;
-    case SV_BF16: gemm_fma_kernel<SV_BF16><<<grid, 256, 0, s>>>(a); break;
-    case SV_W12: gemm_fma_kernel<SV_W12><<<grid, 256, 0, s>>>(a); break;
+    case SV_F32: return launch_k(gemm_fma_kernel<SV_F32>, grid, dim3(256), 0, s, a.pdl != 0, a);
+    case SV_BF16: return launch_k(gemm_fma_kernel<SV_BF16>, grid, dim3(256), 0, s, a.pdl != 0, a);
+    case SV_W12: return launch_k(gemm_fma_kernel<SV_W12>, grid, dim3(256), 0, s, a.pdl != 0, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace sv

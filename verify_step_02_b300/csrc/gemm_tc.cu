@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = a.tc_stages;
   float* Ys = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * STAGE);
   EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * kYsLd);
-  uint64_t* full = reinterpret_cast<uint64_t*>(esm + 1);
+  TokData* tok = reinterpret_cast<TokData*>(esm + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tok + 1);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
@@ -110,40 +111,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      for (long long u = u0; u < u1; ++u) {
+      // weight boxes, all sub-tiles back to back: each row's KS elements are
+      // requested together (contiguous bytes in HBM)
+      auto load_w = [&](long long u, uint8_t* st, uint64_t* bar) {
         const long long t = u / a.kb;
         const int kb = static_cast<int>(u - t * a.kb);
-        const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
-        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
-        uint8_t* st = smem + static_cast<size_t>(stage) * STAGE;
-        mbar_arrive_expect_tx(full + stage, STAGE);
+        const int nt = static_cast<int>(t / a.m_tiles);
         const int r0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
         const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : r0 + kGemmBN / 2;
-        // weight boxes first, all sub-tiles back to back: each row's KS elements
-        // are requested together (contiguous bytes in HBM)
 #pragma unroll
         for (int q = 0; q < NSUB; ++q) {
-          tma_load_2d(st + q * SUB, &tmw, kb * KS + q * 64, r0, full + stage, pw);
-          tma_load_2d(st + q * SUB + kABytes / 2, &tmw, kb * KS + q * 64, r1, full + stage, pw);
+          tma_load_2d(st + q * SUB, &tmw, kb * KS + q * 64, r0, bar, pw);
+          tma_load_2d(st + q * SUB + kABytes / 2, &tmw, kb * KS + q * 64, r1, bar, pw);
         }
+      };
+      auto load_x = [&](long long u, uint8_t* st, uint64_t* bar) {
+        const long long t = u / a.kb;
+        const int kb = static_cast<int>(u - t * a.kb);
+        const int mt = static_cast<int>(t - (t / a.m_tiles) * a.m_tiles);
 #pragma unroll
         for (int q = 0; q < NSUB; ++q) {
           uint8_t* sb = st + q * SUB + kABytes;
           const int k = kb * KS + q * 64;
 #pragma unroll
           for (int j = 0; j < NT / 32; ++j) {
-            tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, full + stage, px);
-            if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, full + stage, px);
+            tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, bar, px);
+            if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, bar, px);
           }
         }
+      };
+      // The weights of the first stages do not depend on earlier kernels:
+      // request them before waiting for those kernels, then the activations.
+      const long long npre = u1 - u0 < S ? u1 - u0 : S;
+      for (long long i = 0; i < npre; ++i) {
+        uint8_t* st = smem + static_cast<size_t>(i) * STAGE;
+        mbar_arrive_expect_tx(full + i, STAGE);
+        load_w(u0 + i, st, full + i);
+      }
+      pdl_wait();
+      for (long long i = 0; i < npre; ++i) load_x(u0 + i, smem + static_cast<size_t>(i) * STAGE, full + i);
+      int stage = static_cast<int>(npre % S);
+      uint32_t phase = npre == S ? 1u : 0u;
+      long long issued = npre;
+      for (long long u = u0 + npre; u < u1; ++u) {
+        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
+        uint8_t* st = smem + static_cast<size_t>(stage) * STAGE;
+        mbar_arrive_expect_tx(full + stage, STAGE);
+        load_w(u, st, full + stage);
+        load_x(u, st, full + stage);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -209,9 +230,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();  // reads what earlier kernels wrote (h, norm statistics, row maps)
     const int et = threadIdx.x - 128;  // tile row = TMEM lane
+    // per-token data of the whole launch, while the weights stream in
+    const TokData* td = a.M <= kTokMax ? tok : nullptr;
+    if (td)
+      for (int m = et; m < a.M; m += 128) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
+    named_bar(1, 128);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int slot0_tile = static_cast<int>(u0 / a.kb);
+    auto sync = [] { named_bar(1, 128); };
     int seg = 0;
     for (long long u = u0; u < u1;) {
       const long long t = u / a.kb;
@@ -230,7 +258,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int m_base = mt * NT;
       const int mtot = a.M - m_base < NT ? a.M - m_base : NT;
       const int slot = static_cast<int>(t) == slot0_tile ? 0 : 1;
-      float* mine = a.partials + ((static_cast<size_t>(c) * 2 + slot) * kGemmBN + et) * NT;
+      // partial tiles are column-major ([token][tile row]) so that a warp's
+      // stores and the reducer's loads are 128-byte coalesced
+      float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
       for (int ch = 0; ch * 32 < mtot; ++ch) {
         float v[32];
         tmem_ld32(tmem + lane_base + b * NT + ch * 32, v);
@@ -239,12 +269,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
           named_bar(1, 128);
           epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128, *esm,
-                        [] { named_bar(1, 128); });
+                        td, sync);
           named_bar(1, 128);
         } else {
-          float4* dst = reinterpret_cast<float4*>(mine + ch * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          for (int i = 0; i < 32; ++i) __stcg(mine + (ch * 32 + i) * kGemmBN, v[i]);
         }
       }
       tc_fence_before();
@@ -258,28 +287,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar(1, 128);
         if (last) {
           __threadfence();
+          // the contributors' slots, in CTA order (a fixed summation order): a
+          // tile is the first tile (slot 0) of every contributor after cf, and of
+          // cf when cf's range starts at the tile's first unit
+          const int ncon = cl - cf + 1;
+          const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
           for (int ch = 0; ch * 32 < mtot; ++ch) {
             float s[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[i] = 0.f;
-            for (int cc = cf; cc <= cl; ++cc) {
-              const int sl = static_cast<long long>(cc) * U / P / a.kb == t ? 0 : 1;
-              const float4* src = reinterpret_cast<const float4*>(
-                  a.partials + ((static_cast<size_t>(cc) * 2 + sl) * kGemmBN + et) * NT + ch * 32);
+#pragma unroll 2
+            for (int j = 0; j < ncon; ++j) {
+              const int cc = cf + j;
+              const int sl = j == 0 ? sl_first : 0;
+              const float* src = a.partials + (static_cast<size_t>(cc) * 2 + sl) * kGemmBN * NT + et;
+              float v[32];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 p = __ldcg(src + i);
-                s[4 * i] += p.x;
-                s[4 * i + 1] += p.y;
-                s[4 * i + 2] += p.z;
-                s[4 * i + 3] += p.w;
-              }
+              for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (ch * 32 + i) * kGemmBN);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) s[i] += v[i];
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = s[i];
             named_bar(1, 128);
-            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128, *esm,
-                        [] { named_bar(1, 128); });
+            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128,
+                          *esm, td, sync);
             named_bar(1, 128);
           }
           if (et == 0) a.counters[t] = 0u;
@@ -301,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 size_t tc_smem_bytes(int nt, bool pair, int ks, int stages) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair, ks) + sizeof(float) * kGemmBN * kYsLd +
-         sizeof(EpiSmem) + sizeof(uint64_t) * (2 * stages + 5) + 16;
+         sizeof(EpiSmem) + sizeof(TokData) + sizeof(uint64_t) * (2 * stages + 5) + 16;
 }
 
 int tc_stages_for(int nt, bool pair, int ks) {
@@ -326,11 +358,16 @@ int tc_ks_for(int nt, bool pair) {
 template <int NT, bool PAIR, int KS>
 cudaError_t launch_ks(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(NT, PAIR, KS, a.tc_stages);
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  gemm_tc_kernel<NT, PAIR, KS><<<a.grid_p, kTcThreads, smem, s>>>(w, x, a);
-  return cudaGetLastError();
+  static bool attr_set[64] = {};  // per device: allow the largest configuration this kernel may use
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget + 2048);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  return launch_k(gemm_tc_kernel<NT, PAIR, KS>, dim3(a.grid_p), dim3(kTcThreads), smem, s, a.pdl != 0, w, x, a);
 }
 
 template <int NT, bool PAIR>

@@ -100,6 +100,15 @@ struct EpiSmem {
   int redi[4][32];
 };
 
+// Per-token epilogue data of a whole launch (block rows m < 256), computed once
+// per CTA while the weights stream (tensor path).
+constexpr int kTokMax = 256;
+struct TokData {
+  float rstd[kTokMax];
+  int pos[kTokMax];
+  long long kv[kTokMax];
+};
+
 struct GemmArgs {
   int wdtype;              // SV_F32, SV_BF16, SV_W12
   const void* w;           // weights (W12: planes back to back)
@@ -127,6 +136,7 @@ struct GemmArgs {
   int grid_p;              // CTAs; CTA c owns units [c U / P, (c+1) U / P), U = n_tiles m_tiles kb
   int tc_stages;           // shared-memory pipeline depth
   int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
+  int pdl;                 // launched as a programmatic dependent of the previous kernel
   Epi epi;
 };
 
@@ -154,6 +164,7 @@ struct AttnArgs {
   unsigned* status;
   int x_pair;
   int kv_bf16;
+  int pdl;                 // launched as a programmatic dependent of the previous kernel
 };
 
 struct AcceptArgs {
@@ -174,9 +185,11 @@ struct AcceptArgs {
   int* accepted_len;
   int* next_token;
   unsigned* status;
+  int pdl;
 };
 
 struct PrepParams {
+  int pdl;
   int B;
   int M;
   int gamma_stride;
@@ -185,6 +198,25 @@ struct PrepParams {
 
 // Set the message sv_last_error() returns on this thread.
 void record_error(const char* msg);
+
+// Launch `kern` on stream s; with pdl the launch may overlap the end of the
+// previous kernel in the stream (the kernel calls pdl_wait before it reads
+// what earlier kernels wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 // ---- launchers (defined in the .cu files) ----
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
@@ -200,7 +232,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtens
 // Tensor-core attention (attention_tc.cu) for bf16 KV caches with 16-position
 // pages and at most 128 query rows per (request, kv head); KV maps: a layer's
 // pool as bf16 [n_pages * n_kv * 16][head_dim], 64 x 16 boxes.
-bool attention_tc_supported(int head_dim, int page_size, int max_rows);
+bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len);
 cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
 // q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
 cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, 
                                                             int max_seq_len, int weights_bf16, int x_pair,
                                                             unsigned* status) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   if (m == 0)
     for (int i = threadIdx.x; i <= p.B; i += blockDim.x) req_row0_dev[i] = p.req_row0[i];
@@ -125,6 +127,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
   __shared__ int s_pick[2];
   __shared__ int s_targ[64];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
   const int row0 = a.req_row0[r], L = a.req_row0[r + 1] - row0 - 1;
   const int C = a.seq_len[r];
   const int* toks = a.tokens + (long long)r * a.gamma_stride;
@@ -278,14 +282,13 @@ cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_l
                         int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
                         float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16, int x_pair,
                         unsigned* status, cudaStream_t s) {
-  prep_kernel<<<p.M, kNormThreads, 0, s>>>(p, tokens, seq_len, row_req, row_pos, req_row0_dev, embed, gain, h, u,
-                                           u_plane, ss, n_ss, d, vocab, max_seq_len, weights_bf16, x_pair, status);
-  return cudaGetLastError();
+  return launch_k(prep_kernel, dim3(p.M), dim3(kNormThreads), 0, s, p.pdl != 0, p, tokens, seq_len, row_req, row_pos,
+                  req_row0_dev, embed, gain, h, u, u_plane, ss, n_ss, d, vocab, max_seq_len, weights_bf16, x_pair,
+                  status);
 }
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
-  accept_kernel<<<a.B, kAccThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(accept_kernel, dim3(a.B), dim3(kAccThreads), 0, s, a.pdl != 0, a);
 }
 
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s) {

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <utility>
@@ -88,6 +89,7 @@ struct sv_model {
   std::vector<void*> allocs;
   // tensor path (bf16 weights): TMA maps of every weight matrix and of the x tensors
   bool use_tc = false;
+  bool use_pdl = true;  // launch the step's kernels as programmatic dependents (overlapped prologues)
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
   CUtensorMap map_lm, map_u, map_ao, map_act;
   // tensor-core attention (bf16 KV): per-layer maps of the K and V page pools,
@@ -205,6 +207,7 @@ GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const voi
   a.epi.d_model = m->cfg.d_model;
   a.epi.eps = m->cfg.rms_eps;
   a.epi.gain_bf16 = m->wbf16;
+  a.pdl = m->use_pdl;
   return a;
 }
 
@@ -259,6 +262,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     if (!kv->k[l] || !kv->v[l]) return fail(SV_ERR_INVALID_ARG, "NULL KV pool for layer %d", l);
   static thread_local PrepParams p;
   p.B = B;
+  p.pdl = m->use_pdl;
   p.gamma_stride = c.max_gamma + 1;
   p.req_row0[0] = 0;
   for (int r = 0; r < B; ++r) {
@@ -328,6 +332,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.status = m->status;
       a.x_pair = m->x_pair;
       a.kv_bf16 = m->wbf16;
+      a.pdl = m->use_pdl;
       if (m->use_tc_attn) {
         if (m->map_k_ptr[l] != kv->k[l] || m->map_v_ptr[l] != kv->v[l] || m->map_kv_pages[l] != kv->n_pages) {
           SV_CUDA(tc_encode_kv_map(&m->map_k[l], kv->k[l], kv->n_pages, c.n_kv_heads, hd), "K pool tensor map");
@@ -411,6 +416,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     a.accepted_len = acc_len;
     a.next_token = next_tok;
     a.status = m->status;
+    a.pdl = m->use_pdl;
     Timed t(m, SV_KC_ACCEPT, s);
     SV_CUDA(launch_accept(a, s), "accept");
   }
@@ -446,6 +452,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->layers.assign(weights->layers, weights->layers + cfg->n_layers);
   m->w.layers = nullptr;
   m->wbf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
+  if (const char* env = getenv("SV_PDL")) m->use_pdl = atoi(env) != 0;
   m->x_pair = m->wbf16;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -506,7 +513,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->d_reqids, sizeof(long long) * c.max_batch));
   TRY(dalloc(m, &m->d_out, sizeof(int) * 2 * c.max_batch));
 #undef TRY
-  m->use_tc_attn = m->wbf16 && attention_tc_supported(c.head_dim, c.page_size, aa.max_rows);
+  m->use_tc_attn = m->wbf16 && attention_tc_supported(c.head_dim, c.page_size, aa.max_rows, c.max_seq_len);
   if (m->use_tc_attn) {
     m->map_k.resize(c.n_layers);
     m->map_v.resize(c.n_layers);
