@@ -51,20 +51,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t 
          (static_cast<uint64_t>(2) << 61);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  return static_cast<uint32_t>(f32_to_bf16_bits(a)) | (static_cast<uint32_t>(f32_to_bf16_bits(b)) << 16);
+// Two float32 values -> their bf16 pair (round to nearest even), low half first.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // 8 float32 values -> 16-byte hi chunk and lo chunk (x = hi + lo).
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-  float h[8], l[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    h[i] = bf16_bits_to_f32(f32_to_bf16_bits(x[i]));
-    l[i] = x[i] - h[i];
+  for (int i = 0; i < 4; ++i) {
+    h[i] = cvt_bf16x2(x[2 * i], x[2 * i + 1]);
+    l[i] = cvt_bf16x2(x[2 * i] - __uint_as_float(h[i] << 16), x[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u));
   }
-  hi = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
-  lo = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte swizzled tile.
@@ -103,7 +105,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int k0 = chunk * kChunk;
   if (k0 >= T) return;
   const int R = nrows * group;
-  const int nq = a.n_heads * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
 
   if (tid == 0) {
@@ -161,8 +162,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_2d(smem + V_OFF + hh * 2 * kTile + lane * 2048, &tmv, hh * 64, row, kv_full, pol);
       }
     }
-    if (lane == 0) {  // the copies land before the CTA can leave
-      volatile int never = 0;
+    if (lane == 0) {
+      // attention leaves HBM mostly idle: bring the output projection's weights
+      // into L2, one slice per CTA of request 0
+      if (r == 0) prefetch_l2_slice(a.l2_next, a.l2_next_bytes, static_cast<long long>(chunk) * nkv + h,
+                                    static_cast<long long>((T + kChunk - 1) / kChunk) * nkv);
+      volatile int never = 0;  // the copies land before the CTA can leave
       mbar_wait(kv_full, 0, &never, kWaitNs);
     }
     __syncwarp();
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float lp = 0.f;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        v[i] = v[i] == -INFINITY ? 0.f : expf(v[i] - m);
+        v[i] = v[i] == -INFINITY ? 0.f : __expf(v[i] - m);
         lp += v[i];
       }
       red[512 + cg * 128 + rho] = lp;
@@ -256,6 +261,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       // V rows of keys past the request's end or on unloaded pages hold stale
       // bytes (possibly not finite); zero them so P = 0 there contributes 0
+      if (k0 + kChunk > T || vmask != 0xFFFFu)
       for (int idx = tid; idx < kChunk * NH * 8; idx += kRowThreads) {
         const int key_i = idx / (NH * 8), rem = idx - key_i * (NH * 8);
         const int hh = rem >> 3, c16 = rem & 7;

@@ -59,14 +59,37 @@ __device__ __forceinline__ void token_data(const Epi& e, int m, float& rs, int& 
   }
 }
 
+// Bring the global inputs the epilogue of tile nt will read (the residual h
+// rows, the RoPE rows of the tokens' positions) into L1 ahead of time, so that
+// a split tile's last arriver does not pay their latency after the reduction.
+__device__ __forceinline__ void epilogue_prefetch(const GemmArgs& a, int nt, int m0, int mcount, int tid,
+                                                  const TokData* td) {
+  const Epi& e = a.epi;
+  const int t = tid % kGemmBN, n = nt * kGemmBN + t;
+  if (n >= a.n_rows) return;
+  if (e.kind == kEpiResid) {
+    if (e.next_gain)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const char*>(e.next_gain) + (e.gain_bf16 ? 2 : 4) * n));
+    for (int c = 0; c < mcount; ++c)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(e.h + static_cast<long long>(m0 + c) * e.ldh + n));
+  } else if (e.kind == kEpiQkv && td) {
+    const int hd = e.head_dim, half = hd >> 1, head = n / hd, i = n - head * hd;
+    if (head >= e.n_heads + e.n_kv_heads) return;  // v rows are not rotated
+    const int ii = i < half ? i : i - half;
+    for (int c = 0; c < mcount; ++c) {
+      const int pos = td->pos[m0 + c];
+      if (pos >= 0) asm volatile("prefetch.global.L1 [%0];" ::"l"(e.rope + static_cast<long long>(pos) * half + ii));
+    }
+  }
+}
+
 // ys: tile values, element (t, c) at ys[t * ldys + c] for tile row t < kGemmBN and
 // token c < mcount <= 32 (global token m0 + c). nt: the weight tile index.
 // td: the launch's per-token data, or nullptr (computed here, per tile).
 // sync(): a barrier over the nthr threads that run the epilogue.
 template <class Sync>
-__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const float* ys, int ldys, int m0,
-                                              int mcount, int tid, int nthr, EpiSmem& sm, const TokData* td,
-                                              Sync sync) {
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, float* ys, int ldys, int m0, int mcount,
+                                              int tid, int nthr, EpiSmem& sm, const TokData* td, Sync sync) {
   const Epi& e = a.epi;
   constexpr int BN = kGemmBN;
   const int t = tid % BN, cg = tid / BN, ng = nthr / BN;
@@ -110,17 +133,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, const f
           if (e.next_gain)
             store_x(e.x_out, e.x_out_plane, static_cast<long long>(m0 + c) * e.d_model + n, hn * g, e.x_pair);
         }
-        if (e.ss_out) {
-          const float sq = warp_sum(hn * hn);
-          if (lane == 0 && c < mcount) sm.red[rg][c] = sq;
-        }
+        if (c < mcount) ys[t * ldys + c] = hn * hn;  // this thread's own tile slot, already consumed
       }
     }
     if (e.ss_out) {
+      // the tile's sum of h^2 per token: warp w sums tokens w, w + nthr/32, ..
+      // over the 128 rows (rows lane + 32k, k in order, then a shuffle tree)
       sync();
-      if (tid < mcount)
-        e.ss_out[static_cast<long long>(m0 + tid) * e.n_ss + nt] =
-            sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
+      for (int c = tid >> 5; c < mcount; c += nthr >> 5) {
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < BN / 32; ++k) q += ys[(lane + 32 * k) * ldys + c];
+        q = warp_sum(q);
+        if (lane == 0) e.ss_out[static_cast<long long>(m0 + c) * e.n_ss + nt] = q;
+      }
     }
   } else if (e.kind == kEpiSwiglu) {
     constexpr int HB = BN / 2;

@@ -39,7 +39,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 epilogue (two warpgroups)
+constexpr int kEpiThreads = 256;
 constexpr int kYsLd = 33;                       // Ys row stride (floats)
 constexpr int kABytes = kGemmBN * 128;          // weight tile of one stage: 128 rows x 64 bf16
 constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
-      mbar_init(acc_empty + i, 128);
+      mbar_init(acc_empty + i, 128);  // the TMEM-reading warpgroup
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -171,6 +172,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           phase ^= 1u;
         }
       }
+      // HBM goes idle as this kernel drains: start a later kernel's weights
+      prefetch_l2_slice(a.l2_next, a.l2_next_bytes, c, P);
       if (*abort_flag) {
         // let the copies still in flight land before the CTA's shared memory goes away
         volatile int never = 0;
@@ -230,27 +233,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    // Warpgroup A (warps 4-7) reads the accumulators out of TMEM (warp w reads
+    // lanes 32 (w % 4) ..) and writes partial tiles; both warpgroups share
+    // the split reduction (16 columns each) and the tile epilogue.
     pdl_wait();  // reads what earlier kernels wrote (h, norm statistics, row maps)
-    const int et = threadIdx.x - 128;  // tile row = TMEM lane
+    const int et2 = threadIdx.x - 128;          // 0 .. 255
+    const bool grpA = et2 < 128;
+    const int et = et2 & 127;                   // tile row
     // per-token data of the whole launch, while the weights stream in
     const TokData* td = a.M <= kTokMax ? tok : nullptr;
     if (td)
-      for (int m = et; m < a.M; m += 128) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
-    named_bar(1, 128);
+      for (int m = et2; m < a.M; m += kEpiThreads) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
+    auto sync = [] { named_bar(1, kEpiThreads); };
+    sync();
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int slot0_tile = static_cast<int>(u0 / a.kb);
-    auto sync = [] { named_bar(1, 128); };
     int seg = 0;
     for (long long u = u0; u < u1;) {
       const long long t = u / a.kb;
       const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
       const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
       const int b = seg & 1;
-      // one thread waits and broadcasts, so all 128 threads agree on the outcome
-      if (et == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
-      named_bar(1, 128);
+      // one thread waits and broadcasts, so all threads agree on the outcome
+      if (et2 == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
+      sync();
       const bool ok = *s_flag != 0;
-      named_bar(1, 128);
+      sync();
       if (!ok) break;
       tc_fence_after();
       const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
@@ -263,28 +271,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
       for (int ch = 0; ch * 32 < mtot; ++ch) {
         float v[32];
-        tmem_ld32(tmem + lane_base + b * NT + ch * 32, v);
+        if (grpA) tmem_ld32(tmem + lane_base + b * NT + ch * 32, v);
         if (alone) {
+          if (grpA) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
-          named_bar(1, 128);
-          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128, *esm,
-                        td, sync);
-          named_bar(1, 128);
-        } else {
+            for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
+          }
+          sync();
+          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2,
+                        kEpiThreads, *esm, td, sync);
+          sync();
+        } else if (grpA) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) __stcg(mine + (ch * 32 + i) * kGemmBN, v[i]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty + b);
+      if (grpA) {
+        tc_fence_before();
+        mbar_arrive(acc_empty + b);
+      }
       if (!alone) {
+        epilogue_prefetch(a, nt, m_base, mtot < 32 ? mtot : 32, et, td);
         __threadfence();
-        named_bar(1, 128);
-        if (et == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
-        named_bar(1, 128);
+        sync();
+        if (et2 == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
+        sync();
         const bool last = *s_flag != 0;
-        named_bar(1, 128);
+        sync();
         if (last) {
           __threadfence();
           // the contributors' slots, in CTA order (a fixed summation order): a
@@ -292,29 +305,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // cf when cf's range starts at the tile's first unit
           const int ncon = cl - cf + 1;
           const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
+          const int col0 = grpA ? 0 : 16;  // each warpgroup sums 16 of the chunk's 32 columns
           for (int ch = 0; ch * 32 < mtot; ++ch) {
-            float s[32];
+            float s[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s[i] = 0.f;
+            for (int i = 0; i < 16; ++i) s[i] = 0.f;
 #pragma unroll 2
             for (int j = 0; j < ncon; ++j) {
               const int cc = cf + j;
               const int sl = j == 0 ? sl_first : 0;
               const float* src = a.partials + (static_cast<size_t>(cc) * 2 + sl) * kGemmBN * NT + et;
-              float v[32];
+              float v[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (ch * 32 + i) * kGemmBN);
+              for (int i = 0; i < 16; ++i) v[i] = __ldcg(src + (ch * 32 + col0 + i) * kGemmBN);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) s[i] += v[i];
+              for (int i = 0; i < 16; ++i) s[i] += v[i];
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = s[i];
-            named_bar(1, 128);
-            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et, 128,
-                          *esm, td, sync);
-            named_bar(1, 128);
+            for (int i = 0; i < 16; ++i) Ys[et * kYsLd + col0 + i] = s[i];
+            sync();
+            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2,
+                          kEpiThreads, *esm, td, sync);
+            sync();
           }
-          if (et == 0) a.counters[t] = 0u;
+          if (et2 == 0) a.counters[t] = 0u;
         }
       }
       ++seg;
