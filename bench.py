@@ -320,7 +320,7 @@ def run_ours(args, world, rank, local):
         gemm_ms, gemm_n = tim["gemm"]
         gemm_bytes_launch = per_layer / 4.0                     # 4 projections per layer
         achieved = gemm_bytes_launch / (gemm_ms / gemm_n * 1e-3) / 1e9 if gemm_n else None
-        traffic = traffic_record("gemm", "8b_m17", ["gemm_fma.cu", "epilogue.cuh"])
+        traffic = traffic_record("gemm", "8b_m17", ["gemm_tc.cu", "epilogue.cuh", "tc_ptx.cuh", "internal.h"])
         launches = sum(n for _, n in tim.values()) / args.steps
         ms_step = t_max / args.steps
         result = {

@@ -163,10 +163,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     if (lane == 0) {
-      // attention leaves HBM mostly idle: bring the output projection's weights
-      // into L2, one slice per CTA of request 0
-      if (r == 0) prefetch_l2_slice(a.l2_next, a.l2_next_bytes, static_cast<long long>(chunk) * nkv + h,
-                                    static_cast<long long>((T + kChunk - 1) / kChunk) * nkv);
       volatile int never = 0;  // the copies land before the CTA can leave
       mbar_wait(kv_full, 0, &never, kWaitNs);
     }

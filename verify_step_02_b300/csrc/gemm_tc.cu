@@ -172,8 +172,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           phase ^= 1u;
         }
       }
-      // HBM goes idle as this kernel drains: start a later kernel's weights
-      prefetch_l2_slice(a.l2_next, a.l2_next_bytes, c, P);
       if (*abort_flag) {
         // let the copies still in flight land before the CTA's shared memory goes away
         volatile int never = 0;

@@ -137,8 +137,6 @@ struct GemmArgs {
   int tc_stages;           // shared-memory pipeline depth
   int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
   int pdl;                 // launched as a programmatic dependent of the previous kernel
-  const void* l2_next;     // weights of a later kernel to bring into L2 once this one's loads are issued
-  long long l2_next_bytes;
   Epi epi;
 };
 
@@ -167,8 +165,6 @@ struct AttnArgs {
   int x_pair;
   int kv_bf16;
   int pdl;                 // launched as a programmatic dependent of the previous kernel
-  const void* l2_next;     // weights of a later kernel to bring into L2 (request 0's CTAs take slices)
-  long long l2_next_bytes;
 };
 
 struct AcceptArgs {

@@ -90,7 +90,6 @@ struct sv_model {
   // tensor path (bf16 weights): TMA maps of every weight matrix and of the x tensors
   bool use_tc = false;
   bool use_pdl = true;  // launch the step's kernels as programmatic dependents (overlapped prologues)
-  bool use_l2pf = true; // bring the next small weight matrix into L2 while HBM is idle
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
   CUtensorMap map_lm, map_u, map_ao, map_act;
   // tensor-core attention (bf16 KV): per-layer maps of the K and V page pools,
@@ -343,10 +342,6 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
-        if (m->use_tc && m->use_l2pf) {  // the O projection's weights follow
-          a.l2_next = L.wo.data;
-          a.l2_next_bytes = (long long)d * nq * 2;
-        }
         a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
@@ -384,10 +379,6 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.h = m->h;
       a.epi.ldh = d;
       a.epi.next_gain = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
-      if (l + 1 < c.n_layers && m->use_tc && m->use_l2pf) {  // the next layer's QKV weights follow
-        a.l2_next = m->layers[l + 1].wqkv.data;
-        a.l2_next_bytes = (long long)N3 * d * 2;
-      }
       a.epi.x_out = m->u;
       a.epi.x_out_plane = m->u_plane;
       a.epi.ss_out = m->ss;
@@ -462,7 +453,6 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->w.layers = nullptr;
   m->wbf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
   if (const char* env = getenv("SV_PDL")) m->use_pdl = atoi(env) != 0;
-  if (const char* env = getenv("SV_L2PF")) m->use_l2pf = atoi(env) != 0;
   m->x_pair = m->wbf16;
   int dev = 0;
   cudaGetDevice(&dev);

@@ -106,25 +106,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
-// Bring `bytes` (a multiple of 16) at a 16-byte-aligned global address into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
-}
-
-// Slice `part` of `nparts` of the byte range [p, p + bytes) into L2 (weights the
-// next kernel streams, requested while this kernel leaves HBM idle).
-__device__ __forceinline__ void prefetch_l2_slice(const void* p, long long bytes, long long part, long long nparts) {
-  if (!p || bytes <= 0 || nparts <= 0) return;
-  const long long per = ((bytes + nparts - 1) / nparts + 15) & ~15LL;
-  long long off = part * per;
-  const long long end = off + per < bytes ? off + per : bytes;
-  for (; off < end; off += 1 << 20) {
-    const long long n = end - off < (1 << 20) ? end - off : (1 << 20);
-    if (n >= 16) prefetch_l2_bulk(static_cast<const char*>(p) + off, static_cast<uint32_t>(n & ~15LL));
-  }
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
