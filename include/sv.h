@@ -91,7 +91,7 @@ typedef struct {
 /* A weight matrix [rows][cols] (the output-major layout y = x W^T).
  * F32/BF16: `data` is a dense row-major device array of that type.
  * W12: `data` holds plane 0, plane 1, plane 2 back to back, each
- *      [rows][sv_w12_row_bytes(cols)] bytes (see sv_pack_w12), and `base` is
+ *      sv_w12_plane_bytes(rows, cols) bytes (see sv_pack_w12), and `base` is
  *      the tensor's exponent base. */
 typedef struct {
   const void* data;
@@ -210,15 +210,22 @@ sv_status sv_model_timing(sv_model* model, double* ms /* [SV_KC_COUNT] */, int64
  * fixes no bit layout; this library's:
  *   bf16 b = s<<15 | E<<7 | m; base = min E over the tensor;
  *   code c = s<<11 | (E - base)<<7 | m (12 bits);
- *   plane p holds nibble p of c, row-major [rows][sv_w12_row_bytes(cols)]
- *   bytes, element k in byte k/2 (low nibble for even k), zero padding.
+ *   plane p holds nibble p of c. A plane is tiled: the matrix is padded
+ *   with zero codes to whole tiles of 64 rows x 128 columns; tile (rt, kt)
+ *   (KT = ceil(cols/128) tiles per row block) is 4096 contiguous bytes at
+ *   (rt*KT + kt)*4096, tile row r at r*64 within it. A tile row holds its
+ *   128 elements in groups of 8, group q in the little-endian 32-bit word at
+ *   bytes 4q..4q+3, whose nibble slot s (bits 4s..4s+3) holds element 8q+2s
+ *   for s < 4 and 8q+2(s-4)+1 for s >= 4. Each tile is one contiguous read
+ *   for the matrix kernels, and a shift and a mask put two elements into
+ *   the two 16-bit lanes of a word.
  * A tensor is representable iff every element is a normal number (not
  * +-0, subnormal, inf or NaN) and max E - min E <= 15.
  */
-int32_t sv_w12_row_bytes(int64_t cols);
+int64_t sv_w12_plane_bytes(int64_t rows, int64_t cols);
 
-/* Pack device bf16 [rows][cols] into device `planes` (3 * rows *
- * sv_w12_row_bytes(cols) bytes, caller-allocated). Writes the base to
+/* Pack device bf16 [rows][cols] into device `planes` (3 *
+ * sv_w12_plane_bytes(rows, cols) bytes, caller-allocated). Writes the base to
  * *base_out and the number of offending elements to *n_unrepresentable
  * (host). Synchronizes `stream`. Returns SV_ERR_NOT_REPRESENTABLE (planes
  * then undefined) when the tensor is not representable. */

@@ -10,20 +10,34 @@ the bit assignment nor the layout; this library's reading:
   NaN) and E - base <= 15 for every element (a 16-binade window).
   12-bit code c = s << 11 | (E - base) << 7 | m.
   plane p (p = 0, 1, 2) holds nibble p of c: (c >> 4p) & 15.
-  Each plane is row-major [rows][ld] bytes, ld = ceil(cols / 32) * 16, with
-  element k of a row in byte k // 2, low nibble for even k, high for odd k;
-  padding nibbles are zero. Planes are stored back to back: plane 0, 1, 2.
+  Each plane is stored in tiles of 64 rows x 128 elements (4096 bytes): the
+  matrix is padded with zero codes to a multiple of 64 rows and 128 columns,
+  tile (rt, kt) (row block rt, column block kt, KT = ceil(cols / 128) blocks
+  per row) starts at byte (rt * KT + kt) * 4096, and row r of the tile takes
+  bytes r * 64 .. r * 64 + 63 of it. A tile row holds its 128 elements in
+  groups of 8: group q in the little-endian 32-bit word at bytes 4q .. 4q+3,
+  whose nibble slot s (bits 4s .. 4s+3) holds element 8q + 2s for s < 4 and
+  element 8q + 2(s - 4) + 1 for s >= 4 (even elements in the low half-word,
+  odd ones in the high half-word, so a shift and a mask put elements 2j and
+  2j+1 into the two 16-bit lanes of a word). Planes are stored back to back:
+  plane 0, 1, 2, each plane_bytes(rows, cols) long.
 """
 import numpy as np
+
+# element (within a group of 8) held by nibble slot s = 0 .. 7 of a plane word
+SLOT_ELEMENT = np.array([0, 2, 4, 6, 1, 3, 5, 7])
 
 
 class NotRepresentable(ValueError):
     pass
 
 
-def row_bytes(cols):
-    """Bytes per plane row: the row padded to a multiple of 32 elements."""
-    return ((cols + 31) // 32) * 16
+TILE_ROWS, TILE_COLS, TILE_BYTES = 64, 128, 4096
+
+
+def plane_bytes(rows, cols):
+    """Bytes of one plane: whole 64 x 128 tiles."""
+    return -(-rows // TILE_ROWS) * -(-cols // TILE_COLS) * TILE_BYTES
 
 
 def fields(bits):
@@ -58,27 +72,36 @@ def pack(bits):
     if bad:
         raise NotRepresentable(bad)
     code = (s << 11) | (off << 7) | m
-    ld = row_bytes(cols)
-    planes = np.zeros((3, rows, ld), dtype=np.uint8)
+    rt, kt = -(-rows // TILE_ROWS), -(-cols // TILE_COLS)
+    padded = np.zeros((rt * TILE_ROWS, kt * TILE_COLS), dtype=np.int64)
+    padded[:rows, :cols] = code
+    # nibble slot t of a row holds element (t // 8) * 8 + SLOT_ELEMENT[t % 8]
+    slot_elem = (np.arange(kt * TILE_COLS) // 8) * 8 + SLOT_ELEMENT[np.arange(kt * TILE_COLS) % 8]
+    planes = np.zeros((3, plane_bytes(rows, cols)), dtype=np.uint8)
     for p in range(3):
-        nib = np.zeros((rows, 2 * ld), dtype=np.int64)
-        nib[:, :cols] = (code >> (4 * p)) & 0xF
-        planes[p] = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+        slots = ((padded >> (4 * p)) & 0xF)[:, slot_elem]
+        rowbytes = slots[:, 0::2] | (slots[:, 1::2] << 4)                # [rows_pad, cols_pad / 2]
+        tiles = rowbytes.reshape(rt, TILE_ROWS, kt, TILE_COLS // 2).transpose(0, 2, 1, 3)
+        planes[p] = tiles.reshape(-1).astype(np.uint8)
     return planes, base
 
 
-def unpack(planes, base, cols):
+def unpack(planes, base, rows, cols):
     """Inverse of pack: uint16 bf16 patterns [rows, cols]."""
     planes = np.asarray(planes, dtype=np.uint8)
-    code = np.zeros(planes.shape[1:2] + (2 * planes.shape[2],), dtype=np.int64)
+    rt, kt = -(-rows // TILE_ROWS), -(-cols // TILE_COLS)
+    slot_elem = (np.arange(kt * TILE_COLS) // 8) * 8 + SLOT_ELEMENT[np.arange(kt * TILE_COLS) % 8]
+    code = np.zeros((rt * TILE_ROWS, kt * TILE_COLS), dtype=np.int64)    # element order
     for p in range(3):
-        lo = planes[p].astype(np.int64) & 0xF
-        hi = planes[p].astype(np.int64) >> 4
+        tiles = planes[p].astype(np.int64).reshape(rt, kt, TILE_ROWS, TILE_COLS // 2)
+        rowbytes = tiles.transpose(0, 2, 1, 3).reshape(rt * TILE_ROWS, kt * TILE_COLS // 2)
+        slots = np.empty_like(code)
+        slots[:, 0::2] = rowbytes & 0xF
+        slots[:, 1::2] = rowbytes >> 4
         nib = np.empty_like(code)
-        nib[:, 0::2] = lo
-        nib[:, 1::2] = hi
+        nib[:, slot_elem] = slots
         code |= nib << (4 * p)
-    code = code[:, :cols]
+    code = code[:rows, :cols]
     s = code >> 11
     e = ((code >> 7) & 0xF) + base
     m = code & 0x7F

@@ -28,7 +28,8 @@ def test_library_exports_every_declared_function():
 
 def test_host_side_argument_errors_need_no_gpu():
     import verify_step_02_b300 as vs
-    assert vs.w12_row_bytes(688) == 352 and vs.w12_row_bytes(1) == 16 and vs.w12_row_bytes(32) == 16
+    assert vs.w12_plane_bytes(1, 1) == 4096 and vs.w12_plane_bytes(65, 129) == 4 * 4096
+    assert vs.w12_plane_bytes(6144, 4096) == 96 * 32 * 4096 and vs.w12_plane_bytes(0, 5) == 0
     h = ctypes.c_void_p()
     st = vs.lib.sv_model_create(None, None, None, ctypes.byref(h))
     assert st == vs.SV_ERR_INVALID_ARG and b"NULL" in vs.lib.sv_last_error()

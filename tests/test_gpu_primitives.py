@@ -97,19 +97,23 @@ def test_linear_matches_float64(kind, m):
             assert err2.max() < 1e-5, (n, k, err2.max())
 
 
+@pytest.mark.parametrize("kind", ["bf16", "w12"])
 @pytest.mark.parametrize("m,n,k", [(17, 6144, 4096), (17, 4096, 12288), (1, 4096, 4096), (33, 1000, 4096),
-                                   (187, 1280, 5120), (256, 512, 1024), (300, 384, 512)])
-def test_linear_bf16_projection_shapes(m, n, k):
+                                   (64, 1000, 4112), (187, 1280, 5120), (256, 512, 1024), (300, 384, 512)])
+def test_linear_projection_shapes(kind, m, n, k):
     """The skinny product at the decoder's projection sizes: many tiles, K shared by several CTAs,
-    ragged N, M beyond one 256-column accumulator; hi/lo pair activations as the verify step
-    passes them, against float64."""
+    ragged N and K, M beyond one 256-column accumulator; hi/lo pair activations as the verify
+    step passes them; bf16 weights or W12 planes rebuilt in the kernel; against float64."""
     rng = np.random.default_rng(m * 131 + n)
     bits = synth.w12_window_bits(rng, (n, k))
     w_dev, w64 = sd.bits_to_bf16(bits), bf16_bits_to_f64(bits)
+    wdtype, base = vs.SV_BF16, 0
+    if kind == "w12":
+        (w_dev, base), wdtype = vs.pack_w12(w_dev), vs.SV_W12
     xf = torch.from_numpy(rng.standard_normal((m, k)).astype(np.float32)).cuda()
     hi = xf.to(torch.bfloat16)
     lo = (xf - hi.float()).to(torch.bfloat16)
-    y, ws = vs.linear(vs.SV_BF16, w_dev, torch.stack([hi, lo]), n, k)
+    y, ws = vs.linear(wdtype, w_dev, torch.stack([hi, lo]), n, k, base=base)
     x2 = (hi.double() + lo.double()).cpu().numpy()
     want = x2 @ w64.T
     scale = np.sqrt((np.abs(x2) ** 2) @ (np.abs(w64) ** 2).T) + 1e-30
@@ -119,5 +123,5 @@ def test_linear_bf16_projection_shapes(m, n, k):
     # operand offset, a dropped K block or a lost lo plane gives errors of order 1e-3 .. 1.
     assert err.max() < 1e-4, err.max()
     # a second call on the same workspace gives the same bits (fixed-order split-K sums)
-    y2, _ = vs.linear(vs.SV_BF16, w_dev, torch.stack([hi, lo]), n, k, workspace=ws)
+    y2, _ = vs.linear(wdtype, w_dev, torch.stack([hi, lo]), n, k, base=base, workspace=ws)
     assert torch.equal(y, y2)

@@ -128,7 +128,9 @@ def test_tiny_token_forcing_32_steps():
     assert int(seq.item()) == st.length + len(emitted) - 1
 
 
-def test_bf16_gqa_ragged_batch_shuffled_pages():
+@pytest.mark.parametrize("kind", ["bf16", "w12"])
+def test_bf16_gqa_ragged_batch_shuffled_pages(kind):
+    """bf16 or W12 weights (both on the tensor-core GEMM: ffn is a multiple of 64)."""
     shape = dict(n_layers=2, d_model=512, n_heads=8, n_kv_heads=2, head_dim=128, ffn=1024, vocab=4096,
                  rope_theta=1e6)
     hw = synth.host_weights(shape, "w12window")
@@ -148,7 +150,7 @@ def test_bf16_gqa_ragged_batch_shuffled_pages():
         stt.v = [decoder.round_to_bf16(rng.standard_normal((c, 2, 128))) for _ in range(2)]
         states.append(stt)
     drafts = [[int(x) for x in rng.integers(0, cfg.vocab, size=n)] for n in lens]
-    model = make_model(shape, "bf16", gpu_weights(hw, "bf16"), 8, gamma, 512)
+    model = make_model(shape, kind, gpu_weights(hw, kind), 8, gamma, 512)
     ks, vs_, table, seq = build_kv(shape, states, PAGE, gamma, "bf16")
     kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
     acc, nxt, lg = run_step(model, states, drafts, gamma, kv)

@@ -70,7 +70,7 @@ def test_w12_exhaustive_single_elements():
             assert not want_ok, hex(int(b))
             continue
         assert want_ok, hex(int(b))
-        back = w12.unpack(planes, base, 1)
+        back = w12.unpack(planes, base, 1, 1)
         assert back[0, 0] == b
         ok += 1
     assert ok == int(((e >= 1) & (e <= 254)).sum())
@@ -85,7 +85,7 @@ def test_w12_window_rule_all_exponent_pairs():
                 planes, base = w12.pack(t)
                 assert fits
                 assert base == min(e1, e2)
-                assert (w12.unpack(planes, base, 2) == t).all()
+                assert (w12.unpack(planes, base, 1, 2) == t).all()
             except w12.NotRepresentable:
                 assert not fits
 
@@ -99,19 +99,36 @@ def test_w12_layout_hand_example():
     planes, base = w12.pack(t)
     assert base == 124
     # c = s<<11 | (E-base)<<7 | m:  c0 = 3<<7 = 0x180, c1 = 0x800|0x180|0x40 = 0x9c0, c2 = 0x040
-    assert planes.shape == (3, 1, 16)                      # row padded to 32 elements = 16 bytes
-    assert planes[0, 0, 0] == 0x00 and planes[0, 0, 1] == 0x00           # low nibbles
-    assert planes[1, 0, 0] == 0xC8 and planes[1, 0, 1] == 0x04           # bits 4..7: 8 | c<<4
-    assert planes[2, 0, 0] == 0x91 and planes[2, 0, 1] == 0x00           # bits 8..11: 1 | 9<<4
-    assert (planes[:, :, 2:] == 0).all()
-    assert (w12.unpack(planes, base, 3) == t).all()
+    # group 0's word: slot 0 = element 0, slot 1 = element 2 (byte 0); slot 4 = element 1 (byte 2)
+    assert planes.shape == (3, 4096)                       # one 64 x 128 tile per plane
+    assert (planes[0] == 0).all()                                          # bits 0..3 are all 0
+    assert planes[1, 0] == 0x48 and planes[1, 2] == 0x0C                  # bits 4..7: 8 | 4<<4; c1: C
+    assert planes[2, 0] == 0x01 and planes[2, 2] == 0x09                  # bits 8..11: 1 | 0<<4; c1: 9
+    assert planes[1, 1] == 0 and planes[2, 1] == 0 and planes[1, 3] == 0 and planes[2, 3] == 0
+    assert (planes[:, 4:] == 0).all()
+    assert (w12.unpack(planes, base, 1, 3) == t).all()
+
+
+def test_w12_tile_placement_hand_example():
+    # 65 x 131 matrix of +1.0 (code 0 with base 127) except element (64, 129) = -1.0
+    # (code 0x800: nibble 8 in plane 2). It lies in tile (rt 1, kt 1) of a 2 x 2 grid,
+    # tile row 0, group 0 (elements 128..135), element 1 of the group -> nibble slot 4,
+    # i.e. the low nibble of byte 2 of the word: byte (1 * 2 + 1) * 4096 + 0 * 64 + 2.
+    t = np.full((65, 131), 0x3F80, dtype=np.uint16)
+    t[64, 129] = 0xBF80
+    planes, base = w12.pack(t)
+    assert base == 127 and planes.shape == (3, w12.plane_bytes(65, 131)) == (3, 4 * 4096)
+    assert (planes[0] == 0).all() and (planes[1] == 0).all()
+    nz = np.flatnonzero(planes[2])
+    assert list(nz) == [3 * 4096 + 2] and planes[2, 3 * 4096 + 2] == 0x08
+    assert (w12.unpack(planes, base, 65, 131) == t).all()
 
 
 def test_w12_random_window_tensor_round_trip_and_values():
     import synth
     bits = synth.w12_window_bits(np.random.default_rng(3), (67, 688))
     planes, base = w12.pack(bits)
-    assert planes.shape == (3, 67, w12.row_bytes(688))
-    back = w12.unpack(planes, base, 688)
+    assert planes.shape == (3, w12.plane_bytes(67, 688))
+    back = w12.unpack(planes, base, 67, 688)
     assert (back == bits).all()
     assert np.array_equal(bf16_bits_to_f64(back), _ieee_value(bits))

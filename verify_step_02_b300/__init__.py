@@ -69,7 +69,7 @@ _SIGS = {
     "sv_model_sync_status": (_i32, [_vp, _vp]),
     "sv_model_set_timing": (_i32, [_vp, _i32]),
     "sv_model_timing": (_i32, [_vp, _vp, _vp]),
-    "sv_w12_row_bytes": (_i32, [_i64]),
+    "sv_w12_plane_bytes": (_i64, [_i64, _i64]),
     "sv_pack_w12": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i64), _vp]),
     "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "sv_linear_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
@@ -204,15 +204,15 @@ class Model:
         return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
 
 
-def w12_row_bytes(cols):
-    return int(lib.sv_w12_row_bytes(int(cols)))
+def w12_plane_bytes(rows, cols):
+    return int(lib.sv_w12_plane_bytes(int(rows), int(cols)))
 
 
 def pack_w12(bf16, stream=None):
-    """bf16 device tensor [rows, cols] -> (uint8 planes [3, rows, row_bytes], base). Raises SvError."""
+    """bf16 device tensor [rows, cols] -> (uint8 planes [3, plane_bytes], base). Raises SvError."""
     import torch
     rows, cols = bf16.shape
-    planes = torch.empty((3, rows, w12_row_bytes(cols)), dtype=torch.uint8, device=bf16.device)
+    planes = torch.empty((3, w12_plane_bytes(rows, cols)), dtype=torch.uint8, device=bf16.device)
     base, bad = ctypes.c_int32(), ctypes.c_int64()
     st = lib.sv_pack_w12(_ptr(bf16), rows, cols, _ptr(planes), ctypes.byref(base), ctypes.byref(bad),
                          _stream(stream))

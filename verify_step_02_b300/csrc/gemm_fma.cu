@@ -55,8 +55,9 @@ __device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, floa
         v[8 * j + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
       }
     }
-  } else {  // W12: bytes k/2 .. k/2+7 of each plane
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(a.w) + (long long)row * a.w12_ld + (k >> 1);
+  } else {  // W12: two 8-element groups of tile (row / 64, k / 128), tile row row % 64
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(a.w) +
+                          ((((long long)(row >> 6) * a.w12_kt + (k >> 7)) << 12) + (row & 63) * 64 + ((k & 127) >> 1));
     const uint2 p0 = __ldg(reinterpret_cast<const uint2*>(base));
     const uint2 p1 = __ldg(reinterpret_cast<const uint2*>(base + a.w12_plane));
     const uint2 p2 = __ldg(reinterpret_cast<const uint2*>(base + 2 * a.w12_plane));
@@ -66,7 +67,8 @@ __device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, floa
       const uint32_t b0 = h ? p0.y : p0.x, b1 = h ? p1.y : p1.x, b2 = h ? p2.y : p2.x;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t c = ((b2 >> (4 * e)) & 0xFu) << 8 | ((b1 >> (4 * e)) & 0xFu) << 4 | ((b0 >> (4 * e)) & 0xFu);
+        const int sh = 4 * ((e & 1) ? 4 + (e >> 1) : (e >> 1));  // nibble slot of element e
+        const uint32_t c = ((b2 >> sh) & 0xFu) << 8 | ((b1 >> sh) & 0xFu) << 4 | ((b0 >> sh) & 0xFu);
         const uint32_t bits = ((c & 0x7FFu) + ebase) | ((c & 0x800u) << 4);
         v[8 * h + e] = __uint_as_float(bits << 16);
       }

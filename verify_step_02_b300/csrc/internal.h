@@ -113,8 +113,8 @@ struct GemmArgs {
   int wdtype;              // SV_F32, SV_BF16, SV_W12
   const void* w;           // weights (W12: planes back to back)
   int w12_base;
-  int w12_ld;              // W12 bytes per plane row
-  long long w12_plane;     // W12 bytes per plane (rows * ld)
+  int w12_kt;              // W12: 128-element tiles per row
+  long long w12_plane;     // W12 bytes per plane
   int n_rows;              // rows of W
   int K;
   const void* x;           // activations [M][K]
@@ -223,6 +223,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // Tensor path (tcgen05, gemm_tc.cu) for bf16 weights with bf16 or hi/lo-pair x.
 // Weight maps: bf16 [rows][K], 64 x 64 boxes; x maps: bf16 [rows][K], 64 x 32
 // boxes; both 128-byte swizzled, zero fill outside the tensor.
+// bf16, or W12 whose gate|up row halves are whole plane tiles (ffn % 64 == 0);
+// after plan_gemm_tc, tc_stages >= 2 says the token tile fits shared memory.
+bool gemm_tc_supported(int wdtype, int pair, int ffn);
 void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count);
 size_t gemm_tc_partial_floats(const GemmArgs& a);
 size_t gemm_tc_counter_count(const GemmArgs& a);
@@ -252,10 +255,14 @@ cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_l
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s);
-cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int ld, int base, uint8_t* planes,
+// W12 planes: 64-row x 128-element tiles of 4096 bytes (see sv.h).
+inline long long w12_plane_bytes(long long rows, long long cols) {
+  return ((rows + 63) / 64) * ((cols + 127) / 128) * 4096;
+}
+cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int base, uint8_t* planes,
                             cudaStream_t s);
-cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, int ld,
-                              uint16_t* out, cudaStream_t s);
+cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, uint16_t* out,
+                              cudaStream_t s);
 cudaError_t launch_philox(unsigned long long seed, long long req, long long pos0, int stream_id, int n, float* out,
                           cudaStream_t s);
 

@@ -243,30 +243,43 @@ __device__ __forceinline__ unsigned w12_code(uint16_t b, int base) {
   return (unsigned)(b >> 15) << 11 | (((b >> 7) & 0xFFu) - (unsigned)base) << 7 | (b & 0x7Fu);
 }
 
-// One thread per plane byte column: elements 2c and 2c + 1 of a row.
-__global__ void w12_pack_kernel(const uint16_t* b, long long rows, long long cols, int ld, int base, uint8_t* planes) {
+// Element (within its group of 8) held by nibble slot s of a plane word: the
+// even elements in slots 0-3, the odd ones in slots 4-7.
+__device__ __forceinline__ int w12_slot_element(int s) { return s < 4 ? 2 * s : 2 * s - 7; }
+
+// Planes are tiled: 64 rows x 128 elements per 4096-byte tile, tile (rt, kt)
+// at byte (rt * kt_n + kt) * 4096, tile row r at r * 64 within it.
+// One thread per plane byte b: tile b / 4096, tile row (b % 4096) / 64, group
+// (b % 64) / 4, and nibble slots 2 (b % 4) and 2 (b % 4) + 1 of that group.
+__global__ void w12_pack_kernel(const uint16_t* b, long long rows, long long cols, int kt_n, long long plane_bytes,
+                                int base, uint8_t* planes) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= rows * ld) return;
-  const long long row = idx / ld, c = idx - row * ld;
-  const long long k0 = 2 * c, k1 = 2 * c + 1;
-  const unsigned c0 = k0 < cols ? w12_code(b[row * cols + k0], base) : 0u;
-  const unsigned c1 = k1 < cols ? w12_code(b[row * cols + k1], base) : 0u;
-  const long long plane = rows * ld;
+  if (idx >= plane_bytes) return;
+  const long long tile = idx >> 12;
+  const int within = static_cast<int>(idx & 4095);
+  const long long rt = tile / kt_n, kt = tile - rt * kt_n;
+  const long long row = rt * 64 + (within >> 6);
+  const int cb = within & 63;
+  const long long g0 = kt * 128 + (cb >> 2) * 8;
+  const int s0 = 2 * (cb & 3);
+  const long long k0 = g0 + w12_slot_element(s0), k1 = g0 + w12_slot_element(s0 + 1);
+  const unsigned c0 = row < rows && k0 < cols ? w12_code(b[row * cols + k0], base) : 0u;
+  const unsigned c1 = row < rows && k1 < cols ? w12_code(b[row * cols + k1], base) : 0u;
 #pragma unroll
   for (int p = 0; p < 3; ++p)
-    planes[p * plane + idx] = static_cast<uint8_t>(((c0 >> (4 * p)) & 0xFu) | ((c1 >> (4 * p)) & 0xFu) << 4);
+    planes[p * plane_bytes + idx] = static_cast<uint8_t>(((c0 >> (4 * p)) & 0xFu) | ((c1 >> (4 * p)) & 0xFu) << 4);
 }
 
-__global__ void w12_unpack_kernel(const uint8_t* planes, int base, long long rows, long long cols, int ld,
-                                  uint16_t* out) {
+__global__ void w12_unpack_kernel(const uint8_t* planes, int base, long long rows, long long cols, int kt_n,
+                                  long long plane_bytes, uint16_t* out) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * cols) return;
   const long long row = idx / cols, k = idx - row * cols;
-  const long long byte = row * ld + (k >> 1);
-  const int sh = (k & 1) * 4;
-  const long long plane = rows * ld;
-  const unsigned c = ((planes[byte] >> sh) & 0xFu) | ((planes[plane + byte] >> sh) & 0xFu) << 4 |
-                     ((planes[2 * plane + byte] >> sh) & 0xFu) << 8;
+  const int e = static_cast<int>(k & 7), slot = (e & 1) ? 4 + (e >> 1) : (e >> 1);
+  const long long byte = (((row >> 6) * kt_n + (k >> 7)) << 12) + (row & 63) * 64 + ((k & 127) >> 3) * 4 + (slot >> 1);
+  const int sh = (slot & 1) * 4;
+  const unsigned c = ((planes[byte] >> sh) & 0xFu) | ((planes[plane_bytes + byte] >> sh) & 0xFu) << 4 |
+                     ((planes[2 * plane_bytes + byte] >> sh) & 0xFu) << 8;
   out[idx] = static_cast<uint16_t>(((c & 0x7FFu) + ((unsigned)base << 7)) | ((c & 0x800u) << 4));
 }
 
@@ -306,17 +319,20 @@ cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigne
   return cudaGetLastError();
 }
 
-cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int ld, int base, uint8_t* planes,
+cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols, int base, uint8_t* planes,
                             cudaStream_t s) {
-  const long long n = rows * ld;
-  w12_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(bf16, rows, cols, ld, base, planes);
+  const int kt_n = static_cast<int>((cols + 127) / 128);
+  const long long n = w12_plane_bytes(rows, cols);
+  w12_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(bf16, rows, cols, kt_n, n, base, planes);
   return cudaGetLastError();
 }
 
-cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, int ld, uint16_t* out,
+cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, uint16_t* out,
                               cudaStream_t s) {
+  const int kt_n = static_cast<int>((cols + 127) / 128);
   const long long n = rows * cols;
-  w12_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(planes, base, rows, cols, ld, out);
+  w12_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(planes, base, rows, cols, kt_n,
+                                                                 w12_plane_bytes(rows, cols), out);
   return cudaGetLastError();
 }
 

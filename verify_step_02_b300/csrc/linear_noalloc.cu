@@ -61,8 +61,8 @@ extern "C" sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32
   a.wdtype = wdtype;
   a.w = w->data;
   a.w12_base = w->base;
-  a.w12_ld = static_cast<int>(((K + 31) / 32) * 16);
-  a.w12_plane = (long long)N * a.w12_ld;
+  a.w12_kt = (K + 127) / 128;
+  a.w12_plane = w12_plane_bytes(N, K);
   a.n_rows = N;
   a.x = x;
   a.x_kind = wdtype == SV_F32 ? kXF32 : (x_planes == 2 ? kXPair : kXBf16);

@@ -38,7 +38,6 @@ sv_status cuda_fail(cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
-int w12_row_bytes(long long cols) { return static_cast<int>(((cols + 31) / 32) * 16); }
 
 struct Timing {
   bool on = false;
@@ -192,8 +191,8 @@ GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const voi
   a.wdtype = m->cfg.weight_dtype;
   a.w = w.data;
   a.w12_base = w.base;
-  a.w12_ld = w12_row_bytes(K);
-  a.w12_plane = (long long)n_rows * a.w12_ld;
+  a.w12_kt = (K + 127) / 128;
+  a.w12_plane = w12_plane_bytes(n_rows, K);
   a.n_rows = n_rows;
   a.x = x;
   a.x_plane = x_plane;
@@ -222,11 +221,14 @@ void gemm_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part,
   }
 }
 
-void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part, size_t* cnt) {
+// The tensor path where it applies and fits, else the FMA path: the larger need of both.
+void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* part, size_t* cnt, int wdtype) {
+  gemm_ws_need(sm, m_max, n_units, K, pair, part, cnt);
   for (int M = 1; M <= m_max; ++M) {
     GemmArgs a;
     memset(&a, 0, sizeof a);
     a.x_kind = kXPair;
+    a.wdtype = wdtype;
     plan_gemm_tc(a, M, n_units, K, pair, sm);
     *part = std::max(*part, gemm_tc_partial_floats(a));
     *cnt = std::max(*cnt, gemm_tc_counter_count(a));
@@ -237,8 +239,12 @@ void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* pa
 sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair, int kc, cudaStream_t s,
                    const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr) {
   Timed t(m, kc, s);
-  if (m->use_tc) {
+  bool tc = m->use_tc && gemm_tc_supported(a.wdtype, pair, a.ffn);
+  if (tc) {
     plan_gemm_tc(a, M, n_units, K, pair, m->sm_count);
+    tc = a.tc_stages >= 2;
+  }
+  if (tc) {
     a.x_lo_row = m->m_max;
     SV_CUDA(launch_gemm_tc(a, *wmap, *xmap, s), what);
   } else {
@@ -431,7 +437,7 @@ extern "C" {
 
 const char* sv_last_error(void) { return g_err.c_str(); }
 
-int32_t sv_w12_row_bytes(int64_t cols) { return cols < 0 ? 0 : w12_row_bytes(cols); }
+int64_t sv_w12_plane_bytes(int64_t rows, int64_t cols) { return rows < 1 || cols < 1 ? 0 : w12_plane_bytes(rows, cols); }
 
 sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void* stream, sv_model** out) {
   if (!out) return fail(SV_ERR_INVALID_ARG, "out is NULL");
@@ -490,13 +496,18 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->req_row0, sizeof(int) * (c.max_batch + 1)));
   TRY(dalloc(m, &m->rope, sizeof(float2) * (size_t)c.max_seq_len * (c.head_dim / 2)));
   size_t part = 0, cnt = 0;
-  m->use_tc = cfg->weight_dtype == SV_BF16;
-  auto need = m->use_tc ? gemm_tc_ws_need : gemm_ws_need;
-  need(m->sm_count, M, nqkv(c), d, kPairNone, &part, &cnt);
-  need(m->sm_count, M, d, nq, kPairNone, &part, &cnt);
-  need(m->sm_count, M, c.ffn, d, kPairSwiglu, &part, &cnt);
-  need(m->sm_count, M, d, c.ffn, kPairNone, &part, &cnt);
-  need(m->sm_count, M, c.vocab, d, kPairNone, &part, &cnt);
+  m->use_tc = cfg->weight_dtype == SV_BF16 || cfg->weight_dtype == SV_W12;
+  auto need = [&](int n_units, int K, int pair) {
+    if (m->use_tc)
+      gemm_tc_ws_need(m->sm_count, M, n_units, K, pair, &part, &cnt, cfg->weight_dtype);
+    else
+      gemm_ws_need(m->sm_count, M, n_units, K, pair, &part, &cnt);
+  };
+  need(nqkv(c), d, kPairNone);
+  need(d, nq, kPairNone);
+  need(c.ffn, d, kPairSwiglu);
+  need(d, c.ffn, kPairNone);
+  need(c.vocab, d, kPairNone);
   TRY(dalloc(m, &m->gemm_part, sizeof(float) * part));
   TRY(dalloc(m, &m->gemm_cnt, sizeof(unsigned) * cnt));
   AttnArgs aa;
@@ -531,7 +542,8 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   if (m->use_tc) {
     cudaError_t me = cudaSuccess;
     auto enc_w = [&](CUtensorMap* mp, const sv_matrix& w, long long rows, int K) {
-      if (me == cudaSuccess) me = tc_encode_weight_map(mp, w.data, rows, K);
+      // bf16 weights stream through tensor maps; W12 planes through contiguous tile copies
+      if (me == cudaSuccess && cfg->weight_dtype == SV_BF16) me = tc_encode_weight_map(mp, w.data, rows, K);
     };
     const int L = c.n_layers;
     m->map_qkv.resize(L);
@@ -702,7 +714,7 @@ sv_status sv_pack_w12(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t*
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     bad += h[3];
   }
-  if (e == cudaSuccess && bad == 0) e = launch_w12_pack(bf16, rows, cols, w12_row_bytes(cols), base, planes, s);
+  if (e == cudaSuccess && bad == 0) e = launch_w12_pack(bf16, rows, cols, base, planes, s);
   cudaFreeAsync(stats, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "pack_w12");
@@ -716,8 +728,7 @@ sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64
                         void* stream) {
   if (!planes || !bf16_out) return fail(SV_ERR_INVALID_ARG, "NULL argument");
   if (rows < 1 || cols < 1 || base < 1 || base > 254) return fail(SV_ERR_INVALID_ARG, "bad sizes or base");
-  SV_CUDA(launch_w12_unpack(planes, base, rows, cols, w12_row_bytes(cols), bf16_out,
-                            static_cast<cudaStream_t>(stream)),
+  SV_CUDA(launch_w12_unpack(planes, base, rows, cols, bf16_out, static_cast<cudaStream_t>(stream)),
           "unpack_w12");
   return SV_OK;
 }
@@ -729,15 +740,18 @@ size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K
   cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
   GemmArgs a;
   memset(&a, 0, sizeof a);
-  if (wdtype == SV_BF16) {  // tensor path; the pair plan needs the most scratch
+  size_t need = 0;
+  if (wdtype == SV_BF16 || wdtype == SV_W12) {  // tensor path; the pair plan needs the most scratch
     a.x_kind = kXPair;
+    a.wdtype = wdtype;
     plan_gemm_tc(a, M, N, K, kPairNone, sm);
     const size_t cnt = (gemm_tc_counter_count(a) * sizeof(unsigned) + 255) & ~(size_t)255;
-    return cnt + gemm_tc_partial_floats(a) * sizeof(float);
+    need = cnt + gemm_tc_partial_floats(a) * sizeof(float);
   }
+  memset(&a, 0, sizeof a);  // the CUDA-core path (float32 weights, or a token tile too wide for the tensor path)
   plan_gemm(a, M, N, K, kPairNone, sm);
   const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
-  return cnt + gemm_partial_floats(a) * sizeof(float);
+  return std::max(need, cnt + gemm_partial_floats(a) * sizeof(float));
 }
 
 sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x, int32_t x_planes,
@@ -758,8 +772,8 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   a.wdtype = wdtype;
   a.w = w->data;
   a.w12_base = w->base;
-  a.w12_ld = w12_row_bytes(K);
-  a.w12_plane = (long long)N * a.w12_ld;
+  a.w12_kt = (K + 127) / 128;
+  a.w12_plane = w12_plane_bytes(N, K);
   a.n_rows = N;
   a.x = x;
   a.x_kind = wdtype == SV_F32 ? kXF32 : (x_planes == 2 ? kXPair : kXBf16);
@@ -767,17 +781,22 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   a.epi.kind = kEpiStore;
   a.epi.y = y;
   a.epi.ldy = N;
-  if (wdtype == SV_BF16) {
+  if (wdtype == SV_BF16 || wdtype == SV_W12) {
     plan_gemm_tc(a, M, N, K, kPairNone, sm);
-    const size_t cnt = (gemm_tc_counter_count(a) * sizeof(unsigned) + 255) & ~(size_t)255;
-    a.counters = static_cast<unsigned*>(workspace);
-    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + cnt);
-    a.x_lo_row = M;
-    CUtensorMap wm, xm;
-    SV_CUDA(tc_encode_weight_map(&wm, w->data, N, K), "weight tensor map");
-    SV_CUDA(tc_encode_x_map(&xm, x, (long long)x_planes * M, K), "x tensor map");
-    SV_CUDA(launch_gemm_tc(a, wm, xm, static_cast<cudaStream_t>(stream)), "linear");
-    return SV_OK;
+    if (a.tc_stages >= 2) {
+      const size_t cnt = (gemm_tc_counter_count(a) * sizeof(unsigned) + 255) & ~(size_t)255;
+      a.counters = static_cast<unsigned*>(workspace);
+      a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + cnt);
+      a.x_lo_row = M;
+      CUtensorMap xm, wm;
+      SV_CUDA(tc_encode_x_map(&xm, x, (long long)x_planes * M, K), "x tensor map");
+      if (wdtype == SV_BF16)
+        SV_CUDA(tc_encode_weight_map(&wm, w->data, N, K), "weight tensor map");
+      else
+        wm = xm;  // W12 planes are read by contiguous tile copies, not a tensor map
+      SV_CUDA(launch_gemm_tc(a, wm, xm, static_cast<cudaStream_t>(stream)), "linear");
+      return SV_OK;
+    }
   }
   plan_gemm(a, M, N, K, kPairNone, sm);
   const size_t cnt = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
