@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
     ap.add_argument("--sweep-dtype", choices=["bf16", "w12"], default="bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "sampled"], default="8b",
+                    help="8b: the headline line (default); the others time the other verify configurations "
+                         "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
+                         "batch 64) and print their own line")
     ap.add_argument("--layers", type=int, default=36,
                     help="decoder layers of the 8B-class model (36; fewer only for small profiling runs, "
                          "which the JSON line's config then names)")
@@ -574,11 +578,138 @@ def run_sweep(args, local):
             "peak_kind": peak_kind, "timing": "CUDA-graph replay of back-to-back launches", "shapes": out}
 
 
+# ------------------------------------------------------------------ the other configurations
+WORKLOADS = {
+    "tiny": "tiny fp32 greedy verify: 2 layers, d 256, 4 x 64 heads, vocab 1024; batch 1, gamma 4, context 64",
+    "27b": "27B-class bf16 ragged verify: 64 layers, d 5120, 40 q / 8 kv heads; batch 32, contexts uniform "
+           "512-8192 on shuffled 16-token pages, verify lengths 1-16 by confidence truncation; greedy",
+    "w12": "8B-class verify with W12 weights (16-binade window): batch 1, gamma 16, context 4096; greedy",
+    "sampled": "tiny fp32 sampled verify: batch 64, context 2048, gamma 8, T = 1, rejection sampling",
+}
+
+
+def run_workload(args, world, rank, local):
+    """Time one of the other verify configurations (timing only; parity is in the tests)."""
+    import torch
+
+    import synth
+    import synth.device as sd
+    import verify_step_02_b300 as vs
+
+    torch.cuda.set_device(local)
+    wl = args.workload
+    rng = np.random.default_rng(20261202)
+    steps_total = args.warmup + args.steps
+    temperature, probs = 0.0, None
+    if wl in ("tiny", "sampled"):
+        shape = synth.SHAPES["tiny"]
+        kind, wdtype, kvdt = "f32", vs.SV_F32, torch.float32
+        B, gamma = (1, 4) if wl == "tiny" else (64, 8)
+        ctx = np.full(B, 64 if wl == "tiny" else 2048)
+        lens = np.full(B, gamma)
+        wdev = sd.host_to_device_weights(synth.host_weights(shape, "f32"), "f32")
+    elif wl == "27b":
+        shape = synth.SHAPES["27b"]
+        kind, wdtype, kvdt = "bf16", vs.SV_BF16, torch.bfloat16
+        B, gamma = 32, 16
+        ctx = rng.integers(512, 8193, size=B)
+        lens = synth.truncated_verify_lens(B, gamma, 0.3, 31, 0)
+        wdev = sd.random_bf16_model(shape)
+    else:  # w12
+        shape = synth.SHAPES["8b"]
+        kind, wdtype, kvdt = "w12", vs.SV_W12, torch.bfloat16
+        B, gamma = 1, 16
+        ctx = np.full(B, CONTEXT)
+        lens = np.full(B, gamma)
+        wdev = sd.random_bf16_model(shape)
+
+        def w12(t, seed):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(seed)
+            bits = (torch.randint(0, 2, t.shape, device="cuda", generator=g, dtype=torch.int32) << 15) | \
+                (torch.randint(111, 127, t.shape, device="cuda", generator=g, dtype=torch.int32) << 7) | \
+                torch.randint(0, 128, t.shape, device="cuda", generator=g, dtype=torch.int32)
+            return vs.pack_w12(bits.to(torch.int16).view(torch.bfloat16))
+        for l, lay in enumerate(wdev["layers"]):
+            for i, name in enumerate(("wqkv", "wo", "wgu", "wd")):
+                lay[name] = w12(lay[name], 1000 * l + i)
+        wdev["lm_head"] = w12(wdev["lm_head"], 99999)
+    V = shape["vocab"]
+    lengths = [int(c) + steps_total * (gamma + 1) + 16 for c in ctx]
+    max_pages = max((n + PAGE - 1) // PAGE for n in lengths) + 1
+    table, n_pages = synth.shuffled_page_table(lengths, PAGE, max_pages, 77, 0)
+    ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, kvdt, fill="normal")
+    seq = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+    kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
+    max_seq = max(lengths) + 16
+    model = vs.Model(vs.make_config(shape, wdtype, B, gamma, max_seq, PAGE), wdev)
+    tok = torch.from_numpy(rng.integers(0, V, size=(B, gamma + 1)).astype(np.int32)).cuda()
+    if wl == "sampled":
+        temperature = 1.0
+        z = torch.randn((B, gamma, V), device="cuda") * 3.0
+        probs = torch.softmax(z, dim=-1).contiguous()
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    rid = torch.arange(B, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def run(i):
+        model.verify(tok, lens, kv, acc, nxt, draft_probs=probs, temperature=temperature, seed=1234 + i,
+                     request_ids=rid)
+
+    clocks = ClockSampler(local)
+    for i in range(args.warmup):
+        run(i)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    acc_sum = torch.zeros(B, dtype=torch.int64, device="cuda")
+    barrier(world)
+    torch.cuda.synchronize()
+    seq_start = seq.cpu().numpy().astype(np.int64)
+    ev[0].record(stream)
+    for j in range(args.steps):
+        run(args.warmup + j)
+        ev[j + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    seq_end = seq.cpu().numpy().astype(np.int64)
+    clk = clocks.stop()
+    per_step = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
+    t_ms = ev[0].elapsed_time(ev[-1])
+    tokens = float((seq_end - seq_start).sum())  # accepted drafts + 1 per request per step
+    value, t_max = aggregate(tokens, t_ms, world)
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peaks()
+    per_layer, wbytes, kv_row = step_bytes(shape)
+    wscale = {"f32": 2.0, "bf16": 1.0, "w12": 0.75}[kind]
+    kv_bytes = kv_row * (1.0 if kind != "f32" else 2.0)
+    M = int(np.sum(np.asarray(lens) + 1))
+    ctx_mean = (seq_start + seq_end) / 2.0
+    step_alg = wbytes * wscale + kv_bytes * float(np.sum(ctx_mean + np.asarray(lens) + 1)) + kv_bytes * M
+    ms_step = t_max / args.steps
+    return {
+        "metric": METRIC, "workload": wl, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "dtype": {"f32": "f32", "bf16": "bf16", "w12": "bf16 (W12 weights)"}[kind],
+        "data": "synthetic (random weights, random N(0,1) KV context, uniform random drafts)",
+        "config": {"workload": WORKLOADS[wl], "batch": B, "gamma": gamma, "M": M},
+        "verify_us": {"median": round(1e3 * statistics.median(per_step), 1),
+                      "p90": round(1e3 * float(np.percentile(per_step, 90)), 1)},
+        "tokens_per_step": round(tokens / args.steps, 3),
+        "hbm": {"bytes_per_step": step_alg, "gbs": round(step_alg / (ms_step * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(step_alg / (ms_step * 1e-3) / 1e9 / peak, 4), "peak_gbs": peak,
+                "peak_kind": peak_kind, "bound_ms": round(step_alg / (peak * 1e9) * 1e3, 4)},
+        "clocks": clk,
+    }
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.sweep != "none":
         res = run_sweep(args, local)
+    elif args.workload != "8b" and args.impl == "ours":
+        res = run_workload(args, world, rank, local)
     elif args.impl == "reference":
         res = run_reference(args, world, rank, local)
     else:

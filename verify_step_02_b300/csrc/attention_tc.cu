@@ -230,12 +230,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tmem_ld32(tS + lane_base + cg * 64, v);
       tmem_ld32(tS + lane_base + cg * 64 + 32, v + 32);
       float mp = -INFINITY;
+      if (k0 + cg * 64 + 63 <= C && ((vmask >> (cg * 4)) & 0xFu) == 0xFu) {
+        // every key of this column group is cached context on loaded pages: no mask
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int kk = cg * 64 + i;  // key within the chunk
-        const bool vis = k0 + kk <= lim && ((vmask >> (kk >> 4)) & 1u);
-        v[i] = vis ? v[i] : -INFINITY;
-        mp = fmaxf(mp, v[i]);
+        for (int i = 0; i < 64; ++i) mp = fmaxf(mp, v[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int kk = cg * 64 + i;  // key within the chunk
+          const bool vis = k0 + kk <= lim && ((vmask >> (kk >> 4)) & 1u);
+          v[i] = vis ? v[i] : -INFINITY;
+          mp = fmaxf(mp, v[i]);
+        }
       }
       red[cg * 128 + rho] = mp;
       sync();
