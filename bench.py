@@ -59,9 +59,9 @@ def parse():
                     help="8b: the headline line (default); the others time the other verify configurations "
                          "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
                          "batch 64) and print their own line")
-    ap.add_argument("--layers", type=int, default=36,
-                    help="decoder layers of the 8B-class model (36; fewer only for small profiling runs, "
-                         "which the JSON line's config then names)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decoder layers (default: the workload's own, 36 for the 8B-class model; fewer only "
+                         "for small profiling runs, which the JSON line's config then names)")
     return ap.parse_args()
 
 
@@ -252,7 +252,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     steps_total = args.warmup + args.steps
-    shape, wdev, kv, model, table = build_workload(3 * steps_total, args.layers)
+    shape, wdev, kv, model, table = build_workload(3 * steps_total, args.layers or 36)
     vocab = shape["vocab"]
     anchor = int(np.random.default_rng(20261202).integers(0, vocab))
     n_ref = int(steps_total * (1 + sum(P_KEEP ** (i + 1) for i in range(GAMMA))) * 1.5) + GAMMA + 8
@@ -340,7 +340,7 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random N(0,0.02) weights, random N(0,1) KV context, greedy-mix drafts)",
             "config": {"workload": "8B-class bf16 single-request verify, gamma 16 (M=17), context 4096, T=0",
-                       "batch": 1, "gamma": GAMMA, "context": CONTEXT, "layers": args.layers, "d_model": 4096,
+                       "batch": 1, "gamma": GAMMA, "context": CONTEXT, "layers": args.layers or 36, "d_model": 4096,
                        "vocab": 151936, "l2": "inputs larger than L2 (15.1 GB of weights per step)",
                        "parallelism": f"replicas x{world}"},
             "verify_us": {"median": round(1e3 * statistics.median(per_step), 1),
@@ -601,22 +601,26 @@ def run_workload(args, world, rank, local):
     rng = np.random.default_rng(20261202)
     steps_total = args.warmup + args.steps
     temperature, probs = 0.0, None
+
+    def shape_of(name):
+        sh = synth.SHAPES[name]
+        return dict(sh, n_layers=args.layers) if args.layers else sh
     if wl in ("tiny", "sampled"):
-        shape = synth.SHAPES["tiny"]
+        shape = shape_of("tiny")
         kind, wdtype, kvdt = "f32", vs.SV_F32, torch.float32
         B, gamma = (1, 4) if wl == "tiny" else (64, 8)
         ctx = np.full(B, 64 if wl == "tiny" else 2048)
         lens = np.full(B, gamma)
         wdev = sd.host_to_device_weights(synth.host_weights(shape, "f32"), "f32")
     elif wl == "27b":
-        shape = synth.SHAPES["27b"]
+        shape = shape_of("27b")
         kind, wdtype, kvdt = "bf16", vs.SV_BF16, torch.bfloat16
         B, gamma = 32, 16
         ctx = rng.integers(512, 8193, size=B)
         lens = synth.truncated_verify_lens(B, gamma, 0.3, 31, 0)
         wdev = sd.random_bf16_model(shape)
     else:  # w12
-        shape = synth.SHAPES["8b"]
+        shape = shape_of("8b")
         kind, wdtype, kvdt = "w12", vs.SV_W12, torch.bfloat16
         B, gamma = 1, 16
         ctx = np.full(B, CONTEXT)
@@ -672,6 +676,13 @@ def run_workload(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     seq_end = seq.cpu().numpy().astype(np.int64)
+    # per-kernel-class device time from an instrumented pass (events between launches)
+    model.set_timing(True)
+    for j in range(args.steps):
+        run(args.warmup + j)
+    torch.cuda.synchronize()
+    tim = model.timing()
+    model.set_timing(False)
     clk = clocks.stop()
     per_step = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
     t_ms = ev[0].elapsed_time(ev[-1])
@@ -692,13 +703,14 @@ def run_workload(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "dtype": {"f32": "f32", "bf16": "bf16", "w12": "bf16 (W12 weights)"}[kind],
         "data": "synthetic (random weights, random N(0,1) KV context, uniform random drafts)",
-        "config": {"workload": WORKLOADS[wl], "batch": B, "gamma": gamma, "M": M},
+        "config": {"workload": WORKLOADS[wl], "batch": B, "gamma": gamma, "M": M, "layers": shape["n_layers"]},
         "verify_us": {"median": round(1e3 * statistics.median(per_step), 1),
                       "p90": round(1e3 * float(np.percentile(per_step, 90)), 1)},
         "tokens_per_step": round(tokens / args.steps, 3),
         "hbm": {"bytes_per_step": step_alg, "gbs": round(step_alg / (ms_step * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(step_alg / (ms_step * 1e-3) / 1e9 / peak, 4), "peak_gbs": peak,
                 "peak_kind": peak_kind, "bound_ms": round(step_alg / (peak * 1e9) * 1e3, 4)},
+        "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in tim.items()},
         "clocks": clk,
     }
 

@@ -8,19 +8,32 @@
 // heads of one KV head (the GQA group) and all block rows of the request are
 // the MMA's 128 rows (rho = j * group + g), so every K/V byte is read once.
 //
-// One CTA = (request, kv head, 256-key chunk):
-//   warp 4   TMA: the chunk's K and V pages (16 keys x 64 dims per box, two
-//            boxes per page for hd 128) straight from the page pool;
-//            and the Q tile: the QKV epilogue left q / sqrt(hd) as a hi/lo
-//            bf16 pair (q = hi + lo to ~16 bits), which a 3D box (64 dims x
-//            group heads x block rows) lands as rows rho = j * group + g;
-//   warp 5   S = Q K^T (M 128, N 256, K hd; hi and lo into one accumulator);
-//   warps 0-3 read their row of S from TMEM, mask it (key <= C_r + j), take
-//            the chunk's max m and p = exp(s - m), sum l, and write P as a
-//            hi/lo bf16 pair over the (now consumed) Q and K buffers;
-//   warp 5   O = P V (M 128, N hd, K 256; V is the N-major operand);
-//   warps 0-3 write the partial (m, l, O) of their row.
-// A second kernel merges a row's chunk partials:
+// One CTA = (request, kv head, chunk of keys); the chunk (256 .. 4096 keys,
+// chosen by the host so the grid stays within a few waves) is processed in
+// sub-chunks of 64 keys through a three-stage K/V ring:
+//   warp 8   TMA: the Q tile once (the QKV epilogue left q / sqrt(hd) as a
+//            hi/lo bf16 pair, q = hi + lo to ~16 bits; a 3D box of 64 dims x
+//            group heads x block rows lands it as rows rho = j * group + g),
+//            the chunk's page-table entries once into shared memory, then
+//            each sub-chunk's K and V pages (16 keys x 64 dims per box)
+//            straight from the page pool into the free stage;
+//   warp 9   S_j = Q K_j^T (M 128, N 64, K hd; hi and lo into one
+//            accumulator; S buffer j mod 2 in TMEM) and O_b += P_j V_j
+//            (b = j mod 2; V is the N-major operand), S_{j+1} issued before
+//            O_b += P_j V_j;
+//   warps 0-7, two sets of four (set b takes the sub-chunks j = b mod 2, so
+//            the two softmaxes overlap): one thread per row reads the row's
+//            64 scores, masks them (key <= C_r + j), keeps the set's running
+//            maximum m_b and sum l_b, and writes P_j = exp(S_j - m_b) as a
+//            hi/lo bf16 pair into the set's P buffer once O_b += P_{j-2}
+//            V_{j-2} has completed. The maximum is raised only when a
+//            sub-chunk exceeds it by more than 8 (then O_b and l_b are
+//            rescaled by e^(m_old - m_new)); otherwise p <= e^8 and O_b, l_b
+//            stay exact in float32 relative to the kept m_b.
+// At the end each row merges its two sets' (m_b, l_b, O_b) through their
+// log-sum-exp and writes the chunk's partial (m, l, O).
+// The partial (m, l, O) of each row goes to a second kernel, which merges the
+// chunks of a row:
 //   out = sum_c O_c e^(m_c - M) / sum_c l_c e^(m_c - M), M = max_c m_c,
 // and writes the attention output as the next projection's x tensor.
 #include <cudaTypedefs.h>
@@ -34,8 +47,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kChunk = 256;
-constexpr int kRowWarps = 16;                         // softmax warps: 4 lane groups x 4 column groups
+constexpr int kSub = 64;                              // keys per sub-chunk
+constexpr int kStages = 3;                            // K/V ring depth
+constexpr int kMaxChunk = 4096;                       // keys per CTA at most
+constexpr int kMaxChunkPages = kMaxChunk / 16;
+constexpr int kSetWarps = 8;                          // a softmax set: two warps per 32-lane TMEM group
+constexpr int kSetThreads = kSetWarps * 32;
+constexpr int kRowWarps = 2 * kSetWarps;              // two sets, for even and odd sub-chunks
 constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kAttnThreads = kRowThreads + 64;        // + TMA warp + MMA warp
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -69,6 +87,13 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// 2^x by the SFU's approximate base-2 exponential (2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of 16-byte chunk `ch` (0..7) of row `row` in a 128-byte swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int row, int ch) {
   return static_cast<uint32_t>(row) * 128u + static_cast<uint32_t>((ch ^ (row & 7)) * 16);
@@ -78,21 +103,28 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const AttnArgs a) {
-  constexpr int NH = HD / 64;  // 64-dim halves of a head
-  // shared memory: [P region 128 KB: Q (2 NH tiles), K (NH x 2 tiles)] [V: NH x 2 tiles] [barriers]
-  constexpr uint32_t Q_OFF = 0, K_OFF = 2 * NH * kTile, V_OFF = 8 * kTile;
+  constexpr int NH = HD / 64;                     // 64-dim halves of a head
+  constexpr uint32_t QB = 2 * NH * kTile;         // Q: hi and lo planes, NH halves of 128 rows x 128 B
+  constexpr uint32_t KT = kSub * 128;             // a half-head tile of one sub-chunk: 64 keys x 128 B
+  constexpr uint32_t KVB = 2 * NH * KT;           // one stage: K (NH halves), then V (NH halves)
+  constexpr uint32_t PB = 2 * kTile;              // one set's P: hi and lo planes, 128 rows x 64 keys bf16
+  constexpr uint32_t KV_OFF = QB, P_OFF = QB + kStages * KVB;
+  constexpr uint32_t PM_OFF = P_OFF + 2 * PB;     // partial row maxima, bf16 [set][hf][128]
+  constexpr uint32_t BAR_OFF = PM_OFF + 2 * 2 * 2 * 128 + 4 * 16;  // + the pair wait flags
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + V_OFF + NH * 2 * kTile);
-  uint64_t* kv_full = bars;  // Q, K and V landed
-  uint64_t* s_full = bars + 2;
-  uint64_t* p_ready = bars + 3;
-  uint64_t* o_full = bars + 4;
-  uint64_t* drain = bars + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                // [kStages]
+  uint64_t* kv_empty = kv_full + kStages;      // [kStages]
+  uint64_t* s_full = kv_empty + kStages;       // [2]: S buffer b holds S_j, j = b mod 2
+  uint64_t* p_ready = s_full + 2;              // [2]: set b has read S_j and written P_j
+  uint64_t* pv_done = p_ready + 2;             // [2]: O_b += P_j V_j complete
+  uint64_t* o_full = pv_done + 2;
+  uint64_t* drain = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* s_flag = abort_flag + 1;
-  volatile uint32_t* valid_mask = reinterpret_cast<volatile uint32_t*>(abort_flag + 2);
+  volatile uint32_t* vmask_s = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // [kStages]: pages loaded
 
   pdl_trigger();
   pdl_wait();
@@ -102,15 +134,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
   if (C < 0 || T > a.max_seq_len) return;  // flagged by the row preparation
-  const int k0 = chunk * kChunk;
+  const int k0 = chunk * a.chunk;
   if (k0 >= T) return;
+  const int nkeys = T - k0 < a.chunk ? T - k0 : a.chunk;
+  const int nsub = (nkeys + kSub - 1) / kSub;
   const int R = nrows * group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
 
   if (tid == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, kRowThreads);
+    mbar_init(q_full, 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(kv_full + st, 1);
+      mbar_init(kv_empty + st, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_ready + b, kSetThreads);
+      mbar_init(pv_done + b, 1);
+    }
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -121,84 +162,141 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 256;
+  // S buffers at columns 0 and 64; set b's O at 128 + b * HD
+  const uint32_t tS = tmem, tO = tmem + 128;
 
   if (warp == kRowWarps) {
     // ------------------------------------------------------------ TMA producer
-    // lane p < 16 looks up page p of the chunk (all lookups in flight at once)
-    const int key = k0 + 16 * lane;
-    int page = -1;
-    if (lane < 16 && key < T) {
-      const int pidx = key >> 4;
-      page = pidx < a.max_pages ? a.page_table[static_cast<long long>(r) * a.max_pages + pidx] : -1;
-      if (page < 0 || page >= a.n_pages) {
-        atomicOr(a.status, kStBadPage);
-        page = -1;
-      }
-    }
-    const uint32_t mask = __ballot_sync(0xffffffffu, page >= 0);
+    const int* ptab = a.page_table + static_cast<long long>(r) * a.max_pages;
     if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
-      *valid_mask = mask;
       const uint32_t qbox = 128u * group * (a.max_rows / group);
-      mbar_arrive_expect_tx(kv_full, static_cast<uint32_t>(__popc(mask)) * NH * 2 * 2048u + 2 * NH * qbox);
+      mbar_arrive_expect_tx(q_full, 2 * NH * qbox);
       const uint64_t polq = policy_evict_last();
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_3d(smem + Q_OFF + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0,
-                      kv_full, polq);
+          tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0, q_full,
+                      polq);
     }
-    __syncwarp();
-    if (page >= 0) {  // the transaction count was raised above, before any of these copies
-      const uint64_t pol = policy_evict_first();
-      const int row = (page * nkv + h) * 16;
+    // the chunk's page ids, all lookups in flight at once: page i sits in
+    // lane i % 32, register i / 32; -1 for a bad entry
+    const int npg = (nkeys + 15) >> 4;
+    int pg[kMaxChunkPages / 32];
 #pragma unroll
-      for (int hh = 0; hh < NH; ++hh) {
-        tma_load_2d(smem + K_OFF + hh * 2 * kTile + lane * 2048, &tmk, hh * 64, row, kv_full, pol);
-        tma_load_2d(smem + V_OFF + hh * 2 * kTile + lane * 2048, &tmv, hh * 64, row, kv_full, pol);
+    for (int t = 0; t < kMaxChunkPages / 32; ++t) {
+      const int i = t * 32 + lane;
+      int page = -1;
+      if (i < npg) {
+        const int pidx = (k0 >> 4) + i;
+        page = pidx < a.max_pages ? ptab[pidx] : -1;
+        if (page < 0 || page >= a.n_pages) {
+          atomicOr(a.status, kStBadPage);
+          page = -1;
+        }
       }
+      pg[t] = page;
     }
-    if (lane == 0) {
-      volatile int never = 0;  // the copies land before the CTA can leave
-      mbar_wait(kv_full, 0, &never, kWaitNs);
+    const uint64_t pol = policy_evict_first();
+    int issued = 0;
+    for (int j = 0; j < nsub; ++j) {
+      const int st = j % kStages;
+      int ok = 1;
+      if (lane == 0 && j >= kStages) ok = mbar_wait(kv_empty + st, (j / kStages - 1) & 1, abort_flag, kWaitNs);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      // lane p < 4 takes page i = 4 j + p of the chunk, from lane i % 32,
+      // register i / 32 (the same register for the sub-chunk's four pages)
+      const int pi = j * (kSub / 16) + (lane & 3);
+      const int t_sel = (j * (kSub / 16)) >> 5;
+      int held = pg[0];
+#pragma unroll
+      for (int t = 1; t < kMaxChunkPages / 32; ++t) held = t == t_sel ? pg[t] : held;
+      int page = __shfl_sync(0xffffffffu, held, pi & 31);
+      if (lane >= kSub / 16 || pi >= npg) page = -1;
+      const uint32_t mask = __ballot_sync(0xffffffffu, page >= 0);
+      uint8_t* buf = smem + KV_OFF + st * KVB;
+      if (lane == 0) {
+        vmask_s[st] = mask;
+        mbar_arrive_expect_tx(kv_full + st, static_cast<uint32_t>(__popc(mask)) * NH * 2 * 2048u);
+      }
+      __syncwarp();
+      if (page >= 0) {  // the transaction count was raised above, before any of these copies
+        const int row = (page * nkv + h) * 16;
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          tma_load_2d(buf + hh * KT + lane * 2048, &tmk, hh * 64, row, kv_full + st, pol);
+          tma_load_2d(buf + (NH + hh) * KT + lane * 2048, &tmv, hh * 64, row, kv_full + st, pol);
+        }
+      }
+      ++issued;
+    }
+    if (lane == 0) {  // the copies land before the CTA can leave
+      volatile int never = 0;
+      mbar_wait(q_full, 0, &never, kWaitNs);
+      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
+        mbar_wait(kv_full + j % kStages, (j / kStages) & 1, &never, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kRowWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(kv_full, 0, abort_flag, kWaitNs);
-      if (ok) {
-        tc_fence_after();
-        const uint32_t q = smem_u32(smem + Q_OFF), k = smem_u32(smem + K_OFF);
-        constexpr uint32_t idesc_s = idesc_bf16_f32(128, kChunk);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kSub);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);  // B (V) is N-major
+      const uint32_t q = smem_u32(smem);
+      bool ok = mbar_wait(q_full, 0, abort_flag, kWaitNs);
+      auto issue_s = [&](int j) {
+        const int b = j & 1;
+        const uint32_t k = smem_u32(smem + KV_OFF + (j % kStages) * KVB);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const int kh = ks >> 2;
           const uint32_t off = (ks & 3) * 32;
-          const uint64_t b = smem_desc_sw128(k + kh * 2 * kTile + off);
-          mma_bf16(tS, smem_desc_sw128(q + kh * kTile + off), b, idesc_s, ks > 0 ? 1u : 0u);
-          mma_bf16(tS, smem_desc_sw128(q + (NH + kh) * kTile + off), b, idesc_s, 1u);
+          const uint64_t bd = smem_desc_sw128(k + kh * KT + off);
+          mma_bf16(tS + b * kSub, smem_desc_sw128(q + kh * kTile + off), bd, idesc_s, ks > 0 ? 1u : 0u);
+          mma_bf16(tS + b * kSub, smem_desc_sw128(q + (NH + kh) * kTile + off), bd, idesc_s, 1u);
         }
-        mma_commit(s_full);
-        ok = mbar_wait(p_ready, 0, abort_flag, kWaitNs);
+        mma_commit(s_full + b);
+      };
+      auto issue_pv = [&](int j) {
+        const int st = j % kStages, b = j & 1;
+        const uint32_t pb = smem_u32(smem + P_OFF + b * PB);
+        const uint32_t v = smem_u32(smem + KV_OFF + st * KVB + NH * KT);
+        const uint32_t to = tO + b * HD;
+#pragma unroll
+        for (int ks = 0; ks < kSub / 16; ++ks) {
+          const uint64_t bd = smem_desc_sw128_mn(v + ks * 2048, KT, 1024);
+          mma_bf16(to, smem_desc_sw128(pb + ks * 32), bd, idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
+          mma_bf16(to, smem_desc_sw128(pb + kTile + ks * 32), bd, idesc_o, 1u);
+        }
+        mma_commit(kv_empty + st);  // K_j / V_j no longer needed
+        mma_commit(pv_done + b);    // P_j no longer needed, O_b complete through j
+      };
+      for (int j = 0; j < nsub && ok; ++j) {
+        const int b = j & 1;
+        ok = mbar_wait(kv_full + j % kStages, (j / kStages) & 1, abort_flag, kWaitNs);
+        // S buffer b was last read by set b for sub-chunk j - 2
+        if (ok && j >= 2) ok = mbar_wait(p_ready + b, ((j >> 1) - 1) & 1, abort_flag, kWaitNs);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(j);
+        if (j >= 1) {
+          ok = mbar_wait(p_ready + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(j - 1);
+        }
       }
       if (ok) {
-        tc_fence_after();
-        const uint32_t pb = smem_u32(smem), v = smem_u32(smem + V_OFF);
-        constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);  // B (V) is N-major
-#pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-          const int kb = ks >> 2;
-          const uint32_t off = (ks & 3) * 32;
-          const uint64_t b = smem_desc_sw128_mn(v + ks * 2048, 2 * kTile, 1024);
-          mma_bf16(tO, smem_desc_sw128(pb + kb * kTile + off), b, idesc_o, ks > 0 ? 1u : 0u);
-          mma_bf16(tO, smem_desc_sw128(pb + (4 + kb) * kTile + off), b, idesc_o, 1u);
+        const int j = nsub - 1;
+        ok = mbar_wait(p_ready + (j & 1), (j >> 1) & 1, abort_flag, kWaitNs);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(j);
+          mma_commit(o_full);
         }
-        mma_commit(o_full);
       }
       mma_commit(drain);
       volatile int never = 0;
@@ -206,95 +304,172 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ rows: softmax, output
-    // warp w reads TMEM lanes 32 (w % 4) .. (its rows) and columns of group
-    // cg = w / 4: keys cg*64 .. cg*64+63 of S, dims cg*32 .. cg*32+31 of O
-    const int lg = warp & 3, cg = warp >> 2;
+    // set = warp / 8 takes sub-chunks j = set (mod 2); warp w reads TMEM lanes
+    // 32 (w % 4) ..; one thread per row rho and key half hf = (w / 4) mod 2:
+    // keys 32 hf .. 32 hf + 31 of each of the set's sub-chunks
+    const int set = warp >> 3, lg = warp & 3, hf = (warp >> 2) & 1;
     const int rho = lg * 32 + lane;
     const bool live = rho < R;
-    const int j = live ? rho / group : 0;
-    float* red = reinterpret_cast<float*>(bars + 8);  // [2][4][128]: partial max, partial sum
-    auto sync = [] { named_bar(1, kRowThreads); };
-    // (waiting on kv_full too makes the producer's page mask visible here)
-    if (tid == 0)
-      *s_flag = mbar_wait(kv_full, 0, abort_flag, kWaitNs) && mbar_wait(s_full, 0, abort_flag, kWaitNs) ? 1 : 0;
-    sync();
-    const bool ok = *s_flag != 0;
-    sync();
-    float m = -INFINITY, l = 0.f;
-    if (ok) {
-      tc_fence_after();
-      const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
-      const uint32_t vmask = *valid_mask;
-      const int lim = live ? C + j : -1;  // last key this row may see
-      float v[64];
-      tmem_ld32(tS + lane_base + cg * 64, v);
-      tmem_ld32(tS + lane_base + cg * 64 + 32, v + 32);
-      float mp = -INFINITY;
-      if (k0 + cg * 64 + 63 <= C && ((vmask >> (cg * 4)) & 0xFu) == 0xFu) {
-        // every key of this column group is cached context on loaded pages: no mask
+    const int lim = live ? C + rho / group : -1;  // last key this row may see
+    const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t to = tO + set * HD;
+    uint8_t* pt = smem + P_OFF + set * PB;
+    // partial maxima of the two warps of a row, truncated to bf16 so both warps
+    // take the same maximum: [set][hf][128]
+    uint16_t* pmax = reinterpret_cast<uint16_t*>(smem + PM_OFF);
+    volatile int* pok = reinterpret_cast<volatile int*>(smem + PM_OFF + 2 * 2 * 2 * 128);  // [set][hf][lg]
+    const int pair_bar = 1 + set * 4 + lg;  // named barrier of the row's two warps
+    float m = -INFINITY, l = 0.f;  // this set's running maximum; this warp's part of the sum
+    bool ok = true;
+    // a warp whose 32 rows are all padding only keeps the handshakes
+    const bool idle = lg * 32 >= R;
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int j = set; j < nsub; j += 2) {
+      const int st = j % kStages;
+      // (waiting on kv_full too makes the producer's page mask visible here)
+      int okw = 1;
+      if (lane == 0)
+        okw = mbar_wait(kv_full + st, (j / kStages) & 1, abort_flag, kWaitNs) &&
+              mbar_wait(s_full + set, (j >> 1) & 1, abort_flag, kWaitNs);
+      __syncwarp();
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (idle && !okw) {
+        ok = false;
+        break;
+      }
+      const uint32_t vmask = vmask_s[st];
+      const int kb = k0 + j * kSub + hf * 32;  // first key of this warp's half
+      float v[32];
+      float corr = 1.f;
+      if (!idle) {
+        // both warps of the row reach the pair barrier, and leave together if either failed
+        if (lane == 0) pok[(set * 2 + hf) * 4 + lg] = okw;
+        if (!okw) {
+          named_bar(pair_bar, 64);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld32(tS + lane_base + set * kSub + hf * 32, v);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (kb + 31 <= C && ((vmask >> (2 * hf)) & 3u) == 3u) {
+          // every key is cached context on a loaded page: no mask
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mp = fmaxf(mp, v[i]);
-      } else {
+          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int kk = cg * 64 + i;  // key within the chunk
-          const bool vis = k0 + kk <= lim && ((vmask >> (kk >> 4)) & 1u);
-          v[i] = vis ? v[i] : -INFINITY;
-          mp = fmaxf(mp, v[i]);
+          for (int i = 0; i < 32; ++i) {
+            const bool vis = kb + i <= lim && ((vmask >> (2 * hf + (i >> 4))) & 1u);
+            v[i] = vis ? v[i] : -INFINITY;
+            mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
+          }
+        }
+        const uint32_t own = __float_as_uint(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]))) >> 16;
+        pmax[(set * 2 + hf) * 128 + rho] = static_cast<uint16_t>(own);
+        named_bar(pair_bar, 64);
+        if (!pok[(set * 2 + (hf ^ 1)) * 4 + lg]) {
+          ok = false;
+          break;
+        }
+        const uint32_t other = pmax[(set * 2 + (hf ^ 1)) * 128 + rho];
+        const float mx = fmaxf(__uint_as_float(own << 16), __uint_as_float(other << 16));
+        // raise the kept maximum only when this sub-chunk exceeds it by more than 8
+        const float m_new = (m == -INFINITY || mx > m + 8.f) ? mx : m;
+        corr = (m == -INFINITY || m_new == m) ? 1.f : __expf(m - m_new);
+        m = m_new;
+        // p = 2^(s log2 e - m log2 e); masked keys (s = -inf) give 0
+        const float ml2 = m == -INFINITY ? 0.f : m * kLog2e;
+        float lp4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = ex2_approx(fmaf(v[i], kLog2e, -ml2));
+          lp4[i & 3] += v[i];
+        }
+        l = l * corr + ((lp4[0] + lp4[1]) + (lp4[2] + lp4[3]));
+      }
+      if (j >= set + 2) {
+        // O_set += P_{j-2} V_{j-2} has completed: P may be overwritten and O_set rescaled
+        if (lane == 0) mbar_wait(pv_done + set, (((j - set) >> 1) - 1) & 1, abort_flag, kWaitNs);
+        __syncwarp();
+      }
+      if (!idle) {
+        // P_j row rho: 16-byte chunk 4 hf + q holds keys 32 hf + 8 q .. + 7 (hi and lo tiles)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 hi, lo;
+          split8(v + 8 * q, hi, lo);
+          *reinterpret_cast<uint4*>(pt + sw128(rho, hf * 4 + q)) = hi;
+          *reinterpret_cast<uint4*>(pt + kTile + sw128(rho, hf * 4 + q)) = lo;
         }
       }
-      red[cg * 128 + rho] = mp;
-      sync();
-      m = fmaxf(fmaxf(red[rho], red[128 + rho]), fmaxf(red[256 + rho], red[384 + rho]));
-      float lp = 0.f;
+      if (j >= set + 2 && __any_sync(0xffffffffu, corr != 1.f)) {
+        // this warp rescales O_set's dims hf * HD / 2 .. + HD / 2
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < HD / 64; ++c) {
+          float o[32];
+          const uint32_t ta = to + lane_base + hf * (HD / 2) + c * 32;
+          tmem_ld32(ta, o);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        v[i] = v[i] == -INFINITY ? 0.f : __expf(v[i] - m);
-        lp += v[i];
-      }
-      red[512 + cg * 128 + rho] = lp;
-      // keys cg*64 .. +63 are key block cg of P: 8 16-byte chunks per plane
-#pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) {
-        uint4 hi, lo;
-        split8(v + 8 * c16, hi, lo);
-        *reinterpret_cast<uint4*>(smem + cg * kTile + sw128(rho, c16)) = hi;
-        *reinterpret_cast<uint4*>(smem + (4 + cg) * kTile + sw128(rho, c16)) = lo;
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(ta, o);
+        }
       }
       // V rows of keys past the request's end or on unloaded pages hold stale
       // bytes (possibly not finite); zero them so P = 0 there contributes 0
-      if (k0 + kChunk > T || vmask != 0xFFFFu)
-      for (int idx = tid; idx < kChunk * NH * 8; idx += kRowThreads) {
-        const int key_i = idx / (NH * 8), rem = idx - key_i * (NH * 8);
-        const int hh = rem >> 3, c16 = rem & 7;
-        if (k0 + key_i >= T || !((vmask >> (key_i >> 4)) & 1u))
-          *reinterpret_cast<uint4*>(smem + V_OFF + hh * 2 * kTile + key_i * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    mbar_arrive(p_ready);
-
-    if (tid == 0) *s_flag = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
-    sync();
-    const bool ok2 = *s_flag != 0;
-    if (ok2) {
-      tc_fence_after();
-      const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
-      const long long slot = (static_cast<long long>(blockIdx.x) * a.max_chunks + chunk) * a.max_rows + rho;
-      if (cg < HD / 32) {  // O dims cg*32 .. +31 (hd 64: column groups 0 and 1)
-        float4* po = reinterpret_cast<float4*>(a.partials + slot * HD + cg * 32);
-        float o[32];
-        tmem_ld32(tO + lane_base + cg * 32, o);
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) __stcg(po + i, make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+      const int kb0 = k0 + j * kSub;
+      if (kb0 + kSub > T || vmask != 0xFu) {
+        uint8_t* vb = smem + KV_OFF + st * KVB + NH * KT;
+        for (int idx = (warp & 7) * 32 + lane; idx < kSub * NH * 8; idx += kSetThreads) {
+          const int key_i = idx / (NH * 8), rem = idx - key_i * (NH * 8);
+          const int hh = rem >> 3, c16 = rem & 7;
+          if (kb0 + key_i >= T || !((vmask >> (key_i >> 4)) & 1u))
+            *reinterpret_cast<uint4*>(vb + hh * KT + key_i * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      if (live && cg == 0) {
-        l = red[512 + rho] + red[640 + rho] + red[768 + rho] + red[896 + rho];
-        __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(m, l));
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(p_ready + set);
+    }
+
+    // merge the two sets' (m, l, O) of each row, then write the chunk partial
+    int okw = 0;
+    if (lane == 0) okw = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
+    okw = __shfl_sync(0xffffffffu, okw, 0);
+    float2* xch = reinterpret_cast<float2*>(smem + P_OFF);  // P is free once O is complete: [set][hf][128]
+    if (okw) xch[(set * 2 + hf) * 128 + rho] = make_float2(m, l);
+    named_bar(9, kRowThreads);
+    if (okw) {
+      const float2 a0 = xch[rho], b0 = xch[128 + rho], a1 = xch[256 + rho], b1 = xch[384 + rho];
+      const float m0 = a0.x, l0 = a0.y + b0.y, m1 = a1.x, l1 = a1.y + b1.y;
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : __expf(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : __expf(m1 - M);
+      const bool has1 = nsub > 1;  // set 1 accumulated at least one P V product
+      const long long slot = (static_cast<long long>(blockIdx.x) * a.max_chunks + chunk) * a.max_rows + rho;
+      tc_fence_after();
+      // warp (set, hf) writes O dims (2 set + hf) HD / 4 .. + HD / 4 of the merged row
+      const int qd = (set * 2 + hf) * (HD / 4);
+#pragma unroll 1
+      for (int c = 0; c < HD / 64; ++c) {
+        const int col = qd + c * 16;
+        float o0[16], o1[16];
+        tmem_ld16(tO + lane_base + col, o0);
+        if (has1) tmem_ld16(tO + HD + lane_base + col, o1);
+        if (live) {
+          float4* po = reinterpret_cast<float4*>(a.partials + slot * HD + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float x[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              x[t] = (w0 != 0.f ? o0[4 * i + t] * w0 : 0.f) + (has1 && w1 != 0.f ? o1[4 * i + t] * w1 : 0.f);
+            __stcg(po + i, make_float4(x[0], x[1], x[2], x[3]));
+          }
+        }
       }
+      if (live && set == 0 && hf == 0)
+        __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(M, l0 * w0 + l1 * w1));
     }
   }
 
@@ -325,7 +500,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
   if (C < 0 || T > a.max_seq_len || rho >= nrows * group) return;
-  const int nchunks = (T + kChunk - 1) / kChunk;
+  const int nchunks = (T + a.chunk - 1) / a.chunk;
   const long long slot0 = static_cast<long long>(item) * a.max_chunks * a.max_rows + rho;
   const float2* ml = reinterpret_cast<const float2*>(a.partials + a.ml_offset) + slot0;
   float* w = s_w + warp * a.max_chunks;
@@ -373,8 +548,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
 }
 
 size_t attn_tc_smem(int hd) {
-  const int nh = hd / 64;
-  return 1024 + 8 * kTile + static_cast<size_t>(nh) * 2 * kTile + 8 * 8 + sizeof(float) * 2 * 4 * 128;
+  const size_t nh = hd / 64, q = 2 * nh * kTile, kv = 2 * nh * kSub * 128, pb = 2 * kTile;
+  return 1024 + q + kStages * kv + 2 * pb + 2 * 2 * 2 * 128 + 4 * 16 + (2 * kStages + 9) * 8 + 32;
 }
 
 template <int HD>
@@ -402,15 +577,24 @@ cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUte
 
 }  // namespace
 
+int attention_tc_chunk(int batch, int n_kv_heads, int max_seq_len, int sm_count) {
+  // keys per CTA: 256, doubled (up to 4096) while the grid would exceed two waves
+  int chunk = 256;
+  while (chunk < kMaxChunk &&
+         static_cast<long long>(batch) * n_kv_heads * ((max_seq_len + chunk - 1) / chunk) > 2LL * sm_count)
+    chunk *= 2;
+  return chunk;
+}
+
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len) {
-  const long long max_chunks = (static_cast<long long>(max_seq_len) + kChunk - 1) / kChunk;
+  const long long max_chunks = (static_cast<long long>(max_seq_len) + 255) / 256;
   return (head_dim == 64 || head_dim == 128) && page_size == 16 && max_rows <= 128 &&
          max_chunks * 8 * sizeof(float) <= 200 * 1024;
 }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
                                 const CUtensorMap& v, cudaStream_t s) {
-  if (a.chunk != kChunk || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
+  if (a.chunk < 256 || a.chunk > kMaxChunk || a.chunk % kSub || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
     return cudaErrorInvalidValue;
   return a.head_dim == 128 ? launch_hd<128>(a, B, q, k, v, s) : launch_hd<64>(a, B, q, k, v, s);
 }

@@ -236,6 +236,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtens
 // pages and at most 128 query rows per (request, kv head); KV maps: a layer's
 // pool as bf16 [n_pages * n_kv * 16][head_dim], 64 x 16 boxes.
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len);
+int attention_tc_chunk(int batch, int n_kv_heads, int max_seq_len, int sm_count);
 cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
 // q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
 cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,

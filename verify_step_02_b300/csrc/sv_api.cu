@@ -348,6 +348,8 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
+        a.chunk = attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
+        a.max_chunks = (c.max_seq_len + a.chunk - 1) / a.chunk;
         a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
