@@ -89,6 +89,7 @@ struct sv_model {
   // tensor path (bf16 weights): TMA maps of every weight matrix and of the x tensors
   bool use_tc = false;
   bool use_pdl = true;  // launch the step's kernels as programmatic dependents (overlapped prologues)
+  int attn_chunk = 0;   // keys per attention CTA (256 .. 4096, a multiple of 64); 0: chosen per launch
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
   CUtensorMap map_lm, map_u, map_ao, map_act;
   // tensor-core attention (bf16 KV): per-layer maps of the K and V page pools,
@@ -348,7 +349,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
-        a.chunk = attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
+        a.chunk = m->attn_chunk > 0 ? m->attn_chunk : attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
         a.max_chunks = (c.max_seq_len + a.chunk - 1) / a.chunk;
         a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
         Timed t(m, SV_KC_ATTENTION, s);
@@ -461,6 +462,10 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->w.layers = nullptr;
   m->wbf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
   if (const char* env = getenv("SV_PDL")) m->use_pdl = atoi(env) != 0;
+  if (const char* env = getenv("SV_ATTN_CHUNK")) {
+    const int v = atoi(env);
+    if (v >= 256 && v <= 4096 && v % 64 == 0) m->attn_chunk = v;
+  }
   m->x_pair = m->wbf16;
   int dev = 0;
   cudaGetDevice(&dev);
