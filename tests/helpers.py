@@ -52,7 +52,7 @@ def top2_gap(z):
     return float(t[1] - t[0])
 
 
-def judge_greedy(logits, drafts, k_gpu, next_gpu):
+def classify_greedy(logits, drafts, k_gpu, next_gpu):
     """'match', 'near_tie' or 'mismatch' for one request's greedy decision."""
     k_o, n_o = accept.greedy_accept(logits, drafts)
     if (k_o, n_o) == (int(k_gpu), int(next_gpu)):
@@ -63,7 +63,7 @@ def judge_greedy(logits, drafts, k_gpu, next_gpu):
     return "mismatch"
 
 
-def judge_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, next_gpu):
+def classify_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, next_gpu):
     u_acc, u_res = accept.uniforms(seed, req, start, len(drafts))
     k_o, n_o = accept.sampled_accept(logits, drafts, q, temperature, u_acc, u_res)
     if (k_o, n_o) == (int(k_gpu), int(next_gpu)):

@@ -21,7 +21,7 @@ import synth.device as sd  # noqa: E402
 import verify_step_02_b300 as vs  # noqa: E402
 from oracle import decoder  # noqa: E402
 
-from helpers import LOGIT_TOL, DeviceContext, device_oracle_weights, judge_greedy  # noqa: E402
+from helpers import LOGIT_TOL, DeviceContext, device_oracle_weights, classify_greedy  # noqa: E402
 
 PAGE = 16
 
@@ -58,7 +58,7 @@ def test_8b_gamma16_block_matches_oracle():
     lg = lg.cpu().numpy().astype(np.float64)
     err = np.abs(lg - lo).max()
     assert err <= LOGIT_TOL["bf16"], err
-    assert judge_greedy(lo, block[1:], acc[0], nxt[0]) in ("match", "near_tie")
+    assert classify_greedy(lo, block[1:], acc[0], nxt[0]) in ("match", "near_tie")
     assert int(seq.item()) == C + int(acc[0]) + 1
     pos = C + np.arange(gamma + 1)
     for l in (0, shape["n_layers"] - 1):
@@ -97,5 +97,5 @@ def test_27b_ragged_batch32_shuffled_pages():
         g = lg[row0[r]:row0[r + 1]].cpu().numpy().astype(np.float64)
         err = np.abs(g - lo).max()
         assert err <= LOGIT_TOL["bf16"], (r, err)
-        assert judge_greedy(lo, blocks[r][1:], acc[r], nxt[r]) in ("match", "near_tie")
+        assert classify_greedy(lo, blocks[r][1:], acc[r], nxt[r]) in ("match", "near_tie")
     model.close()

@@ -18,7 +18,7 @@ import synth.device as sd  # noqa: E402
 import verify_step_02_b300 as vs  # noqa: E402
 from oracle import accept, decoder, spec  # noqa: E402
 
-from helpers import (LOGIT_TOL, build_kv, judge_greedy, judge_sampled, oracle_weights,  # noqa: E402
+from helpers import (LOGIT_TOL, build_kv, classify_greedy, classify_sampled, oracle_weights,  # noqa: E402
                      torch_dtype)
 
 PAGE = 16
@@ -85,7 +85,7 @@ def test_tiny_single_step_rows_kv_and_commit(kind):
     acc, nxt, lg = run_step(model, [st], [drafts], gamma, kv)
     tol = LOGIT_TOL["f32" if kind == "f32" else "bf16"]
     assert np.abs(lg - lo).max() <= tol, np.abs(lg - lo).max()
-    assert judge_greedy(lo, drafts, acc[0], nxt[0]) in ("match", "near_tie")
+    assert classify_greedy(lo, drafts, acc[0], nxt[0]) in ("match", "near_tie")
     assert seq.cpu().numpy()[0] == st.length + int(acc[0]) + 1
     pos = st.length + np.arange(gamma + 1)
     for l in range(shape["n_layers"]):
@@ -159,7 +159,7 @@ def test_bf16_gqa_ragged_batch_shuffled_pages(kind):
         k_o, n_o, lo, _, _ = spec.verify(cfg, W, stt, drafts[r])
         rows = lens[r] + 1
         assert np.abs(lg[row:row + rows] - lo).max() <= LOGIT_TOL["bf16"], (r, np.abs(lg[row:row + rows] - lo).max())
-        assert judge_greedy(lo, drafts[r], acc[r], nxt[r]) in ("match", "near_tie")
+        assert classify_greedy(lo, drafts[r], acc[r], nxt[r]) in ("match", "near_tie")
         row += rows
     assert np.array_equal(seq.cpu().numpy(), np.array(ctx) + acc + 1)
 
@@ -204,7 +204,7 @@ def test_tiny_sampled_batch64_ctx2048():
     for r in range(B):
         lo = logits_o[r]
         assert np.abs(lg[r * (gamma + 1):(r + 1) * (gamma + 1)] - lo).max() <= LOGIT_TOL["f32"]
-        verdicts.append(judge_sampled(lo, drafts[r], probs[r], T, seed, 1000 + r, C, acc[r], nxt[r]))
+        verdicts.append(classify_sampled(lo, drafts[r], probs[r], T, seed, 1000 + r, C, acc[r], nxt[r]))
     assert "mismatch" not in verdicts, verdicts
     assert verdicts.count("near_tie") <= 2
     assert acc.sum() > 0
