@@ -285,6 +285,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the two elements' codes into its 16-bit lanes.
     const int cw = warp < 4 ? warp - 2 : warp - 6;   // 0 .. 5
     const int ct = cw * 32 + lane;
+    // thread ct converts the 8-element groups g = ct mod 16 (a 4-byte word of
+    // each plane, a 16-byte chunk of bf16) of rows r = ct / 16 + 12 k; a plane
+    // tile row is 64 bytes at r * 64 (the two 64-row halves are 4096 bytes apart)
+    const int g = ct & 15, r0 = ct >> 4;
+    const int q = g >> 3, c16 = g & 7;
     const uint32_t b2 = (static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u;
     int stage = 0;
     uint32_t phase = 0;
@@ -295,26 +300,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = mbar_wait(full + stage, phase, abort_flag, kWaitNs) &&
              mbar_wait(aempty + ai % kW12Ring, ((ai / kW12Ring) & 1) ^ 1u, abort_flag, kWaitNs);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const uint8_t* pl = smem + static_cast<size_t>(stage) * STAGE;
-      uint8_t* at = aring + (ai % kW12Ring) * NSUB * kABytes;
-#pragma unroll 4
-      for (int it = ct; it < 128 * 16; it += NCONV * 32) {
-        const int r = it >> 4, g = it & 15;
-        const int po = (r >> 6) * 4096 + (r & 63) * 64 + g * 4;
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(pl + po);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(pl + 8192 + po);
-        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(pl + 16384 + po);
+      const uint8_t* pw = smem + static_cast<size_t>(stage) * STAGE + r0 * 64 + g * 4;
+      uint8_t* aw = aring + (ai % kW12Ring) * NSUB * kABytes + q * kABytes;
+#pragma unroll 2
+      for (int r = r0; r < 128; r += NCONV * 2) {
+        const int po = (r - r0) * 64;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(pw + po);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(pw + 8192 + po);
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(pw + 16384 + po);
         // slots 0,2,4,6 hold elements 0,4,1,5; slots 1,3,5,7 hold 2,6,3,7
         const uint32_t X = (w0 & 0x0F0F0F0Fu) | ((w1 << 4) & 0xF0F0F0F0u);
         const uint32_t Y = ((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u);
         const uint32_t Z0 = w2 & 0x0F0F0F0Fu, Z1 = (w2 >> 4) & 0x0F0F0F0Fu;
-        const uint32_t cw[4] = {__byte_perm(X, Z0, 0x6240), __byte_perm(Y, Z1, 0x6240), __byte_perm(X, Z0, 0x7351),
-                                __byte_perm(Y, Z1, 0x7351)};  // elements (0,1) (2,3) (4,5) (6,7)
+        const uint32_t cw4[4] = {__byte_perm(X, Z0, 0x6240), __byte_perm(Y, Z1, 0x6240), __byte_perm(X, Z0, 0x7351),
+                                 __byte_perm(Y, Z1, 0x7351)};  // elements (0,1) (2,3) (4,5) (6,7)
+        // ((c & 0x7FF) + (base << 7)) | ((c & 0x800) << 4) per 16-bit lane, as
+        // (c + (base << 7)) + 15 (c & 0x800): the sign moves up by adding it 15
+        // more times, and the exponent sum stays below bit 15 for any code
+        // that packing accepted (base + e <= 254)
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = ((cw[j] & 0x07FF07FFu) + b2) | ((cw[j] << 4) & 0x80008000u);
-        const int q = g >> 3, c16 = g & 7;
-        *reinterpret_cast<uint4*>(at + q * kABytes + r * 128 + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < 4; ++j) o[j] = (cw4[j] & 0x08000800u) * 15u + (cw4[j] + b2);
+        *reinterpret_cast<uint4*>(aw + r * 128 + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
       __syncwarp();
