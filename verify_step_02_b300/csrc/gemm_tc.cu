@@ -311,16 +311,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // slots 0,2,4,6 hold elements 0,4,1,5; slots 1,3,5,7 hold 2,6,3,7
         const uint32_t X = (w0 & 0x0F0F0F0Fu) | ((w1 << 4) & 0xF0F0F0F0u);
         const uint32_t Y = ((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u);
-        const uint32_t Z0 = w2 & 0x0F0F0F0Fu, Z1 = (w2 >> 4) & 0x0F0F0F0Fu;
+        // p2 nibbles with the sign moved from bit 3 to bit 7 of the byte: after the
+        // byte permute a lane holds (c & 0x7FF) | (sign << 15)
+        const uint32_t Z0 = (w2 & 0x07070707u) | ((w2 << 4) & 0x80808080u);
+        const uint32_t Z1 = ((w2 >> 4) & 0x07070707u) | (w2 & 0x80808080u);
         const uint32_t cw4[4] = {__byte_perm(X, Z0, 0x6240), __byte_perm(Y, Z1, 0x6240), __byte_perm(X, Z0, 0x7351),
                                  __byte_perm(Y, Z1, 0x7351)};  // elements (0,1) (2,3) (4,5) (6,7)
-        // ((c & 0x7FF) + (base << 7)) | ((c & 0x800) << 4) per 16-bit lane, as
-        // (c + (base << 7)) + 15 (c & 0x800): the sign moves up by adding it 15
-        // more times, and the exponent sum stays below bit 15 for any code
-        // that packing accepted (base + e <= 254)
+        // ((c & 0x7FF) + (base << 7)) | (sign << 15) per 16-bit lane is one add: the
+        // exponent sum base + e <= 254 (any code that packing accepted) stays below bit 15
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = (cw4[j] & 0x08000800u) * 15u + (cw4[j] + b2);
+        for (int j = 0; j < 4; ++j) o[j] = cw4[j] + b2;
         *reinterpret_cast<uint4*>(aw + r * 128 + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
