@@ -14,14 +14,16 @@
 // the partial tiles in CTA order (a fixed order: results do not depend on
 // timing) and runs the projection's epilogue. No CTA waits on another.
 //
-// Roles inside a CTA (256 threads):
+// Roles inside a CTA (384 threads; W12 weights: 512):
 //   warp 0     one thread issues TMA loads of the weight tile (two 64-row
 //              boxes) and the x tile (32-row boxes per plane) into an S-stage
 //              shared-memory ring;
 //   warp 1     allocates the TMEM accumulators (two buffers of NT columns) and
 //              one thread issues tcgen05.mma (M 128, N NT, K 16) per stage;
 //   warps 4-7  read finished accumulators out of TMEM (warp w reads lanes
-//              32 (w % 4) ..), and write partial tiles or run the epilogue.
+//              32 (w % 4) ..), and write partial tiles or run the epilogue;
+//              warps 8-11 share the reduction and the epilogue (bf16), or
+//              with warps 2, 3 and 12-15 rebuild the W12 tiles.
 // Every wait is bounded; a wait that runs out sets the status word's timeout
 // bit and the whole CTA winds down (waits for its copies and MMAs in flight,
 // frees TMEM, returns).
@@ -40,6 +42,7 @@ namespace {
 using namespace tc;
 
 constexpr int kTcThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 epilogue (two warpgroups)
+constexpr int kTcThreadsW12 = 512;  // W12: warps 4-7 epilogue, warps 2, 3 and 8-15 rebuild weights
 constexpr int kEpiThreads = 256;
 constexpr int kYsLd = 33;                       // Ys row stride (floats)
 constexpr int kABytes = kGemmBN * 128;          // weight tile of one stage: 128 rows x 64 bf16
@@ -67,7 +70,7 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
 }
 
 template <int NT, bool PAIR, int KS, bool W12>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                    const GemmArgs a) {
   constexpr int BX = NT * 128;              // bytes of one x plane per 64-wide sub-tile
@@ -76,9 +79,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int XOFF = W12 ? kW12Planes : kABytes;      // x of sub-tile q at q * SUB + XOFF
   constexpr int NSUB = KS / 64;
   constexpr int STAGE = stage_bytes(NT, PAIR, KS, W12);
-  constexpr uint32_t TCOLS = tmem_cols(NT);
+  // hi/lo x planes: their tiles sit back to back in shared memory (rows 0 .. NT - 1,
+  // then NT .. 2 NT - 1), so one MMA of N = 2 NT reads the weight tile once and
+  // leaves W x_hi and W x_lo side by side in TMEM; the epilogue adds them
+  constexpr bool FUSE = PAIR && 2 * NT <= 256;
+  constexpr int ACC = FUSE ? 2 * NT : NT;               // accumulator columns per TMEM buffer
+  constexpr uint32_t TCOLS = tmem_cols(ACC);
   constexpr int EPT = W12 ? 128 : kEpiThreads;          // epilogue threads (W12: warps 8-11 rebuild weights)
-  constexpr int NCONV = 6;                              // W12 rebuild warps: 2, 3, 8 .. 11
+  constexpr int NCONV = kTcThreadsW12 / 32 - 6;         // W12 rebuild warps: 2, 3, 8 .. 15
   static_assert(!W12 || KS == 128, "W12 tiles are 128 elements wide");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBN, NT);
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBN, ACC);
       int stage = 0, seg = 0, ai = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int b = seg & 1;
         if (!mbar_wait(acc_empty + b, ((seg >> 1) & 1) ^ 1u, abort_flag, kWaitNs)) break;
         tc_fence_after();
-        const uint32_t d = tmem + b * NT;
+        const uint32_t d = tmem + b * ACC;
         for (long long v = u; v < uend; ++v) {
           // W12: the rebuild warps saw this stage land before they filled the tile
           if (!mbar_wait(W12 ? afull + ai % kW12Ring : full + stage, W12 ? (ai / kW12Ring) & 1 : phase, abort_flag,
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = smem_desc_sw128(sa + k * 32);
               mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || q > 0 || k > 0) ? 1u : 0u);
-              if (PAIR) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
+              if (PAIR && !FUSE) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
             }
           }
           mma_commit(empty + stage);  // frees the stage once these MMAs have read it
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, kDrainNs);
     }
-  } else if (W12 && (warp == 2 || warp == 3 || (warp >= 8 && warp < 12))) {
+  } else if (W12 && (warp == 2 || warp == 3 || warp >= 8)) {
     // ------------------------------------------------------------ W12 rebuild
     // Each unit's three plane tiles become the bf16 weight tile, in the
     // 128-byte swizzled layout the MMA reads: per element, code
@@ -283,10 +291,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // of 8 elements, X and Y hold p0 | p1 << 4 of the even and odd nibble
     // slots, Z0 and Z1 the p2 nibbles; one byte permute per output word puts
     // the two elements' codes into its 16-bit lanes.
-    const int cw = warp < 4 ? warp - 2 : warp - 6;   // 0 .. 5
+    const int cw = warp < 4 ? warp - 2 : warp - 6;   // 0 .. NCONV - 1
     const int ct = cw * 32 + lane;
     // thread ct converts the 8-element groups g = ct mod 16 (a 4-byte word of
-    // each plane, a 16-byte chunk of bf16) of rows r = ct / 16 + 12 k; a plane
+    // each plane, a 16-byte chunk of bf16) of rows r = ct / 16 + 2 NCONV k; a plane
     // tile row is 64 bytes at r * 64 (the two 64-row halves are 4096 bytes apart)
     const int g = ct & 15, r0 = ct >> 4;
     const int q = g >> 3, c16 = g & 7;
@@ -375,7 +383,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
       for (int ch = 0; ch * 32 < mtot; ++ch) {
         float v[32];
-        if (grpA) tmem_ld32(tmem + lane_base + b * NT + ch * 32, v);
+        if (grpA) {
+          tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
+          if (FUSE) {  // the lo plane's products
+            float w[32];
+            tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += w[i];
+          }
+        }
         if (alone) {
           if (grpA) {
 #pragma unroll
@@ -487,7 +503,8 @@ cudaError_t launch_ks(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_k(gemm_tc_kernel<NT, PAIR, KS, W12>, dim3(a.grid_p), dim3(kTcThreads), smem, s, a.pdl != 0, w, x,
+  return launch_k(gemm_tc_kernel<NT, PAIR, KS, W12>, dim3(a.grid_p), dim3(W12 ? kTcThreadsW12 : kTcThreads), smem, s,
+                  a.pdl != 0, w, x,
                   a);
 }
 
