@@ -236,8 +236,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtens
 // pages and at most 128 query rows per (request, kv head); KV maps: a layer's
 // pool as bf16 [n_pages * n_kv * 16][head_dim], 64 x 16 boxes.
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len);
-// Keys per CTA of a launch: 256, doubled (to 4096 at most) while the grid of
-// batch x n_kv_heads x chunks would exceed two waves of sm_count CTAs.
 int attention_tc_chunk(int batch, int n_kv_heads, int max_seq_len, int sm_count);
 cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
 // q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
