@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
     ap.add_argument("--sweep-dtype", choices=["bf16", "w12"], default="bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="after the timed steps, run two traced steps and add a per-kernel timeline summary "
+                         "(device %globaltimer per CTA) to the JSON line")
     ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "sampled"], default="8b",
                     help="8b: the headline line (default); the others time the other verify configurations "
                          "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
@@ -181,8 +184,57 @@ def traffic_record(kernel, workload, files):
     return rec.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------ device timeline
+LAYER_KERNELS = ("qkv", "attention", "attn_merge", "o", "gate_up", "down")
+
+
+def trace_summary(records, launches, n_layers):
+    """Per-kernel critical-path timeline of traced verify steps (microseconds).
+
+    records: uint64 [n, 8] per-CTA records; launches: [(first, ctas, kind)] in
+    launch order (the layer kernels of each step, then the LM head). For each
+    kernel, times are measured from the moment the previous kernel's last CTA
+    exited: its first CTA start, its median dependency-wait return, its median
+    first operands, its last MMA issue, and its last CTA exit (= the time it
+    adds to the step). Layer 0 is skipped (its predecessor is not traced).
+    """
+    per_step = 6 * n_layers + 1
+    names = []
+    for i in range(len(launches)):
+        j = i % per_step
+        names.append("lm_head" if j == per_step - 1 else LAYER_KERNELS[j % 6])
+    acc = {}
+    prev_exit = None
+    for i, (first, ctas, kind) in enumerate(launches):
+        r = records[first:first + ctas].astype(np.float64)
+        w = lambda k: r[:, k][r[:, k] > 0]
+        starts, waits, mma0, mma1, exits = w(1), w(2), w(3), w(4), w(6)
+        if len(exits) == 0:
+            prev_exit = None
+            continue
+        ex = exits.max()
+        j = i % per_step
+        if prev_exit is not None and j >= 6:
+            d = acc.setdefault(names[i], {k: [] for k in ("start", "wait", "first_mma", "last_mma", "exit")})
+            d["start"].append(starts.min() - prev_exit)
+            if len(waits):
+                d["wait"].append(np.median(waits) - prev_exit)
+            if len(mma0):
+                d["first_mma"].append(np.median(mma0) - prev_exit)
+            if len(mma1):
+                d["last_mma"].append(mma1.max() - prev_exit)
+            d["exit"].append(ex - prev_exit)
+        prev_exit = ex
+    out = {}
+    for name, d in acc.items():
+        out[name] = {k: round(float(np.mean(v)) / 1e3, 2) for k, v in d.items() if v}
+    layer_us = sum(out[n]["exit"] for n in LAYER_KERNELS if n in out)
+    return {"per_kernel_us_after_previous_exit": out, "layer_us": round(layer_us, 2),
+            "note": "device %globaltimer per CTA, means over layers 1.. of two traced steps"}
+
+
 # ------------------------------------------------------------------ workload
-def build_workload(steps_total, layers=36):
+def build_workload(steps_total, layers=36, flags=0):
     import torch
 
     import synth
@@ -197,9 +249,9 @@ def build_workload(steps_total, layers=36):
     ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, torch.bfloat16, fill="normal")
     seq = torch.tensor([CONTEXT], dtype=torch.int32, device="cuda")
     kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
-    cfg = vs.make_config(shape, vs.SV_BF16, 1, GAMMA, max_seq, PAGE)
+    cfg = vs.make_config(shape, vs.SV_BF16, 1, GAMMA, max_seq, PAGE, flags=flags)
     model = vs.Model(cfg, wdev)
-    return shape, wdev, kv, model, table
+    return shape, wdev, kv, model, table, cfg
 
 
 def greedy_reference(model, kv, anchor, n_tokens):
@@ -252,7 +304,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     steps_total = args.warmup + args.steps
-    shape, wdev, kv, model, table = build_workload(3 * steps_total, args.layers or 36)
+    shape, wdev, kv, model, table, cfg = build_workload(3 * steps_total, args.layers or 36)
     vocab = shape["vocab"]
     anchor = int(np.random.default_rng(20261202).integers(0, vocab))
     n_ref = int(steps_total * (1 + sum(P_KEEP ** (i + 1) for i in range(GAMMA))) * 1.5) + GAMMA + 8
@@ -306,18 +358,58 @@ def run_ours(args, world, rank, local):
     t_e2e = time.perf_counter() - t0
     barrier(world)
 
-    # ---- instrumented pass: per-kernel-class device time (events between launches)
+    # ---- instrumented pass: per-kernel-class device time from CUDA events around
+    # every launch, on a second engine over the same weights whose kernels run
+    # one after another (no programmatic dependent launch), so the classes add
+    # up to that pass's step time
+    import ctypes
+    cfg_np = vs.Config.from_buffer_copy(cfg)
+    cfg_np.flags |= vs.SV_FLAG_NO_PDL
+    model_np = vs.Model(cfg_np, wdev)
+    kv.seq_len.fill_(CONTEXT)
+
+    def run_np(i):
+        model_np.verify(blocks_d[i:i + 1], [GAMMA], kv, acc[i:i + 1], nxt[i:i + 1])
+    for i in range(args.warmup):
+        run_np(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for j in range(args.steps):
+        run_np(args.warmup + j)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_np = e0.elapsed_time(e1) / args.steps
     kv.seq_len.fill_(CONTEXT)
     for i in range(args.warmup):
-        run(i)
+        run_np(i)
     torch.cuda.synchronize()
-    model.set_timing(True)
+    model_np.set_timing(True)
     for j in range(args.steps):
-        run(args.warmup + j)
+        run_np(args.warmup + j)
     torch.cuda.synchronize()
-    tim = model.timing()
-    model.set_timing(False)
+    tim = model_np.timing()
+    model_np.set_timing(False)
+    model_np.close()
     clk = clocks.stop()
+
+    # ---- optional device timeline of two steps (the default engine)
+    trace = None
+    if args.trace:
+        n_layers = args.layers or 36
+        cap = 2 * (n_layers * (4 * 148 + 2 * 8 * 64) + 148 + 64)
+        recs = torch.zeros((cap, 8), dtype=torch.int64, device="cuda")
+        kv.seq_len.fill_(CONTEXT)
+        for i in range(args.warmup):
+            run(i)
+        torch.cuda.synchronize()
+        model.set_trace(recs)
+        for j in range(2):
+            run(args.warmup + j)
+        torch.cuda.synchronize()
+        launches = model.trace_launches()
+        model.set_trace(None)
+        trace = trace_summary(recs.cpu().numpy().view(np.uint64), launches, n_layers)
 
     value, t_max = aggregate(tokens, t_ms, world)
     e2e_all, _ = aggregate(e2e_tokens, t_e2e * 1e3, world)
@@ -354,8 +446,13 @@ def run_ours(args, world, rank, local):
                          "frac": round(achieved / peak, 4) if achieved else None, "traffic": traffic,
                          "peak_kind": peak_kind, "launches": gemm_n,
                          "bytes_per_launch": gemm_bytes_launch,
-                         "avg_launch_us": round(gemm_ms / gemm_n * 1e3, 2) if gemm_n else None},
+                         "avg_launch_us": round(gemm_ms / gemm_n * 1e3, 2) if gemm_n else None,
+                         "timing": "CUDA events around each launch in a pass without programmatic dependent "
+                                   "launch (each kernel alone, start to finish)"},
             "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in tim.items()},
+            "kernel_ms_timing": {"pass": "no programmatic dependent launch; events around every launch",
+                                 "ms_per_step_of_that_pass": round(ms_np, 4),
+                                 "sum_of_classes": round(sum(v[0] for v in tim.values()) / args.steps, 4)},
             "e2e": {"value": round(e2e_all, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * (GAMMA + 1),
                     "d2h_bytes_per_step": 8},
             "gpu_launches": int(round(launches * args.steps)),
@@ -363,6 +460,8 @@ def run_ours(args, world, rank, local):
             "near_tie_flips_vs_plan": flips,
             "clocks": clk,
         }
+        if trace is not None:
+            result["trace"] = trace
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(wdev, kv, table, blocks[args.warmup], tokens / args.steps)
     return result
@@ -431,68 +530,123 @@ def cpu_baseline(wdev, kv, table, block, tokens_per_step):
             "seconds_per_step": round(t_step, 3),
             "sample": "float64 numpy oracle forward of decoder layers 0-1 for one 17-row block at context 4096, "
                       "plus the full LM head; step time = 18 x (two-layer time) + LM-head time; tokens/step "
-                      "from the GPU run"}
+                      "from the GPU run (the same decode plan)"}
+
+
+def expected_tokens_per_step(p_keep=P_KEEP, gamma=GAMMA):
+    """Tokens per verify of the prefix rule when draft i (1-based) matches w.p. p^i, independently.
+
+    accepted >= i needs drafts 1..i all to match: P = prod_{j<=i} p^j = p^(i(i+1)/2); one more
+    token (correction or bonus) is always emitted.
+    """
+    return 1.0 + sum(p_keep ** (i * (i + 1) // 2) for i in range(1, gamma + 1))
+
+
+def reference_inputs(layers):
+    """Host inputs of the oracle sample, drawn like the GPU workload's, without the CUDA library.
+
+    The sampled layers' weights, the embedding and the LM head come from the same per-tensor
+    streams as synth.device.random_bf16_model (drawn on the device by torch, then copied to the
+    host); the context keys/values are N(0,1) rounded to bf16.
+    """
+    import torch
+
+    import synth
+    from oracle.decoder import Config, DenseWeights
+    shape = synth.SHAPES["8b"]
+    ms = synth.matrix_shapes(shape)
+    d = shape["d_model"]
+    bits = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    one = np.full(d, 0x3F80, np.uint16)  # bf16 1.0
+    host_layers = []
+    for l in layers:
+        host_layers.append({
+            "attn_norm": one, "mlp_norm": one,
+            "wqkv": bits(synth.device_bf16_normal(ms["wqkv"], 0.02, (l, synth.T_WQKV), "cuda")),
+            "wo": bits(synth.device_bf16_normal(ms["wo"], 0.02, (l, synth.T_WO), "cuda")),
+            "wgu": bits(synth.device_bf16_normal(ms["wgu"], 0.02, (l, synth.T_WGU), "cuda")),
+            "wd": bits(synth.device_bf16_normal(ms["wd"], 0.02, (l, synth.T_WD), "cuda")),
+        })
+    embed = bits(synth.device_bf16_normal((shape["vocab"], d), 0.02, (0, synth.T_EMBED), "cuda"))
+    lm = bits(synth.device_bf16_normal((shape["vocab"], d), 0.02, (0, synth.T_LM_HEAD), "cuda"))
+    torch.cuda.empty_cache()
+    cfg = Config(**dict(shape, n_layers=len(layers)), kv_dtype="bf16")
+    W = DenseWeights(cfg, host_layers, embed, one, lm, bf16=True)
+    rng = synth.rng(7, 0)
+    kvshape = (CONTEXT, shape["n_kv_heads"], shape["head_dim"])
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    ck = [to_bf16(rng.standard_normal(kvshape)) for _ in layers]
+    cv = [to_bf16(rng.standard_normal(kvshape)) for _ in layers]
+    return cfg, W, ck, cv
 
 
 def run_reference(args, world, rank, local):
-    """The CPU oracle on the same workload: each step runs one decoder layer of a verify block."""
+    """The CPU oracle on the same workload; each timed step runs one decoder layer of a verify block.
+
+    The oracle is the reference arm (the pages publish no code). A whole oracle step (36 layers and
+    the LM head of a 17-row block) takes minutes, so every step times one layer (layers 0 and 1
+    alternating) and the reported step time is extrapolated: 36 x that layer's time + the LM head's
+    time (measured once). The CUDA library is not loaded by this arm.
+    """
     if rank != 0:
         return None
     import torch
     torch.cuda.set_device(local)
-    shape, wdev, kv, model, table = build_workload(4)
-    vocab = shape["vocab"]
+    cfg, W, ck, cv = reference_inputs([0, 1])
     rng = np.random.default_rng(20261202)
-    block = [int(rng.integers(0, vocab))] + [int(x) for x in rng.integers(0, vocab, size=GAMMA)]
-    cfg, W, ck, cv = oracle_sample(wdev, kv, table, block, [0, 1])
-    model.close()
-    del wdev
-    torch.cuda.empty_cache()
+    block = [int(rng.integers(0, cfg.vocab))] + [int(x) for x in rng.integers(0, cfg.vocab, size=GAMMA)]
     t_head = time_oracle_head(W, len(block))
-    tokens_per_step = 1 + sum(P_KEEP ** (i + 1) for i in range(GAMMA))  # expected accepted + 1 of the draft rule
-    one = [cfg.__class__(**dict(cfg.__dict__, n_layers=1))]
-    times = []
+    tokens_per_step = expected_tokens_per_step()
+    one = cfg.__class__(**dict(cfg.__dict__, n_layers=1))
+
+    class OneLayer:
+        def __init__(self, w, l):
+            self.w, self.l, self.cfg = w, l, one
+
+        def embed(self, t):
+            return self.w.embed(t)
+
+        def layer(self, _):
+            return self.w.layer(self.l)
+
+        def final_norm(self):
+            return self.w.final_norm()
+
+        def logits(self, x, rowwise):
+            return np.zeros((x.shape[0], 1))
+
+    from oracle import decoder
+    layer_s = []
+    t_run0 = time.perf_counter()
     for s in range(args.warmup + args.steps):
         l = s % 2
-
-        class OneLayer:
-            def __init__(self, w, l):
-                self.w, self.l, self.cfg = w, l, one[0]
-
-            def embed(self, t):
-                return self.w.embed(t)
-
-            def layer(self, _):
-                return self.w.layer(self.l)
-
-            def final_norm(self):
-                return self.w.final_norm()
-
-            def logits(self, x, rowwise):
-                return np.zeros((x.shape[0], 1))
-
-        from oracle import decoder
         t0 = time.perf_counter()
-        decoder.forward_block(one[0], OneLayer(W, l), [ck[l]], [cv[l]], block, CONTEXT, rowwise=False)
-        dt = time.perf_counter() - t0
+        decoder.forward_block(one, OneLayer(W, l), [ck[l]], [cv[l]], block, CONTEXT, rowwise=False)
         if s >= args.warmup:
-            times.append(dt * 36 + t_head)
-    t_step = statistics.mean(times)
+            layer_s.append(time.perf_counter() - t0)
+    run_s = time.perf_counter() - t_run0
+    t_layer = statistics.mean(layer_s)
+    t_step = t_layer * 36 + t_head
     value = tokens_per_step / t_step
     cores = len(os.sched_getaffinity(0))
+    sample = ("per timed step: the float64 numpy oracle forward of one decoder layer (layers 0 and 1 "
+              "alternating) of one 17-row block at context 4096; the step time is extrapolated as 36 x the "
+              "mean layer time + the LM head's time (measured once); tokens/step = 1 + the expected accepted "
+              f"drafts of the workload's draft rule ({tokens_per_step:.3f})")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1),
+        "extrapolated_from": {"sample": "one decoder layer per timed step",
+                              "sample_ms_per_step": round(t_layer * 1e3, 1),
+                              "lm_head_ms": round(t_head * 1e3, 1), "scale": "36 layers + LM head",
+                              "timed_loop_s": round(run_s, 2)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (random N(0,0.02) weights, random N(0,1) KV context, random drafts)",
         "config": {"workload": "8B-class bf16 single-request verify, gamma 16 (M=17), context 4096, T=0",
                    "batch": 1, "gamma": GAMMA, "context": CONTEXT, "layers": 36, "d_model": 4096,
                    "vocab": 151936, "parallelism": "rank 0 only"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "per step: the float64 numpy oracle forward of one decoder layer (layers 0/1 "
-                                   "alternating) for one 17-row block at context 4096, x36, plus the LM head "
-                                   "time measured once; tokens/step = 1 + expected accepted drafts of the "
-                                   "draft rule (3.92)"},
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -87,6 +87,12 @@ typedef struct {
  * model's workspace (readable with sv_model_logits). Sampled verifies always
  * keep them. */
 #define SV_FLAG_KEEP_LOGITS 1
+/* Launch the step's kernels one after another, each starting when the one
+ * before it has finished. By default every kernel is a programmatic dependent
+ * of the previous one, so its prologue (barrier set-up, its first weight
+ * loads) overlaps the end of that kernel. With this flag the step is slower,
+ * but per-kernel event timing (sv_model_set_timing) adds up to the step. */
+#define SV_FLAG_NO_PDL 2
 
 /* A weight matrix [rows][cols] (the output-major layout y = x W^T).
  * F32/BF16: `data` is a dense row-major device array of that type.
@@ -203,6 +209,21 @@ sv_status sv_model_sync_status(sv_model* model, void* stream);
 enum { SV_KC_GEMM = 0, SV_KC_ATTENTION = 1, SV_KC_NORM = 2, SV_KC_LM_HEAD = 3, SV_KC_ACCEPT = 4, SV_KC_COUNT = 5 };
 sv_status sv_model_set_timing(sv_model* model, int32_t enable);
 sv_status sv_model_timing(sv_model* model, double* ms /* [SV_KC_COUNT] */, int64_t* launches /* [SV_KC_COUNT] */);
+
+/* Per-CTA device timeline, for measurement. While records != NULL, each
+ * traced kernel of a verify (the tensor-core projections, the tensor-core
+ * attention and its merge) writes one record of 8 uint64 words per CTA into
+ * `records` (device, capacity records, zero-filled by the caller): word 0 =
+ * kind << 48 | SM id << 32 | CTA index (kinds: 1 projection, 2 attention,
+ * 3 attention merge), words 1-6 = the %globaltimer value in ns when the CTA
+ * started, returned from its dependency wait, had its first operands, issued
+ * its last MMA, finished its epilogue, and exited (0 where a CTA has no such
+ * step). Launches that no longer fit are not traced. Setting a new buffer (or
+ * NULL, 0 to stop) restarts the count. sv_model_trace_launches writes
+ * (first record, CTAs, kind) for each traced launch, in launch order, into
+ * host int64 launches[3 * max_launches] and their number to *n_launches. */
+sv_status sv_model_set_trace(sv_model* model, uint64_t* records, int64_t capacity);
+sv_status sv_model_trace_launches(sv_model* model, int64_t* launches, int64_t max_launches, int64_t* n_launches);
 
 /*
  * W12 codec (SpecPilot digest, "Reasons": BF16 split into three 4-bit

@@ -20,7 +20,8 @@ lib = ctypes.CDLL(LIB_PATH)
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_NOT_REPRESENTABLE, SV_ERR_KV_CAPACITY = 0, 1, 2, 3
 SV_ERR_OUT_OF_MEMORY, SV_ERR_CUDA, SV_ERR_DEVICE_CHECK, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
 SV_F32, SV_BF16, SV_W12 = 0, 1, 2
-SV_FLAG_KEEP_LOGITS = 1
+SV_FLAG_KEEP_LOGITS, SV_FLAG_NO_PDL = 1, 2
+TRACE_KINDS = {1: "gemm", 2: "attention", 3: "attn_merge"}
 KERNEL_CLASSES = ("gemm", "attention", "norm", "lm_head", "accept")
 
 
@@ -69,6 +70,8 @@ _SIGS = {
     "sv_model_sync_status": (_i32, [_vp, _vp]),
     "sv_model_set_timing": (_i32, [_vp, _i32]),
     "sv_model_timing": (_i32, [_vp, _vp, _vp]),
+    "sv_model_set_trace": (_i32, [_vp, _vp, _i64]),
+    "sv_model_trace_launches": (_i32, [_vp, _vp, _i64, ctypes.POINTER(_i64)]),
     "sv_w12_plane_bytes": (_i64, [_i64, _i64]),
     "sv_pack_w12": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i64), _vp]),
     "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
@@ -202,6 +205,22 @@ class Model:
         n = (ctypes.c_int64 * 5)()
         _check(lib.sv_model_timing(self.handle, ms, n))
         return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+    def set_trace(self, records):
+        """records: zero-filled device uint64-sized tensor [capacity, 8], or None to stop tracing."""
+        if records is None:
+            _check(lib.sv_model_set_trace(self.handle, None, 0))
+        else:
+            _check(lib.sv_model_set_trace(self.handle, _ptr(records), int(records.shape[0])))
+
+    def trace_launches(self):
+        """[(first record, CTAs, kind name)] of the traced launches, in launch order."""
+        n = ctypes.c_int64()
+        _check(lib.sv_model_trace_launches(self.handle, None, 0, ctypes.byref(n)))
+        buf = (ctypes.c_int64 * max(1, 3 * n.value))()
+        _check(lib.sv_model_trace_launches(self.handle, buf, n.value, ctypes.byref(n)))
+        return [(buf[3 * i], buf[3 * i + 1], TRACE_KINDS.get(buf[3 * i + 2], str(buf[3 * i + 2])))
+                for i in range(n.value)]
 
 
 def w12_plane_bytes(rows, cols):

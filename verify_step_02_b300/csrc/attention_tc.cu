@@ -40,6 +40,7 @@
 
 #include "device_util.cuh"
 #include "internal.h"
+#include "prefetch.cuh"
 #include "tc_ptx.cuh"
 
 namespace sv {
@@ -126,6 +127,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* vmask_s = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // [kStages]: pages loaded
 
+  const int lin = blockIdx.y * gridDim.x + blockIdx.x, ncta = gridDim.x * gridDim.y;
+  unsigned long long* const rec = a.trace ? a.trace + static_cast<size_t>(lin) * kTraceWords : nullptr;
+  if (rec && threadIdx.x == 0) {
+    rec[0] = (static_cast<unsigned long long>(kTrAttn) << 48) | (static_cast<unsigned long long>(sm_id()) << 32) |
+             static_cast<unsigned>(lin);
+    trace_mark(rec, 1);
+  }
   pdl_trigger();
   pdl_wait();
   const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
@@ -133,13 +141,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int C = a.seq_len[r];
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
-  if (C < 0 || T > a.max_seq_len) return;  // flagged by the row preparation
   const int k0 = chunk * a.chunk;
-  if (k0 >= T) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (C < 0 || T > a.max_seq_len || k0 >= T) {
+    // no keys here (or a request flagged by the row preparation): this CTA
+    // only requests its share of the next product's weights into L2
+    if (warp == 0) l2_prefetch_window(a.pf, lin, ncta, lane);
+    if (tid == 0) trace_mark(rec, 6);
+    return;
+  }
+  if (tid == 0) trace_mark(rec, 2);
   const int nkeys = T - k0 < a.chunk ? T - k0 : a.chunk;
   const int nsub = (nkeys + kSub - 1) / kSub;
   const int R = nrows * group;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -233,6 +247,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       ++issued;
     }
+    // the K/V loads are issued; HBM has room for the next product's weights
+    l2_prefetch_window(a.pf, lin, ncta, lane);
     if (lane == 0) {  // the copies land before the CTA can leave
       volatile int never = 0;
       mbar_wait(q_full, 0, &never, kWaitNs);
@@ -277,6 +293,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < nsub && ok; ++j) {
         const int b = j & 1;
         ok = mbar_wait(kv_full + j % kStages, (j / kStages) & 1, abort_flag, kWaitNs);
+        if (j == 0) trace_mark(rec, 3);
         // S buffer b was last read by set b for sub-chunk j - 2
         if (ok && j >= 2) ok = mbar_wait(p_ready + b, ((j >> 1) - 1) & 1, abort_flag, kWaitNs);
         if (!ok) break;
@@ -298,6 +315,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_commit(o_full);
         }
       }
+      trace_mark(rec, 4);
       mma_commit(drain);
       volatile int never = 0;
       mbar_wait(drain, 0, &never, kDrainNs);
@@ -471,6 +489,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (live && set == 0 && hf == 0)
         __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(M, l0 * w0 + l1 * w1));
     }
+    if (tid == 0) trace_mark(rec, 5);
   }
 
   tc_fence_before();
@@ -479,7 +498,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (tid == 0 && *abort_flag) atomicOr(a.status, kStTimeout);
+  if (tid == 0) {
+    if (*abort_flag) atomicOr(a.status, kStTimeout);
+    trace_mark(rec, 6);
+  }
 }
 
 // One warp per (request, kv head, row): merge the row's chunk partials. Lanes
@@ -494,8 +516,17 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   const int item = blockIdx.x, r = item / nkv, h = item - r * nkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rho = blockIdx.y * 8 + warp;
+  unsigned long long* const rec =
+      a.trace_merge ? a.trace_merge + (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * kTraceWords
+                    : nullptr;
+  if (rec && threadIdx.x == 0) {
+    rec[0] = (static_cast<unsigned long long>(kTrMerge) << 48) | (static_cast<unsigned long long>(tc::sm_id()) << 32) |
+             (blockIdx.y * gridDim.x + blockIdx.x);
+    tc::trace_mark(rec, 1);
+  }
   pdl_trigger();
   pdl_wait();
+  if (rec && threadIdx.x == 0) tc::trace_mark(rec, 2);
   const int C = a.seq_len[r];
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
@@ -545,6 +576,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   const float invL = 1.0f / L;
 #pragma unroll
   for (int i = 0; i < D; ++i) store_x(a.out, a.out_plane, orow + i, o[i] * invL, a.x_pair);
+  if (rec && lane == 0) atomicMax(rec + 6, tc::global_ns());
 }
 
 size_t attn_tc_smem(int hd) {

@@ -1,0 +1,521 @@
+// Weight-streaming skinny GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// y[m][n] = x[m] . W[n] for bf16 weights W [rows][K] and bf16 activations, one
+// plane or a hi/lo pair (x = hi + lo: both planes are multiplied into the same
+// float32 accumulator). The verify block has M = sum(L_r + 1) rows, a few to a
+// few hundred, so W is the big operand: it is the MMA's A operand (128 weight
+// rows per tile, the MMA's M), and the block's tokens are its N (32 .. 256
+// columns). Every weight byte is read from HBM exactly once per launch.
+//
+// Work split ("stream-K"): the launch has P <= #SM CTAs and U = tiles x K
+// blocks of 64 units of work; CTA c takes units [c U / P, (c+1) U / P), so
+// every SM streams the same number of weight bytes. A tile whose K range is
+// shared by several CTAs is finished by the last of them to arrive, which sums
+// the partial tiles in CTA order (a fixed order: results do not depend on
+// timing) and runs the projection's epilogue. No CTA waits on another.
+//
+// Roles inside a CTA (384 threads; W12 weights: 512):
+//   warp 0     one thread issues TMA loads of the weight tile (two 64-row
+//              boxes) and the x tile (32-row boxes per plane) into an S-stage
+//              shared-memory ring;
+//   warp 1     allocates the TMEM accumulators (two buffers of NT columns) and
+//              one thread issues tcgen05.mma (M 128, N NT, K 16) per stage;
+//   warps 4-7  read finished accumulators out of TMEM (warp w reads lanes
+//              32 (w % 4) ..), and write partial tiles or run the epilogue;
+//              warps 8-11 share the reduction and the epilogue (bf16), or
+//              with warps 2, 3 and 12-15 rebuild the W12 tiles.
+// Every wait is bounded; a wait that runs out sets the status word's timeout
+// bit and the whole CTA winds down (waits for its copies and MMAs in flight,
+// frees TMEM, returns).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "epilogue.cuh"
+#include "gemm_tc_plan.h"
+#include "internal.h"
+#include "prefetch.cuh"
+#include "tc_ptx.cuh"
+
+namespace sv {
+namespace tcg {
+
+using namespace tc;
+
+constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s
+constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
+
+__host__ __device__ constexpr uint32_t tmem_cols(int nt) {
+  return 2 * nt <= 32 ? 32u : 2 * nt <= 64 ? 64u : 2 * nt <= 128 ? 128u : 2 * nt <= 256 ? 256u : 512u;
+}
+
+// First CTA whose unit range contains unit x: the largest c with floor(c U / P) <= x.
+__device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
+  return static_cast<int>(((x + 1) * P + U - 1) / U - 1);
+}
+
+template <int NT, bool PAIR, bool W12>
+__global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
+                   const GemmArgs a) {
+  constexpr int KS = tc_ks_for(NT, PAIR, W12);
+  constexpr int BX = NT * 128;              // bytes of one x plane per 64-wide sub-tile
+  constexpr int XQ = BX * (PAIR ? 2 : 1);   // x bytes per sub-tile
+  constexpr int SUB = W12 ? XQ : kABytes + XQ;          // one 64-wide sub-tile: (weights,) then x
+  constexpr int XOFF = W12 ? kW12Planes : kABytes;      // x of sub-tile q at q * SUB + XOFF
+  constexpr int NSUB = KS / 64;
+  constexpr int STAGE = stage_bytes(NT, PAIR, KS, W12);
+  // hi/lo x planes: their tiles sit back to back in shared memory (rows 0 .. NT - 1,
+  // then NT .. 2 NT - 1), so one MMA of N = 2 NT reads the weight tile once and
+  // leaves W x_hi and W x_lo side by side in TMEM; the epilogue adds them
+  constexpr bool FUSE = PAIR && 2 * NT <= 256;
+  constexpr int ACC = FUSE ? 2 * NT : NT;               // accumulator columns per TMEM buffer
+  constexpr uint32_t TCOLS = tmem_cols(ACC);
+  constexpr int EPT = W12 ? 128 : kEpiThreads;          // epilogue threads (W12: warps 8-11 rebuild weights)
+  constexpr int NCONV = kTcThreadsW12 / 32 - 6;         // W12 rebuild warps: 2, 3, 8 .. 15
+  static_assert(!W12 || KS == 128, "W12 tiles are 128 elements wide");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.tc_stages;
+  uint8_t* aring = smem + static_cast<size_t>(S) * STAGE;  // W12: rebuilt bf16 weight tiles, 2 x NSUB x 16 KB
+  float* Ys = reinterpret_cast<float*>(aring + (W12 ? kW12Ring * NSUB * kABytes : 0));
+  EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * kYsLd);
+  TokData* tok = reinterpret_cast<TokData*>(esm + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tok + 1);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint64_t* afull = drain + 1;     // W12 ring: rebuilt tile ready
+  uint64_t* aempty = afull + 2;    // W12 ring: tile consumed by the MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = a.grid_p, c = blockIdx.x;
+  const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
+  const long long u0 = c * U / P, u1 = (c + 1) * U / P;
+  unsigned long long* const rec = a.trace ? a.trace + static_cast<size_t>(c) * kTraceWords : nullptr;
+  if (rec && threadIdx.x == 0) {
+    rec[0] = (static_cast<unsigned long long>(kTrGemm) << 48) | (static_cast<unsigned long long>(sm_id()) << 32) |
+             static_cast<unsigned>(c);
+    trace_mark(rec, 1);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, W12 ? 1 + NCONV : 1);  // W12: the MMAs (x) and every rebuild warp (planes)
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(afull + i, NCONV);
+      mbar_init(aempty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(acc_full + i, 1);
+      mbar_init(acc_empty + i, 128);  // the TMEM-reading warpgroup
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    if (!W12) prefetch_tmap(&tmw);
+    prefetch_tmap(&tmx);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TCOLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+      // weight boxes, all sub-tiles back to back: each row's KS elements are
+      // requested together (contiguous bytes in HBM)
+      const int w12_row_blocks = (a.n_rows + 63) / 64;
+      // bytes one unit brings into its stage (W12: row halves past the matrix are not read)
+      auto unit_bytes = [&](long long u) -> uint32_t {
+        if (!W12) return STAGE;
+        const int nt = static_cast<int>(u / a.kb / a.m_tiles);
+        const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : nt * kGemmBN + kGemmBN / 2;
+        return STAGE - (r1 / 64 < w12_row_blocks ? 0 : 3 * 4096);
+      };
+      auto load_w = [&](long long u, uint8_t* st, uint64_t* bar) {
+        const long long t = u / a.kb;
+        const int kb = static_cast<int>(u - t * a.kb);
+        const int nt = static_cast<int>(t / a.m_tiles);
+        const int r0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
+        const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : r0 + kGemmBN / 2;
+        if constexpr (W12) {
+          // the planes' 4096-byte tiles (row block, kb) of both row halves: contiguous reads
+          const uint8_t* wb = static_cast<const uint8_t*>(a.w);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int rb = (hh ? r1 : r0) / 64;
+            if (rb >= w12_row_blocks) continue;
+            const long long off = (static_cast<long long>(rb) * a.w12_kt + kb) * 4096;
+#pragma unroll
+            for (int p = 0; p < 3; ++p)
+              bulk_load(st + p * 8192 + hh * 4096, wb + p * a.w12_plane + off, 4096, bar, pw);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < NSUB; ++q) {
+            tma_load_2d(st + q * SUB, &tmw, kb * KS + q * 64, r0, bar, pw);
+            tma_load_2d(st + q * SUB + kABytes / 2, &tmw, kb * KS + q * 64, r1, bar, pw);
+          }
+        }
+      };
+      auto load_x = [&](long long u, uint8_t* st, uint64_t* bar) {
+        const long long t = u / a.kb;
+        const int kb = static_cast<int>(u - t * a.kb);
+        const int mt = static_cast<int>(t - (t / a.m_tiles) * a.m_tiles);
+#pragma unroll
+        for (int q = 0; q < NSUB; ++q) {
+          uint8_t* sb = st + q * SUB + XOFF;
+          const int k = kb * KS + q * 64;
+#pragma unroll
+          for (int j = 0; j < NT / 32; ++j) {
+            tma_load_2d(sb + j * 4096, &tmx, k, mt * NT + j * 32, bar, px);
+            if (PAIR) tma_load_2d(sb + BX + j * 4096, &tmx, k, a.x_lo_row + mt * NT + j * 32, bar, px);
+          }
+        }
+      };
+      // The weights of the first stages do not depend on earlier kernels:
+      // request them before waiting for those kernels, then the activations.
+      const long long npre = u1 - u0 < S ? u1 - u0 : S;
+      for (long long i = 0; i < npre; ++i) {
+        uint8_t* st = smem + static_cast<size_t>(i) * STAGE;
+        mbar_arrive_expect_tx(full + i, unit_bytes(u0 + i));
+        load_w(u0 + i, st, full + i);
+      }
+      pdl_wait();
+      trace_mark(rec, 2);
+      for (long long i = 0; i < npre; ++i) load_x(u0 + i, smem + static_cast<size_t>(i) * STAGE, full + i);
+      int stage = static_cast<int>(npre % S);
+      uint32_t phase = npre == S ? 1u : 0u;
+      long long issued = npre;
+      for (long long u = u0 + npre; u < u1; ++u) {
+        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
+        uint8_t* st = smem + static_cast<size_t>(stage) * STAGE;
+        mbar_arrive_expect_tx(full + stage, unit_bytes(u));
+        load_w(u, st, full + stage);
+        load_x(u, st, full + stage);
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*abort_flag) {
+        // let the copies still in flight land before the CTA's shared memory goes away
+        volatile int never = 0;
+        const long long n = issued < S ? issued : S;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;  // issue number
+          mbar_wait(full + (q % S), static_cast<uint32_t>((q / S) & 1), &never, kDrainNs);
+        }
+      }
+    }
+    // every load of this CTA is issued: HBM would go idle through the tail, so
+    // request the next product's first weights into L2
+    __syncwarp();
+    if (!*abort_flag) l2_prefetch_window(a.pf, c, P, lane);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kGemmBN, ACC);
+      int stage = 0, seg = 0, ai = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1 && ok;) {
+        const long long t = u / a.kb;
+        const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+        const int b = seg & 1;
+        if (!mbar_wait(acc_empty + b, ((seg >> 1) & 1) ^ 1u, abort_flag, kWaitNs)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * ACC;
+        for (long long v = u; v < uend; ++v) {
+          // W12: the rebuild warps saw this stage land before they filled the tile
+          if (!mbar_wait(W12 ? afull + ai % kW12Ring : full + stage, W12 ? (ai / kW12Ring) & 1 : phase, abort_flag,
+                         kWaitNs)) {
+            ok = false;
+            break;
+          }
+          if (ai == 0) trace_mark(rec, 3);
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + static_cast<size_t>(stage) * STAGE);
+          const uint32_t at = smem_u32(aring + (ai % kW12Ring) * NSUB * kABytes);
+#pragma unroll
+          for (int q = 0; q < NSUB; ++q) {
+            const uint32_t sa = W12 ? at + q * kABytes : st + q * SUB, sb = st + q * SUB + XOFF;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc_sw128(sa + k * 32);
+              mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || q > 0 || k > 0) ? 1u : 0u);
+              if (PAIR && !FUSE) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
+            }
+          }
+          mma_commit(empty + stage);  // frees the stage once these MMAs have read it
+          if (W12) mma_commit(aempty + ai % kW12Ring);
+          ++ai;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(acc_full + b);
+        ++seg;
+        u = uend;
+      }
+      trace_mark(rec, 4);
+      // every MMA issued above has completed once `drain` flips
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, kDrainNs);
+    }
+  } else if (W12 && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ------------------------------------------------------------ W12 rebuild
+    // Each unit's three plane tiles become the bf16 weight tile, in the
+    // 128-byte swizzled layout the MMA reads: per element, code
+    // c = p0 | p1 << 4 | p2 << 8 and bf16 = ((c & 0x7FF) + (base << 7)) |
+    // ((c & 0x800) << 4), two elements per 32-bit word (SpecPilot digest,
+    // "Reasons": the planes are rebuilt to BF16 inside the GEMM). For a group
+    // of 8 elements, X and Y hold p0 | p1 << 4 of the even and odd nibble
+    // slots, Z0 and Z1 the p2 nibbles; one byte permute per output word puts
+    // the two elements' codes into its 16-bit lanes.
+    const int cw = warp < 4 ? warp - 2 : warp - 6;   // 0 .. NCONV - 1
+    const int ct = cw * 32 + lane;
+    // thread ct converts the 8-element groups g = ct mod 16 (a 4-byte word of
+    // each plane, a 16-byte chunk of bf16) of rows r = ct / 16 + 2 NCONV k; a plane
+    // tile row is 64 bytes at r * 64 (the two 64-row halves are 4096 bytes apart)
+    const int g = ct & 15, r0 = ct >> 4;
+    const int q = g >> 3, c16 = g & 7;
+    const uint32_t b2 = (static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u;
+    int stage = 0;
+    uint32_t phase = 0;
+    int ai = 0;
+    for (long long u = u0; u < u1; ++u, ++ai) {
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait(full + stage, phase, abort_flag, kWaitNs) &&
+             mbar_wait(aempty + ai % kW12Ring, ((ai / kW12Ring) & 1) ^ 1u, abort_flag, kWaitNs);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint8_t* pw = smem + static_cast<size_t>(stage) * STAGE + r0 * 64 + g * 4;
+      uint8_t* aw = aring + (ai % kW12Ring) * NSUB * kABytes + q * kABytes;
+#pragma unroll 2
+      for (int r = r0; r < 128; r += NCONV * 2) {
+        const int po = (r - r0) * 64;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(pw + po);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(pw + 8192 + po);
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(pw + 16384 + po);
+        // slots 0,2,4,6 hold elements 0,4,1,5; slots 1,3,5,7 hold 2,6,3,7
+        const uint32_t X = (w0 & 0x0F0F0F0Fu) | ((w1 << 4) & 0xF0F0F0F0u);
+        const uint32_t Y = ((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u);
+        // p2 nibbles with the sign moved from bit 3 to bit 7 of the byte: after the
+        // byte permute a lane holds (c & 0x7FF) | (sign << 15)
+        const uint32_t Z0 = (w2 & 0x07070707u) | ((w2 << 4) & 0x80808080u);
+        const uint32_t Z1 = ((w2 >> 4) & 0x07070707u) | (w2 & 0x80808080u);
+        const uint32_t cw4[4] = {__byte_perm(X, Z0, 0x6240), __byte_perm(Y, Z1, 0x6240), __byte_perm(X, Z0, 0x7351),
+                                 __byte_perm(Y, Z1, 0x7351)};  // elements (0,1) (2,3) (4,5) (6,7)
+        // ((c & 0x7FF) + (base << 7)) | (sign << 15) per 16-bit lane is one add: the
+        // exponent sum base + e <= 254 (any code that packing accepted) stays below bit 15
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = cw4[j] + b2;
+        *reinterpret_cast<uint4*>(aw + r * 128 + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(afull + ai % kW12Ring);
+        mbar_arrive(empty + stage);  // planes consumed
+      }
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else if (warp >= 4 && warp < 4 + EPT / 32) {
+    // ------------------------------------------------------------ epilogue
+    // Warpgroup A (warps 4-7) reads the accumulators out of TMEM (warp w reads
+    // lanes 32 (w % 4) ..) and writes partial tiles; with two warpgroups both
+    // share the split reduction (16 columns each) and the tile epilogue.
+    pdl_wait();  // reads what earlier kernels wrote (h, norm statistics, row maps)
+    const int et2 = threadIdx.x - 128;          // 0 .. EPT - 1
+    const bool grpA = et2 < 128;
+    const int et = et2 & 127;                   // tile row
+    // per-token data of the whole launch, while the weights stream in
+    const TokData* td = a.M <= kTokMax ? tok : nullptr;
+    if (td)
+      for (int m = et2; m < a.M; m += EPT) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
+    auto sync = [] { named_bar(1, EPT); };
+    sync();
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int slot0_tile = static_cast<int>(u0 / a.kb);
+    int seg = 0;
+    for (long long u = u0; u < u1;) {
+      const long long t = u / a.kb;
+      const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+      const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
+      const int b = seg & 1;
+      // one thread waits and broadcasts, so all threads agree on the outcome
+      if (et2 == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
+      sync();
+      const bool ok = *s_flag != 0;
+      sync();
+      if (!ok) break;
+      tc_fence_after();
+      const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
+      const bool alone = cf == cl;
+      const int m_base = mt * NT;
+      const int mtot = a.M - m_base < NT ? a.M - m_base : NT;
+      const int slot = static_cast<int>(t) == slot0_tile ? 0 : 1;
+      // partial tiles are column-major ([token][tile row]) so that a warp's
+      // stores and the reducer's loads are 128-byte coalesced
+      float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
+      for (int ch = 0; ch * 32 < mtot; ++ch) {
+        float v[32];
+        if (grpA) {
+          tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
+          if (FUSE) {  // the lo plane's products
+            float w[32];
+            tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += w[i];
+          }
+        }
+        if (alone) {
+          if (grpA) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
+          }
+          sync();
+          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2, EPT,
+                        *esm, td, sync);
+          sync();
+        } else if (grpA) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) __stcg(mine + (ch * 32 + i) * kGemmBN, v[i]);
+        }
+      }
+      if (grpA) {
+        tc_fence_before();
+        mbar_arrive(acc_empty + b);
+      }
+      if (!alone) {
+        epilogue_prefetch(a, nt, m_base, mtot < 32 ? mtot : 32, et, td);
+        __threadfence();
+        sync();
+        if (et2 == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
+        sync();
+        const bool last = *s_flag != 0;
+        sync();
+        if (last) {
+          __threadfence();
+          // the contributors' slots, in CTA order (a fixed summation order): a
+          // tile is the first tile (slot 0) of every contributor after cf, and of
+          // cf when cf's range starts at the tile's first unit
+          const int ncon = cl - cf + 1;
+          const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
+          constexpr int RW = 32 / (EPT / 128);  // columns of a chunk each warpgroup sums
+          const int col0 = grpA ? 0 : RW;
+          constexpr int NB = W12 ? 1 : 4;  // contributors whose loads are in flight together
+          for (int ch = 0; ch * 32 < mtot; ++ch) {
+            float s[RW];
+#pragma unroll
+            for (int i = 0; i < RW; ++i) s[i] = 0.f;
+            for (int j0 = 0; j0 < ncon; j0 += NB) {
+              float v[NB][RW];
+#pragma unroll
+              for (int jj = 0; jj < NB; ++jj) {
+                const int j = j0 + jj;
+                if (j < ncon) {
+                  const int sl = j == 0 ? sl_first : 0;
+                  const float* src = a.partials + (static_cast<size_t>(cf + j) * 2 + sl) * kGemmBN * NT + et;
+#pragma unroll
+                  for (int i = 0; i < RW; ++i) v[jj][i] = __ldcg(src + (ch * 32 + col0 + i) * kGemmBN);
+                }
+              }
+              // summed in CTA order, whatever the loads' completion order
+#pragma unroll
+              for (int jj = 0; jj < NB; ++jj)
+                if (j0 + jj < ncon) {
+#pragma unroll
+                  for (int i = 0; i < RW; ++i) s[i] += v[jj][i];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RW; ++i) Ys[et * kYsLd + col0 + i] = s[i];
+            sync();
+            epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2, EPT,
+                          *esm, td, sync);
+            sync();
+          }
+          if (et2 == 0) a.counters[t] = 0u;
+        }
+      }
+      ++seg;
+      u = uend;
+    }
+    if (et2 == 0) trace_mark(rec, 5);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TCOLS);
+  }
+  if (threadIdx.x == 0) {
+    if (*abort_flag && a.epi.status) atomicOr(a.epi.status, kStTimeout);
+    trace_mark(rec, 6);
+  }
+}
+
+template <int NT, bool PAIR, bool W12>
+cudaError_t gemm_tc_launch(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
+  constexpr int KS = tc_ks_for(NT, PAIR, W12);
+  const size_t smem = tc_smem_bytes(NT, PAIR, KS, a.tc_stages, W12);
+  static bool attr_set[64] = {};  // per device: allow the largest configuration this kernel may use
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, W12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget + 2048);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  return launch_k(gemm_tc_kernel<NT, PAIR, W12>, dim3(a.grid_p), dim3(W12 ? kTcThreadsW12 : kTcThreads), smem, s,
+                  a.pdl != 0, w, x, a);
+}
+
+}  // namespace tcg
+}  // namespace sv
+
+// Explicit instantiations for token tile NT (one translation unit per NT, so
+// the kernel variants compile in parallel). W12 tiles stop at kW12MaxNT.
+#define SV_GEMM_TC_INSTANTIATE(NT)                                                                               \
+  namespace sv {                                                                                                 \
+  namespace tcg {                                                                                                \
+  template cudaError_t gemm_tc_launch<NT, true, false>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&,  \
+                                                       cudaStream_t);                                            \
+  template cudaError_t gemm_tc_launch<NT, false, false>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, \
+                                                        cudaStream_t);                                           \
+  }                                                                                                              \
+  }
+#define SV_GEMM_TC_INSTANTIATE_W12(NT)                                                                          \
+  namespace sv {                                                                                                \
+  namespace tcg {                                                                                               \
+  template cudaError_t gemm_tc_launch<NT, true, true>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&,  \
+                                                      cudaStream_t);                                            \
+  template cudaError_t gemm_tc_launch<NT, false, true>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, \
+                                                       cudaStream_t);                                           \
+  }                                                                                                             \
+  }

@@ -1,0 +1,5 @@
+// Tensor-core skinny GEMM kernels for token tiles of 128 columns.
+#include "gemm_tc.cuh"
+
+SV_GEMM_TC_INSTANTIATE(128)
+

@@ -109,6 +109,35 @@ struct TokData {
   long long kv[kTokMax];
 };
 
+// A window of a later matrix product's weights to bring into L2 while the
+// current kernel leaves HBM idle (its own loads are all issued; its tail, the
+// next launch's start and the dependency waits follow). It names the target
+// product's work split, so CTA c of the current kernel requests the units
+// [u0 + first, u0 + first + count) of the target's CTAs c, c + grid, ...,
+// which the target then reads from L2 instead of HBM.
+struct L2Window {
+  const void* w;           // target weights (nullptr: no window)
+  int wdtype;              // SV_BF16 or SV_W12
+  int K;
+  int n_rows;
+  int pair;                // PairKind of the target
+  int ffn;
+  int kb, ks, m_tiles;     // the target's K blocks per tile, K step, token tiles
+  long long U;             // the target's units (tiles x K blocks)
+  int grid_p;              // the target's CTAs
+  int w12_kt;
+  long long w12_plane;
+  int first, count;        // units of each target CTA's range
+};
+
+// Per-CTA timeline (sv_model_set_trace): a traced launch writes one record of
+// kTraceWords 64-bit words per CTA; word 0 = kind << 48 | smid << 32 | CTA,
+// words 1-6 = %globaltimer (ns) at the kernel's milestones (0 = not reached):
+// 1 start, 2 dependency wait returned, 3 first operands landed, 4 last MMA
+// issued, 5 epilogue done, 6 exit.
+constexpr int kTraceWords = 8;
+enum TraceKind : int { kTrGemm = 1, kTrAttn = 2, kTrMerge = 3, kTrPrep = 4, kTrAccept = 5, kTrGemmFma = 6 };
+
 struct GemmArgs {
   int wdtype;              // SV_F32, SV_BF16, SV_W12
   const void* w;           // weights (W12: planes back to back)
@@ -137,6 +166,8 @@ struct GemmArgs {
   int tc_stages;           // shared-memory pipeline depth
   int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
   int pdl;                 // launched as a programmatic dependent of the previous kernel
+  L2Window pf;             // a later product's weights to request into L2 (tensor path)
+  unsigned long long* trace;  // this launch's per-CTA records, or nullptr
   Epi epi;
 };
 
@@ -165,6 +196,9 @@ struct AttnArgs {
   int x_pair;
   int kv_bf16;
   int pdl;                 // launched as a programmatic dependent of the previous kernel
+  L2Window pf;             // the next product's weights to request into L2 once the K/V loads are issued
+  unsigned long long* trace;  // per-CTA records of the attention launch, or nullptr
+  unsigned long long* trace_merge;  // per-CTA records of the merge launch, or nullptr
 };
 
 struct AcceptArgs {

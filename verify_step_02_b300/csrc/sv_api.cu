@@ -89,7 +89,6 @@ struct sv_model {
   // tensor path (bf16 weights): TMA maps of every weight matrix and of the x tensors
   bool use_tc = false;
   bool use_pdl = true;  // launch the step's kernels as programmatic dependents (overlapped prologues)
-  int attn_chunk = 0;   // keys per attention CTA (256 .. 4096, a multiple of 64); 0: chosen per launch
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;
   CUtensorMap map_lm, map_u, map_ao, map_act;
   // tensor-core attention (bf16 KV): per-layer maps of the K and V page pools,
@@ -102,6 +101,10 @@ struct sv_model {
   bool last_logits = false;
   int last_m = 0;
   Timing timing;
+  // per-CTA timeline (sv_model_set_trace)
+  unsigned long long* trace = nullptr;
+  long long trace_cap = 0, trace_used = 0;
+  std::vector<long long> trace_launches;  // (first record, CTAs, kind) per traced launch
 };
 
 namespace {
@@ -185,6 +188,77 @@ struct Timed {
   ~Timed() { timed_end(m, kc, s); }
 };
 
+// Records for one traced launch of `ctas` CTAs, or nullptr (tracing off or full).
+unsigned long long* trace_slot(sv_model* m, long long ctas, int kind) {
+  if (!m->trace || m->trace_used + ctas > m->trace_cap) return nullptr;
+  unsigned long long* p = m->trace + m->trace_used * kTraceWords;
+  m->trace_launches.push_back(m->trace_used);
+  m->trace_launches.push_back(ctas);
+  m->trace_launches.push_back(kind);
+  m->trace_used += ctas;
+  return p;
+}
+
+// Bytes of the next products' weights each kernel requests into L2 once its
+// own loads are issued (well inside the 126 MB L2, beside the streamed
+// weights, the KV and the activations).
+constexpr long long kPrefetchBytes = 32ll << 20;
+
+// A projection's tensor-core plan at block size M (tc false: the CUDA-core
+// path runs it, and nothing is prefetched for it).
+struct ProjPlan {
+  GemmArgs a;
+  bool tc = false;
+  long long unit_bytes = 0;  // weight bytes of one work unit
+  long long per_cta = 0;     // most units any CTA takes
+};
+
+ProjPlan plan_projection(const sv_model* m, int M, int n_units, int K, int pair, int ffn) {
+  ProjPlan p;
+  memset(&p.a, 0, sizeof p.a);
+  p.a.wdtype = m->cfg.weight_dtype;
+  p.a.x_kind = m->x_pair ? kXPair : kXF32;
+  p.a.ffn = ffn;
+  p.a.n_rows = pair == kPairSwiglu ? 2 * ffn : n_units;
+  if (!m->use_tc || !gemm_tc_supported(p.a.wdtype, pair, ffn)) return p;
+  plan_gemm_tc(p.a, M, n_units, K, pair, m->sm_count);
+  p.tc = p.a.tc_stages >= 2;
+  if (p.tc) {
+    const long long U = (long long)p.a.n_tiles * p.a.m_tiles * p.a.kb;
+    p.per_cta = (U + p.a.grid_p - 1) / p.a.grid_p;
+    p.unit_bytes = p.a.wdtype == SV_W12 ? 6LL * 4096 : (long long)kGemmBN * p.a.tc_ks * 2;
+  }
+  return p;
+}
+
+// Units [first, first + count) of every CTA range of projection `t` (weights
+// `w`), count bounded by `bytes`; *cursor advances past them.
+L2Window l2_window(const ProjPlan& t, const sv_matrix& w, int K, long long* cursor, long long bytes) {
+  L2Window pf;
+  memset(&pf, 0, sizeof pf);
+  if (!t.tc || *cursor >= t.per_cta) return pf;
+  long long n = bytes / ((long long)t.a.grid_p * t.unit_bytes);
+  if (n > t.per_cta - *cursor) n = t.per_cta - *cursor;
+  if (n <= 0) return pf;
+  pf.w = w.data;
+  pf.wdtype = t.a.wdtype;
+  pf.K = K;
+  pf.n_rows = t.a.n_rows;
+  pf.pair = t.a.pair;
+  pf.ffn = t.a.ffn;
+  pf.kb = t.a.kb;
+  pf.ks = t.a.tc_ks;
+  pf.m_tiles = t.a.m_tiles;
+  pf.U = (long long)t.a.n_tiles * t.a.m_tiles * t.a.kb;
+  pf.grid_p = t.a.grid_p;
+  pf.w12_kt = (K + 127) / 128;
+  pf.w12_plane = w12_plane_bytes(t.a.n_rows, K);
+  pf.first = static_cast<int>(*cursor);
+  pf.count = static_cast<int>(n);
+  *cursor += n;
+  return pf;
+}
+
 // ------------------------------------------------------------------ GEMM helpers
 GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const void* x, long long x_plane) {
   GemmArgs a;
@@ -238,7 +312,8 @@ void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* pa
 
 // wmap / xmap: the tensor maps of the weight and the x tensor (tensor path only).
 sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair, int kc, cudaStream_t s,
-                   const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr) {
+                   const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr,
+                   const L2Window* pf = nullptr) {
   Timed t(m, kc, s);
   bool tc = m->use_tc && gemm_tc_supported(a.wdtype, pair, a.ffn);
   if (tc) {
@@ -247,6 +322,8 @@ sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair
   }
   if (tc) {
     a.x_lo_row = m->m_max;
+    if (pf) a.pf = *pf;
+    a.trace = trace_slot(m, a.grid_p, kTrGemm);
     SV_CUDA(launch_gemm_tc(a, *wmap, *xmap, s), what);
   } else {
     plan_gemm(a, M, n_units, K, pair, m->sm_count);
@@ -281,6 +358,16 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   p.M = M;
   const int d = c.d_model, hd = c.head_dim, nq = c.n_heads * hd, N3 = nqkv(c);
   const bool keep = T > 0.f || (c.flags & SV_FLAG_KEEP_LOGITS);
+  // Every projection's plan at this M; each kernel then requests a window of
+  // the next product's weights into L2 (each window continues where the
+  // previous one for that product stopped, past the stages the product
+  // itself requests before its dependency wait).
+  const ProjPlan pl_qkv = plan_projection(m, M, N3, d, kPairNone, 0);
+  const ProjPlan pl_o = plan_projection(m, M, d, nq, kPairNone, 0);
+  const ProjPlan pl_gu = plan_projection(m, M, c.ffn, d, kPairSwiglu, c.ffn);
+  const ProjPlan pl_d = plan_projection(m, M, d, c.ffn, kPairNone, 0);
+  const ProjPlan pl_lm = plan_projection(m, M, c.vocab, d, kPairNone, 0);
+  auto first_units = [](const ProjPlan& t) { return (long long)(t.tc ? t.a.tc_stages : 0); };
 
   {
     Timed t(m, SV_KC_NORM, s);
@@ -291,6 +378,16 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const sv_layer_weights& L = m->layers[l];
+    long long cur_o = first_units(pl_o), cur_gu = first_units(pl_gu), cur_d = first_units(pl_d);
+    const bool last = l + 1 == c.n_layers;
+    const ProjPlan& pl_next = last ? pl_lm : pl_qkv;
+    const sv_matrix& w_next = last ? m->w.lm_head : m->layers[l + 1].wqkv;
+    long long cur_next = first_units(pl_next);
+    const L2Window pf_qkv = l2_window(pl_o, L.wo, nq, &cur_o, kPrefetchBytes);
+    const L2Window pf_attn = l2_window(pl_gu, L.wgu, d, &cur_gu, kPrefetchBytes);
+    const L2Window pf_o = l2_window(pl_gu, L.wgu, d, &cur_gu, kPrefetchBytes);
+    const L2Window pf_gu = l2_window(pl_d, L.wd, c.ffn, &cur_d, kPrefetchBytes);
+    const L2Window pf_d = l2_window(pl_next, w_next, d, &cur_next, kPrefetchBytes);
     {  // QKV projection, RoPE, q out, k/v into the page slots
       GemmArgs a = gemm_base(m, L.wqkv, N3, d, m->u, m->u_plane);
       a.epi.kind = kEpiQkv;
@@ -313,7 +410,8 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.max_pages = kv->max_pages_per_seq;
       a.epi.page_size = c.page_size;
       a.epi.n_pages = kv->n_pages;
-      sv_status st = run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm", &m->map_qkv[l], &m->map_u);
+      sv_status st =
+          run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm", &m->map_qkv[l], &m->map_u, &pf_qkv);
       if (st) return st;
     }
     {
@@ -349,9 +447,12 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
-        a.chunk = m->attn_chunk > 0 ? m->attn_chunk : attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
+        a.chunk = attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
         a.max_chunks = (c.max_seq_len + a.chunk - 1) / a.chunk;
         a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
+        a.pf = pf_attn;
+        a.trace = trace_slot(m, (long long)B * c.n_kv_heads * a.max_chunks, kTrAttn);
+        a.trace_merge = trace_slot(m, (long long)B * c.n_kv_heads * ((a.max_rows + 7) / 8), kTrMerge);
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
       } else {
@@ -368,7 +469,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.x_out = m->u;
       a.epi.x_out_plane = m->u_plane;
       a.epi.ss_out = m->ss;
-      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao);
+      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao, &pf_o);
       if (st) return st;
     }
     {
@@ -379,7 +480,8 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.act_plane = m->act_plane;
       a.epi.ffn = c.ffn;
       a.epi.ss_in = m->ss;
-      sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm", &m->map_gu[l], &m->map_u);
+      sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm", &m->map_gu[l],
+                              &m->map_u, &pf_gu);
       if (st) return st;
     }
     {
@@ -391,7 +493,8 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.x_out = m->u;
       a.epi.x_out_plane = m->u_plane;
       a.epi.ss_out = m->ss;
-      sv_status st = run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act);
+      sv_status st =
+          run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act, &pf_d);
       if (st) return st;
     }
   }
@@ -461,11 +564,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   m->layers.assign(weights->layers, weights->layers + cfg->n_layers);
   m->w.layers = nullptr;
   m->wbf16 = cfg->weight_dtype == SV_F32 ? 0 : 1;
-  if (const char* env = getenv("SV_PDL")) m->use_pdl = atoi(env) != 0;
-  if (const char* env = getenv("SV_ATTN_CHUNK")) {
-    const int v = atoi(env);
-    if (v >= 256 && v <= 4096 && v % 64 == 0) m->attn_chunk = v;
-  }
+  m->use_pdl = (cfg->flags & SV_FLAG_NO_PDL) == 0;
   m->x_pair = m->wbf16;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -695,6 +794,27 @@ sv_status sv_model_timing(sv_model* model, double* ms, int64_t* launches) {
     ms[k] = t.ms[k];
     launches[k] = t.launches[k];
   }
+  return SV_OK;
+}
+
+sv_status sv_model_set_trace(sv_model* model, uint64_t* records, int64_t capacity) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  if ((records == nullptr) != (capacity == 0) || capacity < 0)
+    return fail(SV_ERR_INVALID_ARG, "records and capacity must both be set or both be 0");
+  model->trace = reinterpret_cast<unsigned long long*>(records);
+  model->trace_cap = capacity;
+  model->trace_used = 0;
+  model->trace_launches.clear();
+  return SV_OK;
+}
+
+sv_status sv_model_trace_launches(sv_model* model, int64_t* launches, int64_t max_launches, int64_t* n_launches) {
+  if (!model || !n_launches) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  const int64_t n = static_cast<int64_t>(model->trace_launches.size() / 3);
+  *n_launches = n;
+  if (launches)
+    for (int64_t i = 0; i < n && i < max_launches; ++i)
+      for (int j = 0; j < 3; ++j) launches[3 * i + j] = model->trace_launches[3 * i + j];
   return SV_OK;
 }
 
