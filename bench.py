@@ -51,13 +51,16 @@ def parse():
     ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sweep", choices=["none", "gemm"], default="none")
+    ap.add_argument("--sweep", choices=["none", "gemm", "step"], default="none",
+                    help="gemm: the skinny GEMM alone per projection shape; step: the whole verify step of the "
+                         "8B-class model per block size M (the step-cost table a prefix scheduler takes)")
     ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
     ap.add_argument("--sweep-dtype", choices=["bf16", "w12"], default="bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", action="store_true",
                     help="after the timed steps, run two traced steps and add a per-kernel timeline summary "
                          "(device %globaltimer per CTA) to the JSON line")
+    ap.add_argument("--trace-out", default=None, help="with --trace: also save the raw per-CTA records (.npz)")
     ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "sampled"], default="8b",
                     help="8b: the headline line (default); the others time the other verify configurations "
                          "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
@@ -185,7 +188,7 @@ def traffic_record(kernel, workload, files):
 
 
 # ------------------------------------------------------------------ device timeline
-LAYER_KERNELS = ("qkv", "attention", "attn_merge", "o", "gate_up", "down")
+LAYER_KERNELS = ("qkv", "attention", "o", "gate_up", "down")
 
 
 def trace_summary(records, launches, n_layers):
@@ -195,28 +198,42 @@ def trace_summary(records, launches, n_layers):
     launch order (the layer kernels of each step, then the LM head). For each
     kernel, times are measured from the moment the previous kernel's last CTA
     exited: its first CTA start, its median dependency-wait return, its median
-    first operands, its last MMA issue, and its last CTA exit (= the time it
-    adds to the step). Layer 0 is skipped (its predecessor is not traced).
+    first operands, its median and last MMA issue, the latest CTA at each step
+    of the last tile's hand-off (projections), and its last CTA exit (= the
+    time it adds to the step). Layer 0 is skipped (its predecessor is not
+    traced).
     """
-    per_step = 6 * n_layers + 1
+    nk = len(LAYER_KERNELS)
+    per_step = nk * n_layers + 1
     names = []
     for i in range(len(launches)):
         j = i % per_step
-        names.append("lm_head" if j == per_step - 1 else LAYER_KERNELS[j % 6])
+        names.append("lm_head" if j == per_step - 1 else LAYER_KERNELS[j % nk])
     acc = {}
     prev_exit = None
     for i, (first, ctas, kind) in enumerate(launches):
         r = records[first:first + ctas].astype(np.float64)
         w = lambda k: r[:, k][r[:, k] > 0]
         starts, waits, mma0, mma1, exits = w(1), w(2), w(3), w(4), w(6)
+        tail = {n: w(k) for n, k in (("t_acc", 7), ("t_stored", 8), ("t_counted", 9), ("t_reduced", 10),
+                                      ("t_epilogue", 11), ("t_x", 12), ("t_summed", 13))}
         if len(exits) == 0:
             prev_exit = None
             continue
         ex = exits.max()
         j = i % per_step
-        if prev_exit is not None and j >= 6:
-            d = acc.setdefault(names[i], {k: [] for k in ("start", "wait", "first_mma", "last_mma", "exit")})
+        if prev_exit is not None and j >= nk:
+            d = acc.setdefault(names[i], {k: [] for k in ("ctas", "start", "wait", "first_mma", "last_mma_median",
+                                                           "last_mma", "t_acc", "t_x", "t_stored",
+                                                           "t_counted", "t_summed", "t_reduced", "t_epilogue",
+                                                           "exit")})
+            d["ctas"].append(ctas)
             d["start"].append(starts.min() - prev_exit)
+            if len(mma1):
+                d["last_mma_median"].append(np.median(mma1) - prev_exit)
+            for n, v in tail.items():
+                if len(v):
+                    d[n].append(v.max() - prev_exit)
             if len(waits):
                 d["wait"].append(np.median(waits) - prev_exit)
             if len(mma0):
@@ -227,7 +244,8 @@ def trace_summary(records, launches, n_layers):
         prev_exit = ex
     out = {}
     for name, d in acc.items():
-        out[name] = {k: round(float(np.mean(v)) / 1e3, 2) for k, v in d.items() if v}
+        out[name] = {k: (int(np.mean(v)) if k == "ctas" else round(float(np.mean(v)) / 1e3, 2))
+                     for k, v in d.items() if v}
     layer_us = sum(out[n]["exit"] for n in LAYER_KERNELS if n in out)
     return {"per_kernel_us_after_previous_exit": out, "layer_us": round(layer_us, 2),
             "note": "device %globaltimer per CTA, means over layers 1.. of two traced steps"}
@@ -397,8 +415,8 @@ def run_ours(args, world, rank, local):
     trace = None
     if args.trace:
         n_layers = args.layers or 36
-        cap = 2 * (n_layers * (4 * 148 + 2 * 8 * 64) + 148 + 64)
-        recs = torch.zeros((cap, 8), dtype=torch.int64, device="cuda")
+        cap = 2 * (n_layers * (4 * 148 + 8 * 16 * 2) + 148 + 64)
+        recs = torch.zeros((cap, 16), dtype=torch.int64, device="cuda")
         kv.seq_len.fill_(CONTEXT)
         for i in range(args.warmup):
             run(i)
@@ -409,7 +427,11 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         launches = model.trace_launches()
         model.set_trace(None)
-        trace = trace_summary(recs.cpu().numpy().view(np.uint64), launches, n_layers)
+        raw = recs.cpu().numpy().view(np.uint64)
+        trace = trace_summary(raw, launches, n_layers)
+        if args.trace_out:
+            np.savez_compressed(args.trace_out, records=raw, launches=np.array([l[:2] for l in launches]),
+                                kinds=np.array([l[2] for l in launches]))
 
     value, t_max = aggregate(tokens, t_ms, world)
     e2e_all, _ = aggregate(e2e_tokens, t_e2e * 1e3, world)
@@ -732,6 +754,68 @@ def run_sweep(args, local):
             "peak_kind": peak_kind, "timing": "CUDA-graph replay of back-to-back launches", "shapes": out}
 
 
+# ------------------------------------------------------------------ step-cost table
+STEP_SWEEP_M = (1, 2, 4, 8, 16, 17, 24, 32, 48, 64, 96, 128, 192, 256)
+
+
+def run_sweep_step(args, local):
+    """Verify-step time of the 8B-class model per block size M (requests of up to 64 rows).
+
+    M = 1 is one step of plain autoregressive greedy decoding; the table (step
+    time and steps per second per M) is what the prefix scheduler
+    (sv_schedule_prefix) maximizes tau / T(M) over. Context 4096 per request,
+    drafts random (the step's work does not depend on acceptance).
+    """
+    import torch
+
+    import synth
+    import synth.device as sd
+    import verify_step_02_b300 as vs
+    torch.cuda.set_device(local)
+    shape = dict(synth.SHAPES["8b"], n_layers=args.layers or 36)
+    max_b, max_g = 4, 63
+    steps = args.steps
+    reps = len(STEP_SWEEP_M) * (steps + args.warmup)
+    max_seq = CONTEXT + reps + 128
+    max_seq = (max_seq + PAGE - 1) // PAGE * PAGE
+    wdev = sd.random_bf16_model(shape)
+    table, n_pages = synth.contiguous_page_table([max_seq] * max_b, PAGE, max_seq // PAGE + 1)
+    ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, torch.bfloat16, fill="normal")
+    seq = torch.full((max_b,), CONTEXT, dtype=torch.int32, device="cuda")
+    kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
+    model = vs.Model(vs.make_config(shape, vs.SV_BF16, max_b, max_g, max_seq, PAGE), wdev)
+    rng = np.random.default_rng(5)
+    tok = torch.from_numpy(rng.integers(0, shape["vocab"], size=(max_b, max_g + 1)).astype(np.int32)).cuda()
+    acc = torch.zeros(max_b, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(max_b, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    per_layer, wbytes, kv_row = step_bytes(shape)
+    rows = {}
+    for M in STEP_SWEEP_M:
+        b = (M + max_g) // (max_g + 1)
+        lens = [M // b - 1 + (1 if r < M % b else 0) for r in range(b)]
+        for _ in range(args.warmup):
+            model.verify(tok[:b], lens, kv, acc[:b], nxt[:b])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            model.verify(tok[:b], lens, kv, acc[:b], nxt[:b])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / steps * 1e3
+        ctx = float(seq[:b].float().mean().item())
+        alg = wbytes + kv_row * b * (ctx + M / b) + kv_row * M
+        rows[str(M)] = {"batch": b, "us": round(us, 1), "steps_per_s": round(1e6 / us, 1),
+                        "hbm_frac": round(alg / (us * 1e-6) / 1e9 / peak, 4)}
+    model.close()
+    return {"sweep": "step", "model": "8B-class bf16, 36 layers", "context": CONTEXT, "layers": shape["n_layers"],
+            "table": rows, "ar_greedy_tokens_per_s": rows["1"]["steps_per_s"], "peak_gbs": peak,
+            "peak_kind": peak_kind,
+            "note": "M rows per step (requests of up to 64 rows); M = 1 is autoregressive greedy decoding"}
+
+
 # ------------------------------------------------------------------ the other configurations
 WORKLOADS = {
     "tiny": "tiny fp32 greedy verify: 2 layers, d 256, 4 x 64 heads, vocab 1024; batch 1, gamma 4, context 64",
@@ -872,8 +956,10 @@ def run_workload(args, world, rank, local):
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
-    if args.sweep != "none":
+    if args.sweep == "gemm":
         res = run_sweep(args, local)
+    elif args.sweep == "step":
+        res = run_sweep_step(args, local)
     elif args.workload != "8b" and args.impl == "ours":
         res = run_workload(args, world, rank, local)
     elif args.impl == "reference":

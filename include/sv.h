@@ -36,6 +36,11 @@
  *   - The library never aborts the process and never traps on the device.
  *     Device-side checks (token ids, page ids) record a status word that
  *     sv_model_sync_status() reads back; the offending rows are skipped.
+ *   - Models, tensor maps and the static scratch of sv_linear_noalloc hold
+ *     device addresses of the context they were made in. cudaDeviceReset
+ *     ends that context: destroy every model before it, and do not use the
+ *     library across it (sv_linear_noalloc keeps the scratch address it
+ *     looked up, which a reset invalidates).
  */
 #ifndef SV_H
 #define SV_H
@@ -51,7 +56,7 @@ typedef enum {
   SV_OK = 0,
   SV_ERR_INVALID_ARG = 1,       /* a size, pointer or option is out of range */
   SV_ERR_NOT_REPRESENTABLE = 2, /* W12: a value is not a normal number or the exponent window exceeds 16 binades */
-  SV_ERR_KV_CAPACITY = 3,       /* a request's block does not fit its page table */
+  SV_ERR_KV_CAPACITY = 3,       /* a request's block did not fit its page table or max_seq_len (device-detected) */
   SV_ERR_OUT_OF_MEMORY = 4,     /* workspace allocation failed */
   SV_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed; see sv_last_error() */
   SV_ERR_DEVICE_CHECK = 6,      /* a device-side check failed (bad token or page id) */
@@ -77,7 +82,7 @@ typedef struct {
   float rms_eps;         /* RMSNorm epsilon */
   int32_t weight_dtype;  /* sv_dtype */
   int32_t max_batch;     /* largest B passed to sv_verify */
-  int32_t max_gamma;     /* largest L_r (drafts per request, anchor excluded) */
+  int32_t max_gamma;     /* largest L_r (drafts per request, anchor excluded), 0 .. 255 */
   int32_t page_size;     /* KV positions per page: 16 */
   int32_t max_seq_len;   /* largest absolute position + 1 that any row may take */
   int32_t flags;         /* SV_FLAG_* */
@@ -157,7 +162,7 @@ void sv_model_destroy(sv_model* model);
  *   draft_probs  device float32 [B][max_gamma][vocab]: q_i, the distribution
  *                d_i was drawn from. Required when temperature > 0, ignored
  *                (may be NULL) when temperature == 0.
- *   temperature  0: greedy match; > 0: rejection sampling with target
+ *   temperature  0: greedy match; >= 1e-6: rejection sampling with target
  *                p = softmax(z / temperature): accept d_i iff
  *                u_i * q_i(d_i) < p_{i-1}(d_i); at the first rejection emit a
  *                draw from max(0, p_{i-1} - q_i) normalized, else a draw from
@@ -171,8 +176,9 @@ void sv_model_destroy(sv_model* model);
  * Writes the K/V of all M rows into their page slots, then commits
  * seq_len[r] += k_r + 1 (rows past the accepted prefix are left to be
  * overwritten). Asynchronous on `stream`.
- * Errors: SV_ERR_INVALID_ARG (B, L_r, temperature, NULL pointers),
- *         SV_ERR_CUDA (launch failure).
+ * Errors: SV_ERR_INVALID_ARG (B, L_r, NULL pointers; a temperature that is
+ *         negative, not finite, or positive but below 1e-6, where z / T
+ *         could overflow in float32), SV_ERR_CUDA (launch failure).
  */
 sv_status sv_verify(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
                     const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
@@ -188,15 +194,36 @@ sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, 
                          const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
                          const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream);
 
+/*
+ * Prefill (or autoregressive decode) through the verify step's kernels: the
+ * target forward over the blocks [t_{r,0}, .., t_{r,L_r}] at positions
+ * C_r .. C_r + L_r, committing every row: the KV of all rows is written and
+ * seq_len[r] += L_r + 1. next_token[r] (device int32 out) is the greedy
+ * token after the block (the argmax of row L_r's logits; lowest index on
+ * ties). tokens and block_lens as in sv_verify (block_lens[r] = L_r = the
+ * block's rows - 1, host, 0 .. max_gamma); a prompt longer than
+ * max_gamma + 1 is fed as consecutive blocks. With L_r = 0 this is one step
+ * of plain autoregressive greedy decoding (the baseline the speed-ups of
+ * speculative decoding are quoted against). Asynchronous on `stream`; errors
+ * as sv_verify.
+ */
+sv_status sv_prefill(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* block_lens,
+                     const sv_kv* kv, int32_t* next_token, void* stream);
+
 /* Copy the float32 logits [M][vocab] of the last verify (rows in request
  * order, anchor row first) to device `dst`. Valid after a sampled verify, or
  * after any verify when the model was created with SV_FLAG_KEEP_LOGITS;
  * otherwise SV_ERR_INVALID_ARG. `rows` must equal that verify's M. */
 sv_status sv_model_logits(sv_model* model, float* dst, int32_t rows, void* stream);
 
-/* Synchronize `stream`, read and clear the device status word. Returns
- * SV_ERR_DEVICE_CHECK if a kernel saw a token id outside [0, vocab) or a
- * page id outside [0, n_pages) since the last call; sv_last_error() names it. */
+/* Synchronize `stream`, read and clear the device status word. Since the last
+ * call, if some request's block did not fit its KV capacity (a row position
+ * reached max_seq_len, or its page index was past max_pages_per_seq) and
+ * nothing else went wrong, returns SV_ERR_KV_CAPACITY; if a kernel saw a token
+ * id outside [0, vocab), a page id outside [0, n_pages) or a wait that timed
+ * out, returns SV_ERR_DEVICE_CHECK. sv_last_error() names every condition.
+ * The offending rows were skipped: their KV was not written and their
+ * attention ignored the missing pages; other requests are unaffected. */
 sv_status sv_model_sync_status(sv_model* model, void* stream);
 
 /* Kernel timing for measurement. When enabled, the library records CUDA
@@ -212,13 +239,17 @@ sv_status sv_model_timing(sv_model* model, double* ms /* [SV_KC_COUNT] */, int64
 
 /* Per-CTA device timeline, for measurement. While records != NULL, each
  * traced kernel of a verify (the tensor-core projections, the tensor-core
- * attention and its merge) writes one record of 8 uint64 words per CTA into
+ * attention and its merge) writes one record of 16 uint64 words per CTA into
  * `records` (device, capacity records, zero-filled by the caller): word 0 =
  * kind << 48 | SM id << 32 | CTA index (kinds: 1 projection, 2 attention,
  * 3 attention merge), words 1-6 = the %globaltimer value in ns when the CTA
  * started, returned from its dependency wait, had its first operands, issued
  * its last MMA, finished its epilogue, and exited (0 where a CTA has no such
- * step). Launches that no longer fit are not traced. Setting a new buffer (or
+ * step). Projections add, for the hand-off of the CTA's last tile: 7 the
+ * accumulator ready for the epilogue, 8 its partial tile stored and fenced,
+ * 9 its arrival counted, 10 the contributors' partials summed (last arriver
+ * only), 11 the tile epilogue done. Launches that no longer fit are not
+ * traced. Setting a new buffer (or
  * NULL, 0 to stop) restarts the count. sv_model_trace_launches writes
  * (first record, CTAs, kind) for each traced launch, in launch order, into
  * host int64 launches[3 * max_launches] and their number to *n_launches. */
@@ -280,10 +311,13 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
  * memory while they run (cudaMalloc can synchronize the whole device and
  * stall other streams, and some hosts, such as inference servers with fixed
  * memory pools or plugins whose host owns every allocation, forbid it).
- * Same arguments and result as sv_linear, without the workspace: the split-K
- * scratch (partial tiles and tile counters) lives in a 16 MiB static device
- * array inside the library, which every GPU that loads the library keeps
- * until the process exits.
+ * The same arguments as sv_linear, without the workspace. It always runs the
+ * CUDA-core (FMA) plan of the product, whatever the weight type: its result
+ * equals sv_linear's within rounding (not bit for bit, since sv_linear takes
+ * the tensor-core path for bf16/W12 weights), and for large bf16/W12 shapes it
+ * is much slower. The split-K scratch (partial tiles and tile counters) lives
+ * in a 16 MiB static device array inside the library, which every GPU that
+ * loads the library keeps until the process exits.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current. Make that first call
  *     before any stream capture.
@@ -303,6 +337,32 @@ sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32_t N, int32
  * position0 + i, stream_id) for i < n, device float32. Asynchronous. */
 sv_status sv_philox_uniform(uint64_t seed, int64_t request_id, int64_t position0, int32_t stream_id, int32_t n,
                             float* out, void* stream);
+
+/*
+ * Hardware-aware prefix scheduler (DSpark summary, "Confidence-Scheduled
+ * Verification"): choose every request's verify length from its draft
+ * confidences and the measured step cost, to maximize the throughput
+ * Theta = tau / T(M), tau = sum_r (1 + sum_{j <= L_r} a_{r,j}) the expected
+ * tokens of the step, a_{r,j} = prod_{i <= j} c_{r,i} the survival
+ * probability of draft j, M = sum_r (L_r + 1) the verified rows.
+ *   conf        HOST float [batch][gamma]: c_{r,i} in [0, 1], the probability
+ *               that draft i passes given drafts 1 .. i-1 did.
+ *   step_us     HOST float [n_cost]: step_us[M - 1] = verify-step time for M
+ *               rows (for example a bench sweep); n_cost >= batch. M past the
+ *               table is never chosen.
+ *   early_stop  nonzero: stop at the first admission that lowers Theta (the
+ *               optimum when Theta is unimodal in M); zero: scan every M.
+ *   verify_lens HOST int32 out [batch]: the chosen L_r.
+ *   expected_tokens, throughput: HOST out (may be NULL): tau and Theta in
+ *               tokens per second.
+ * A global sort of the a_{r,j} admitted greedily visits the best choice of
+ * drafts for every M (a_{r,j} never increases in j, so the M - B largest form
+ * a prefix of each request's drafts). Host only; no GPU work.
+ * Errors: SV_ERR_INVALID_ARG (sizes, NULL pointers, a confidence outside
+ * [0, 1], a cost that is not finite and positive).
+ */
+sv_status sv_schedule_prefix(int32_t batch, int32_t gamma, const float* conf, const float* step_us, int32_t n_cost,
+                             int32_t early_stop, int32_t* verify_lens, double* expected_tokens, double* throughput);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* sv_last_error(void);

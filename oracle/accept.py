@@ -77,6 +77,30 @@ def sampled_accept(logits, drafts, q, temperature, u_acc, u_res):
     return len(drafts), inverse_cdf(p[len(drafts)], u_res[len(drafts)])
 
 
+def sampled_accept_one_draft_batch(logits, drafts, q, temperature, u_acc, u_res0, u_res1):
+    """sampled_accept for N independent one-draft blocks that share their target rows and q.
+
+    logits [2, V] (rows 0 and 1 of every block); drafts [N]; q [V]; u_acc, u_res0,
+    u_res1 [N] (the accept uniform, the residual draw's and the bonus draw's).
+    The same rule as sampled_accept, applied to every block at once. Returns
+    (accepted [N] in {0, 1}, next_token [N]).
+    """
+    p = softmax(logits, temperature)
+    q = np.asarray(q, dtype=np.float64)
+    d = np.asarray(drafts, dtype=np.int64)
+    acc = np.asarray(u_acc) * q[d] < p[0, d]
+    r = np.maximum(0.0, p[0] - q)
+    if r.sum() <= 0.0:
+        r = p[0]
+
+    def draw(w, u):  # inverse_cdf for every u at once
+        cdf = np.cumsum(w)
+        v = np.searchsorted(cdf, np.asarray(u) * cdf[-1], side="right")
+        return np.minimum(v, np.nonzero(w > 0)[0][-1])
+    nxt = np.where(acc, draw(p[1], u_res1), draw(r, u_res0))
+    return acc.astype(np.int64), nxt
+
+
 def uniforms(seed, request_id, start_pos, n_drafts):
     """u_acc [L] and u_res [L+1] for a request whose anchor sits at start_pos."""
     pos = start_pos + np.arange(1, n_drafts + 2)

@@ -88,6 +88,37 @@ def classify_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, ne
     return "mismatch"
 
 
+def report_decisions(name, verdicts, max_near_ties):
+    """Print how many decisions matched the oracle and how many were near-ties; fail on any
+    mismatch (a decision that differs where the oracle's margins were clear) or on more
+    near-ties than `max_near_ties`."""
+    n_match, n_tie = verdicts.count("match"), verdicts.count("near_tie")
+    n_bad = len(verdicts) - n_match - n_tie
+    print(f"[decisions] {name}: {len(verdicts)} compared, {n_match} identical, {n_tie} near-tie, {n_bad} mismatch")
+    assert n_bad == 0, verdicts
+    assert n_tie <= max_near_ties, verdicts
+
+
+def engine_greedy_chain(model, kv, anchors, n, gamma):
+    """n greedy tokens per request from the engine itself (one row per request per step), to
+    build drafts that agree with the target for long prefixes; seq_len is restored after."""
+    import torch
+    b = len(anchors)
+    seq0 = kv.seq_len.clone()
+    tok = torch.zeros((b, gamma + 1), dtype=torch.int32, device="cuda")
+    tok[:, 0] = torch.as_tensor(np.asarray(anchors, dtype=np.int32), device="cuda")
+    acc = torch.zeros(b, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(b, dtype=torch.int32, device="cuda")
+    out = []
+    for _ in range(n):
+        model.verify(tok, [0] * b, kv, acc, nxt)
+        out.append(nxt.clone())
+        tok[:, 0] = nxt
+    model.sync_status()
+    kv.seq_len.copy_(seq0)
+    return torch.stack(out, 1).cpu().numpy()
+
+
 class DeviceLayers:
     """Per-layer host copies (bf16 patterns) of device weights, fetched when the oracle asks."""
 

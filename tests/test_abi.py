@@ -42,3 +42,17 @@ def test_host_side_argument_errors_need_no_gpu():
     st = vs.lib.sv_verify(None, 1, None, None, None, None, 0.0, 0, None, None, None, None)
     assert st == vs.SV_ERR_INVALID_ARG
     assert vs.lib.sv_unpack_w12(None, 127, 1, 1, None, None) == vs.SV_ERR_INVALID_ARG
+
+
+def test_tiny_positive_temperature_is_refused_on_the_host():
+    """0 < T < 1e-6 would overflow z / T in float32; the call fails before it needs a model or a GPU."""
+    import verify_step_02_b300 as vs
+    for t in (1e-9, 9.9e-7, -1.0, float("nan"), float("inf")):
+        st = vs.lib.sv_verify(None, 1, None, None, None, None, t, 0, None, None, None, None)
+        assert st == vs.SV_ERR_INVALID_ARG and b"temperature" in vs.lib.sv_last_error(), t
+        st = vs.lib.sv_verify_host(None, 1, None, None, None, None, t, 0, None, None, None, None)
+        assert st == vs.SV_ERR_INVALID_ARG and b"temperature" in vs.lib.sv_last_error(), t
+    for t in (0.0, 1e-6, 1.0):  # accepted temperatures reach the next check (the NULL model)
+        st = vs.lib.sv_verify(None, 1, None, None, None, None, t, 0, None, None, None, None)
+        assert st == vs.SV_ERR_INVALID_ARG and b"model is NULL" in vs.lib.sv_last_error(), t
+

@@ -98,7 +98,7 @@ def test_linear_matches_float64(kind, m):
 
 
 @pytest.mark.parametrize("kind", ["bf16", "w12"])
-@pytest.mark.parametrize("m,n,k", [(17, 6144, 4096), (17, 4096, 12288), (1, 4096, 4096), (33, 1000, 4096),
+@pytest.mark.parametrize("m,n,k", [(17, 6144, 4096), (17, 4096, 12288), (17, 24576, 4096), (64, 4096, 4096), (1, 4096, 4096), (33, 1000, 4096),
                                    (64, 1000, 4112), (187, 1280, 5120), (256, 512, 1024), (300, 384, 512)])
 def test_linear_projection_shapes(kind, m, n, k):
     """The skinny product at the decoder's projection sizes: many tiles, K shared by several CTAs,

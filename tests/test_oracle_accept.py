@@ -110,6 +110,37 @@ def test_acceptance_rate_is_one_minus_tv_and_output_is_target(zeros_p, zeros_q):
     assert chi.pvalue > 1e-3
 
 
+N_BIG = 1_000_000
+
+
+@pytest.mark.parametrize("v", [8, 16])
+@pytest.mark.parametrize("zeros_p,zeros_q", [(False, False), (True, False), (False, True), (True, True)])
+def test_acceptance_rate_and_output_law_at_one_million(v, zeros_p, zeros_q):
+    """The same closed form and chi-square as above at N = 10^6 single-draft blocks and
+    V in {8, 16}, on the oracle's batched one-draft rule; that rule equals the per-block
+    sampled_accept exactly on the first 20 000 blocks."""
+    T = 0.7
+    rng = np.random.default_rng(100 + 10 * v + 2 * zeros_p + zeros_q)
+    p, q = _dists(v, rng, zeros_p, zeros_q)
+    z = np.tile(_logits_for(p, T), (2, 1))
+    drafts = rng.choice(v, size=N_BIG, p=q)
+    from oracle import philox
+    pos = np.arange(N_BIG) * 4
+    u0 = philox.uniform(77, 3, pos + 1, 0)
+    u1 = philox.uniform(77, 3, pos + 1, 1)
+    u2 = philox.uniform(77, 3, pos + 2, 1)
+    acc, nxt = accept.sampled_accept_one_draft_batch(z, drafts, q, T, u0, u1, u2)
+    for n in range(20_000):
+        k, t = accept.sampled_accept(z, [drafts[n]], q[None, :], T, [u0[n]], [u1[n], u2[n]])
+        assert (k, t) == (acc[n], nxt[n])
+    want = np.minimum(p, q).sum()
+    assert stats.binomtest(int(acc.sum()), N_BIG, want).pvalue > 1e-3
+    first = np.bincount(np.where(acc == 1, drafts, nxt), minlength=v)
+    mask = p > 0
+    assert first[~mask].sum() == 0
+    assert stats.chisquare(first[mask], N_BIG * p[mask]).pvalue > 1e-3
+
+
 def test_two_position_chain_joint_distribution():
     """Joint law of the first two emitted tokens equals p0(x1) p1(x2 | x1).
 

@@ -14,7 +14,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsv.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libsv.so is not built ({LIB_PATH}); run python -m verify_step_02_b300.build")
+    raise ImportError(f"libsv.so is not built ({LIB_PATH}); run python {os.path.join(_HERE, 'build.py')}")
 lib = ctypes.CDLL(LIB_PATH)
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_NOT_REPRESENTABLE, SV_ERR_KV_CAPACITY = 0, 1, 2, 3
@@ -67,6 +67,7 @@ _SIGS = {
     "sv_verify": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _f32, _u64, _vp, _vp, _vp, _vp]),
     "sv_verify_host": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _f32, _u64, _vp, _vp, _vp, _vp]),
     "sv_model_logits": (_i32, [_vp, _vp, _i32, _vp]),
+    "sv_prefill": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _vp]),
     "sv_model_sync_status": (_i32, [_vp, _vp]),
     "sv_model_set_timing": (_i32, [_vp, _i32]),
     "sv_model_timing": (_i32, [_vp, _vp, _vp]),
@@ -79,6 +80,8 @@ _SIGS = {
     "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sv_linear_noalloc": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp]),
     "sv_philox_uniform": (_i32, [_u64, _i64, _i64, _i32, _i32, _vp, _vp]),
+    "sv_schedule_prefix": (_i32, [_i32, _i32, _vp, _vp, _i32, _i32, _vp, ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_double)]),
     "sv_last_error": (ctypes.c_char_p, []),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -168,6 +171,12 @@ class Model:
                              ctypes.byref(kv.struct), _ptr(draft_probs), float(temperature), int(seed),
                              _ptr(request_ids), _ptr(accepted_len), _ptr(next_token), _stream(stream)))
 
+    def prefill(self, tokens, block_lens, kv, next_token, stream=None):
+        """Forward and commit every row of the blocks; next_token (device) = greedy token after each block."""
+        lens = np.ascontiguousarray(np.asarray(block_lens, dtype=np.int32))
+        _check(lib.sv_prefill(self.handle, len(lens), _ptr(tokens), lens.ctypes.data_as(ctypes.c_void_p),
+                              ctypes.byref(kv.struct), _ptr(next_token), _stream(stream)))
+
     def verify_host(self, tokens, verify_lens, kv, draft_probs=None, temperature=0.0, seed=0, request_ids=None,
                     stream=None, out=None):
         """Host-memory inputs and outputs (numpy or pinned torch CPU tensors); synchronizes."""
@@ -207,7 +216,7 @@ class Model:
         return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
 
     def set_trace(self, records):
-        """records: zero-filled device uint64-sized tensor [capacity, 8], or None to stop tracing."""
+        """records: zero-filled device 64-bit tensor [capacity, 16], or None to stop tracing."""
         if records is None:
             _check(lib.sv_model_set_trace(self.handle, None, 0))
         else:
@@ -273,3 +282,21 @@ def philox_uniform(seed, request_id, position0, stream_id, n, stream=None):
     _check(lib.sv_philox_uniform(int(seed), int(request_id), int(position0), int(stream_id), int(n), _ptr(out),
                                  _stream(stream)))
     return out
+
+
+def schedule_prefix(conf, step_us, early_stop=False):
+    """Verify lengths maximizing expected tokens / step time (host only).
+
+    conf: [B, gamma] draft confidences; step_us: step time for M = 1 .. len(step_us) rows.
+    Returns (lens int32 [B], expected tokens, throughput in tokens/s).
+    """
+    c = np.ascontiguousarray(np.asarray(conf, dtype=np.float32))
+    t = np.ascontiguousarray(np.asarray(step_us, dtype=np.float32))
+    b, g = c.shape
+    lens = np.zeros(b, np.int32)
+    tau, th = ctypes.c_double(), ctypes.c_double()
+    _check(lib.sv_schedule_prefix(b, g, c.ctypes.data_as(ctypes.c_void_p), t.ctypes.data_as(ctypes.c_void_p), len(t),
+                                  int(bool(early_stop)), lens.ctypes.data_as(ctypes.c_void_p), ctypes.byref(tau),
+                                  ctypes.byref(th)))
+    return lens, tau.value, th.value
+

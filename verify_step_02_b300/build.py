@@ -1,6 +1,7 @@
 """Build libsv.so in place: every CUDA source of the library for sm_103a.
 
-Usage: python -m verify_step_02_b300.build [--force]
+Usage: python verify_step_02_b300/build.py [--force] (run as a script: importing the
+package itself needs the built library).
 The shared library lands next to this file, so it travels with the source
 tree. Objects are cached under _build/ and rebuilt when a source or header
 is newer than its object.

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
           kv = kv_load(kc, off);
           vv = kv_load(vc, off);
         } else if (d == 0) {
-          atomicOr(a.status, kStBadPage);
+          atomicOr(a.status, pidx >= a.max_pages ? kStNoPage : kStBadPage);
         }
       }
       Ks[i * (hd + 1) + d] = kv;

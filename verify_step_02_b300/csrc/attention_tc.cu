@@ -8,22 +8,24 @@
 // heads of one KV head (the GQA group) and all block rows of the request are
 // the MMA's 128 rows (rho = j * group + g), so every K/V byte is read once.
 //
-// One CTA = (request, kv head, chunk of keys); the chunk (256 .. 4096 keys,
-// chosen by the host so the grid stays within a few waves) is processed in
+// The keys of one (request, kv head) are split over a thread-block cluster
+// of CS CTAs (CS chosen by the host from the batch so the grid fills the
+// SMs; each CTA's key range, a multiple of 64 keys, follows from the
+// request's actual length on the device). Each CTA processes its range in
 // sub-chunks of 64 keys through a three-stage K/V ring:
-//   warp 8   TMA: the Q tile once (the QKV epilogue left q / sqrt(hd) as a
+//   warp 16  TMA: the Q tile once (the QKV epilogue left q / sqrt(hd) as a
 //            hi/lo bf16 pair, q = hi + lo to ~16 bits; a 3D box of 64 dims x
 //            group heads x block rows lands it as rows rho = j * group + g),
-//            the chunk's page-table entries once into shared memory, then
-//            each sub-chunk's K and V pages (16 keys x 64 dims per box)
-//            straight from the page pool into the free stage;
-//   warp 9   S_j = Q K_j^T (M 128, N 64, K hd; hi and lo into one
+//            the range's page-table entries (256 at a time), then each
+//            sub-chunk's K and V pages (16 keys x 64 dims per box) straight
+//            from the page pool into the free stage;
+//   warp 17  S_j = Q K_j^T (M 128, N 64, K hd; hi and lo into one
 //            accumulator; S buffer j mod 2 in TMEM) and O_b += P_j V_j
 //            (b = j mod 2; V is the N-major operand), S_{j+1} issued before
 //            O_b += P_j V_j;
-//   warps 0-7, two sets of four (set b takes the sub-chunks j = b mod 2, so
-//            the two softmaxes overlap): one thread per row reads the row's
-//            64 scores, masks them (key <= C_r + j), keeps the set's running
+//   warps 0-15, two sets of eight (set b takes the sub-chunks j = b mod 2, so
+//            the two softmaxes overlap; two warps per row, 32 keys each): the
+//            row's scores are masked (key <= C_r + j), the set keeps its running
 //            maximum m_b and sum l_b, and writes P_j = exp(S_j - m_b) as a
 //            hi/lo bf16 pair into the set's P buffer once O_b += P_{j-2}
 //            V_{j-2} has completed. The maximum is raised only when a
@@ -31,16 +33,16 @@
 //            rescaled by e^(m_old - m_new)); otherwise p <= e^8 and O_b, l_b
 //            stay exact in float32 relative to the kept m_b.
 // At the end each row merges its two sets' (m_b, l_b, O_b) through their
-// log-sum-exp and writes the chunk's partial (m, l, O).
-// The partial (m, l, O) of each row goes to a second kernel, which merges the
-// chunks of a row:
+// log-sum-exp into the CTA's partial (m, l, O), kept in shared memory. After
+// a cluster barrier, rank i merges rows i R / CS .. of all CS partials over
+// distributed shared memory,
 //   out = sum_c O_c e^(m_c - M) / sum_c l_c e^(m_c - M), M = max_c m_c,
 // and writes the attention output as the next projection's x tensor.
 #include <cudaTypedefs.h>
 
 #include "device_util.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
-#include "prefetch.cuh"
 #include "tc_ptx.cuh"
 
 namespace sv {
@@ -50,8 +52,8 @@ using namespace tc;
 
 constexpr int kSub = 64;                              // keys per sub-chunk
 constexpr int kStages = 3;                            // K/V ring depth
-constexpr int kMaxChunk = 4096;                       // keys per CTA at most
-constexpr int kMaxChunkPages = kMaxChunk / 16;
+constexpr int kPageBlock = 256;                       // page-table entries the producer holds at once
+constexpr int kMaxCluster = 16;                       // CTAs per (request, kv head)
 constexpr int kSetWarps = 8;                          // a softmax set: two warps per 32-lane TMEM group
 constexpr int kSetThreads = kSetWarps * 32;
 constexpr int kRowWarps = 2 * kSetWarps;              // two sets, for even and odd sub-chunks
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* vmask_s = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // [kStages]: pages loaded
 
-  const int lin = blockIdx.y * gridDim.x + blockIdx.x, ncta = gridDim.x * gridDim.y;
+  const int lin = blockIdx.y * gridDim.x + blockIdx.x;
   unsigned long long* const rec = a.trace ? a.trace + static_cast<size_t>(lin) * kTraceWords : nullptr;
   if (rec && threadIdx.x == 0) {
     rec[0] = (static_cast<unsigned long long>(kTrAttn) << 48) | (static_cast<unsigned long long>(sm_id()) << 32) |
@@ -137,23 +139,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   pdl_trigger();
   pdl_wait();
   const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
-  const int r = blockIdx.x / nkv, h = blockIdx.x - r * nkv, chunk = blockIdx.y;
+  // blockIdx.x = (request, kv head, row tile): a row tile is a.q_rows block rows
+  // (a.q_rows * group <= 128 MMA rows), so a long block spans several tiles
+  const int rt = blockIdx.x % a.n_row_tiles, rh = blockIdx.x / a.n_row_tiles;
+  const int r = rh / nkv, h = rh - r * nkv;
+  const int CS = gridDim.y, rank = blockIdx.y;  // the cluster spans the grid's y dimension
   const int C = a.seq_len[r];
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
-  const int T = C + nrows;
-  const int k0 = chunk * a.chunk;
+  const int j0 = rt * a.q_rows;                                    // first block row of the tile
+  const int ntok = nrows - j0 < a.q_rows ? nrows - j0 : a.q_rows;  // its block rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  if (C < 0 || T > a.max_seq_len || k0 >= T) {
-    // no keys here (or a request flagged by the row preparation): this CTA
-    // only requests its share of the next product's weights into L2
-    if (warp == 0) l2_prefetch_window(a.pf, lin, ncta, lane);
+  // a request flagged by the row preparation, or a row tile past the block: every
+  // CTA of the cluster leaves here
+  if (C < 0 || C + nrows > a.max_seq_len || ntok <= 0) {
     if (tid == 0) trace_mark(rec, 6);
     return;
   }
   if (tid == 0) trace_mark(rec, 2);
-  const int nkeys = T - k0 < a.chunk ? T - k0 : a.chunk;
-  const int nsub = (nkeys + kSub - 1) / kSub;
-  const int R = nrows * group;
+  const int T = C + j0 + ntok;  // keys any row of the tile may see
+  // this CTA's keys [k0, k0 + nkeys): the T keys in CS ranges of a multiple of 64
+  const int per = ((T + CS - 1) / CS + kSub - 1) / kSub * kSub;
+  const int k0 = rank * per;
+  const int nkeys = T - k0 < per ? T - k0 : per;  // <= 0: no keys (an empty partial)
+  const int nsub = nkeys > 0 ? (nkeys + kSub - 1) / kSub : 0;
+  const int R = ntok * group;
+  // the CTA's partial (m, l, O) of each row, in the K/V ring once every MMA is done
+  float* Os = reinterpret_cast<float*>(smem + KV_OFF);        // [128 rows][HD]
+  float2* ML = reinterpret_cast<float2*>(smem + KV_OFF + 128 * HD * 4);  // [128 rows]
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -179,55 +191,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // S buffers at columns 0 and 64; set b's O at 128 + b * HD
   const uint32_t tS = tmem, tO = tmem + 128;
 
-  if (warp == kRowWarps) {
+  if (nsub == 0) {
+    // no keys in this CTA's range: an empty partial
+    for (int rho = tid; rho < 128; rho += kAttnThreads) ML[rho] = make_float2(-INFINITY, 0.f);
+  } else if (warp == kRowWarps) {
     // ------------------------------------------------------------ TMA producer
     const int* ptab = a.page_table + static_cast<long long>(r) * a.max_pages;
     if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
-      const uint32_t qbox = 128u * group * (a.max_rows / group);
+      const uint32_t qbox = 128u * group * a.q_rows;
       mbar_arrive_expect_tx(q_full, 2 * NH * qbox);
       const uint64_t polq = policy_evict_last();
 #pragma unroll
       for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh)
-          tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0, q_full,
+          tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0 + j0, q_full,
                       polq);
     }
-    // the chunk's page ids, all lookups in flight at once: page i sits in
-    // lane i % 32, register i / 32; -1 for a bad entry
+    // the range's page ids, kPageBlock at a time with all lookups in flight:
+    // page i of the block sits in lane i % 32, register i / 32; -1 for a bad entry
     const int npg = (nkeys + 15) >> 4;
-    int pg[kMaxChunkPages / 32];
+    int pg[kPageBlock / 32];
+    auto load_pages = [&](int blk) {
 #pragma unroll
-    for (int t = 0; t < kMaxChunkPages / 32; ++t) {
-      const int i = t * 32 + lane;
-      int page = -1;
-      if (i < npg) {
-        const int pidx = (k0 >> 4) + i;
-        page = pidx < a.max_pages ? ptab[pidx] : -1;
-        if (page < 0 || page >= a.n_pages) {
-          atomicOr(a.status, kStBadPage);
-          page = -1;
+      for (int t = 0; t < kPageBlock / 32; ++t) {
+        const int i = blk * kPageBlock + t * 32 + lane;
+        int page = -1;
+        if (i < npg) {
+          const int pidx = (k0 >> 4) + i;
+          page = pidx < a.max_pages ? ptab[pidx] : -1;
+          if (page < 0 || page >= a.n_pages) {
+            atomicOr(a.status, pidx >= a.max_pages ? kStNoPage : kStBadPage);
+            page = -1;
+          }
         }
+        pg[t] = page;
       }
-      pg[t] = page;
-    }
+    };
     const uint64_t pol = policy_evict_first();
     int issued = 0;
     for (int j = 0; j < nsub; ++j) {
       const int st = j % kStages;
+      const int pj = j * (kSub / 16);  // the sub-chunk's first page in the range
+      if (pj % kPageBlock == 0) load_pages(pj / kPageBlock);
       int ok = 1;
       if (lane == 0 && j >= kStages) ok = mbar_wait(kv_empty + st, (j / kStages - 1) & 1, abort_flag, kWaitNs);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      // lane p < 4 takes page i = 4 j + p of the chunk, from lane i % 32,
-      // register i / 32 (the same register for the sub-chunk's four pages)
-      const int pi = j * (kSub / 16) + (lane & 3);
-      const int t_sel = (j * (kSub / 16)) >> 5;
+      // lane p < 4 takes page i = pj + p of the range, from lane i % 32,
+      // register (i % kPageBlock) / 32 (the same register for the sub-chunk's four pages)
+      const int pi = pj + (lane & 3);
+      const int t_sel = (pj % kPageBlock) >> 5;
       int held = pg[0];
 #pragma unroll
-      for (int t = 1; t < kMaxChunkPages / 32; ++t) held = t == t_sel ? pg[t] : held;
+      for (int t = 1; t < kPageBlock / 32; ++t) held = t == t_sel ? pg[t] : held;
       int page = __shfl_sync(0xffffffffu, held, pi & 31);
       if (lane >= kSub / 16 || pi >= npg) page = -1;
       const uint32_t mask = __ballot_sync(0xffffffffu, page >= 0);
@@ -247,8 +266,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       ++issued;
     }
-    // the K/V loads are issued; HBM has room for the next product's weights
-    l2_prefetch_window(a.pf, lin, ncta, lane);
     if (lane == 0) {  // the copies land before the CTA can leave
       volatile int never = 0;
       mbar_wait(q_full, 0, &never, kWaitNs);
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int set = warp >> 3, lg = warp & 3, hf = (warp >> 2) & 1;
     const int rho = lg * 32 + lane;
     const bool live = rho < R;
-    const int lim = live ? C + rho / group : -1;  // last key this row may see
+    const int lim = live ? C + j0 + rho / group : -1;  // last key this row may see
     const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t to = tO + set * HD;
     uint8_t* pt = smem + P_OFF + set * PB;
@@ -450,7 +467,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_arrive(p_ready + set);
     }
 
-    // merge the two sets' (m, l, O) of each row, then write the chunk partial
+    // merge the two sets' (m, l, O) of each row into the CTA's partial, in shared memory
     int okw = 0;
     if (lane == 0) okw = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
     okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -464,7 +481,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float w0 = m0 == -INFINITY ? 0.f : __expf(m0 - M);
       const float w1 = m1 == -INFINITY ? 0.f : __expf(m1 - M);
       const bool has1 = nsub > 1;  // set 1 accumulated at least one P V product
-      const long long slot = (static_cast<long long>(blockIdx.x) * a.max_chunks + chunk) * a.max_rows + rho;
       tc_fence_after();
       // warp (set, hf) writes O dims (2 set + hf) HD / 4 .. + HD / 4 of the merged row
       const int qd = (set * 2 + hf) * (HD / 4);
@@ -474,20 +490,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float o0[16], o1[16];
         tmem_ld16(tO + lane_base + col, o0);
         if (has1) tmem_ld16(tO + HD + lane_base + col, o1);
-        if (live) {
-          float4* po = reinterpret_cast<float4*>(a.partials + slot * HD + col);
+        float4* po = reinterpret_cast<float4*>(Os + rho * HD + col);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float x[4];
+        for (int i = 0; i < 4; ++i) {
+          float x[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-              x[t] = (w0 != 0.f ? o0[4 * i + t] * w0 : 0.f) + (has1 && w1 != 0.f ? o1[4 * i + t] * w1 : 0.f);
-            __stcg(po + i, make_float4(x[0], x[1], x[2], x[3]));
-          }
+          for (int t = 0; t < 4; ++t)
+            x[t] = (w0 != 0.f ? o0[4 * i + t] * w0 : 0.f) + (has1 && w1 != 0.f ? o1[4 * i + t] * w1 : 0.f);
+          po[i] = make_float4(x[0], x[1], x[2], x[3]);
         }
       }
-      if (live && set == 0 && hf == 0)
-        __stcg(reinterpret_cast<float2*>(a.partials + a.ml_offset) + slot, make_float2(M, l0 * w0 + l1 * w1));
+      if (set == 0 && hf == 0) ML[rho] = live ? make_float2(M, l0 * w0 + l1 * w1) : make_float2(-INFINITY, 0.f);
+    } else if (set == 0 && hf == 0) {
+      ML[rho] = make_float2(-INFINITY, 0.f);
     }
     if (tid == 0) trace_mark(rec, 5);
   }
@@ -498,85 +513,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (tid == 0) trace_mark(rec, 7);
+  // every CTA of the cluster has its partial in shared memory
+  if (CS > 1) cluster_sync();
+  if (tid == 0) trace_mark(rec, 8);
+  {
+    // rank i merges rows [i rpr, (i + 1) rpr) of the CS partials: first each row's
+    // weights e^(m_c - M) / sum_c l_c e^(m_c - M) (one thread per row, into the
+    // free P buffers), then the output rows, 4 dims per item
+    const int rpr = (R + CS - 1) / CS;
+    const int rr0 = rank * rpr, rr1 = rr0 + rpr < R ? rr0 + rpr : R;
+    const uint32_t os_addr = smem_u32(Os), ml_addr = smem_u32(ML);
+    float* wts = reinterpret_cast<float*>(smem + P_OFF);            // [rpr][kMaxCluster]
+    float2* mls = reinterpret_cast<float2*>(smem + P_OFF + 16384);   // [rpr][kMaxCluster]
+    const int nrr = rr1 - rr0;
+    // every rank's (m, l) of this rank's rows, all loads in flight
+    for (int it = tid; it < nrr * CS; it += kAttnThreads) {
+      const int rr = it / CS, k = it - rr * CS;
+      mls[rr * kMaxCluster + k] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * (rr0 + rr), static_cast<uint32_t>(k)));
+    }
+    __syncthreads();
+    for (int rr = tid; rr < nrr; rr += kAttnThreads) {
+      float M = -INFINITY;
+      for (int k = 0; k < CS; ++k) M = fmaxf(M, mls[rr * kMaxCluster + k].x);
+      float L = 0.f;
+      for (int k = 0; k < CS; ++k) {
+        const float2 v = mls[rr * kMaxCluster + k];
+        const float w = v.x == -INFINITY ? 0.f : __expf(v.x - M);
+        wts[rr * kMaxCluster + k] = w;
+        L += v.y * w;
+      }
+      // L = 0 only for rows whose keys were all on bad pages (flagged): output 0
+      const float inv = L > 0.f ? 1.0f / L : 0.f;
+      for (int k = 0; k < CS; ++k) wts[rr * kMaxCluster + k] *= inv;
+    }
+    __syncthreads();
+    if (tid == 0) trace_mark(rec, 9);
+    constexpr int D4 = HD / 4;
+    constexpr int KB = 8;  // ranks whose O loads are in flight together
+    for (int it = tid; it < nrr * D4; it += kAttnThreads) {
+      const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k0 = 0; k0 < CS; k0 += KB) {
+        float4 o[KB];
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk)
+          if (k0 + kk < CS && wts[rr * kMaxCluster + k0 + kk] != 0.f)
+            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (rho * HD + d), static_cast<uint32_t>(k0 + kk)));
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+          const float w = k0 + kk < CS ? wts[rr * kMaxCluster + k0 + kk] : 0.f;
+          if (w != 0.f) {
+            acc.x += o[kk].x * w;
+            acc.y += o[kk].y * w;
+            acc.z += o[kk].z * w;
+            acc.w += o[kk].w * w;
+          }
+        }
+      }
+      const int jrow = j0 + rho / group, g = rho % group;
+      const long long orow = static_cast<long long>(row0 + jrow) * a.n_heads * HD + (h * group + g) * HD + d;
+      store_x4(a.out, a.out_plane, orow, acc, a.x_pair);
+    }
+  }
+  if (tid == 0) trace_mark(rec, 5);
+  // no CTA leaves while a rank of its cluster may still read its partial
+  if (CS > 1) cluster_sync();
   if (tid == 0) {
     if (*abort_flag) atomicOr(a.status, kStTimeout);
     trace_mark(rec, 6);
   }
-}
-
-// One warp per (request, kv head, row): merge the row's chunk partials. Lanes
-// read the chunks' (m, l) once, form the weights e^(m_c - M) in shared memory
-// and the denominator; then each lane sums its hd / 32 output dims over the
-// chunks.
-template <int HD>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
-  constexpr int D = HD / 32;
-  extern __shared__ float s_w[];  // [8 warps][max_chunks]
-  const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
-  const int item = blockIdx.x, r = item / nkv, h = item - r * nkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rho = blockIdx.y * 8 + warp;
-  unsigned long long* const rec =
-      a.trace_merge ? a.trace_merge + (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * kTraceWords
-                    : nullptr;
-  if (rec && threadIdx.x == 0) {
-    rec[0] = (static_cast<unsigned long long>(kTrMerge) << 48) | (static_cast<unsigned long long>(tc::sm_id()) << 32) |
-             (blockIdx.y * gridDim.x + blockIdx.x);
-    tc::trace_mark(rec, 1);
-  }
-  pdl_trigger();
-  pdl_wait();
-  if (rec && threadIdx.x == 0) tc::trace_mark(rec, 2);
-  const int C = a.seq_len[r];
-  const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
-  const int T = C + nrows;
-  if (C < 0 || T > a.max_seq_len || rho >= nrows * group) return;
-  const int nchunks = (T + a.chunk - 1) / a.chunk;
-  const long long slot0 = static_cast<long long>(item) * a.max_chunks * a.max_rows + rho;
-  const float2* ml = reinterpret_cast<const float2*>(a.partials + a.ml_offset) + slot0;
-  float* w = s_w + warp * a.max_chunks;
-  float M = -INFINITY;
-  for (int c = lane; c < nchunks; c += 32) {
-    const float2 v = __ldcg(ml + static_cast<long long>(c) * a.max_rows);
-    w[c] = v.x;
-    M = fmaxf(M, v.x);
-  }
-  M = warp_max(M);
-  float L = 0.f;
-  for (int c = lane; c < nchunks; c += 32) {
-    const float mc = w[c];
-    const float wc = mc == -INFINITY ? 0.f : expf(mc - M);
-    L += __ldcg(ml + static_cast<long long>(c) * a.max_rows).y * wc;
-    w[c] = wc;
-  }
-  L = warp_sum(L);
-  __syncwarp();
-  float o[D];
-#pragma unroll
-  for (int i = 0; i < D; ++i) o[i] = 0.f;
-  const float* po = a.partials + slot0 * HD + lane * D;
-#pragma unroll 4
-  for (int c = 0; c < nchunks; ++c) {
-    const float wc = w[c];
-    const float* p = po + static_cast<long long>(c) * a.max_rows * HD;
-    if constexpr (D == 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
-      o[0] = fmaf(wc, v.x, o[0]);
-      o[1] = fmaf(wc, v.y, o[1]);
-      o[2] = fmaf(wc, v.z, o[2]);
-      o[3] = fmaf(wc, v.w, o[3]);
-    } else {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
-      o[0] = fmaf(wc, v.x, o[0]);
-      o[1] = fmaf(wc, v.y, o[1]);
-    }
-  }
-  const int j = rho / group, g = rho - j * group;
-  const long long orow = static_cast<long long>(row0 + j) * a.n_heads * HD + (h * group + g) * HD + lane * D;
-  const float invL = 1.0f / L;
-#pragma unroll
-  for (int i = 0; i < D; ++i) store_x(a.out, a.out_plane, orow + i, o[i] * invL, a.x_pair);
-  if (rec && lane == 0) atomicMax(rec + 6, tc::global_ns());
 }
 
 size_t attn_tc_smem(int hd) {
@@ -585,48 +591,89 @@ size_t attn_tc_smem(int hd) {
 }
 
 template <int HD>
-cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                      cudaStream_t s) {
-  const size_t smem = attn_tc_smem(HD);
+cudaError_t set_attrs() {
   static bool attr_set[64] = {};  // per device
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = cudaSuccess;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_merge_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  e = launch_k(attn_tc_kernel<HD>, dim3(B * a.n_kv_heads, a.max_chunks), dim3(kAttnThreads), smem, s, a.pdl != 0, q,
-               k, v, a);
+  if (dev >= 0 && dev < 64 && attr_set[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(attn_tc_smem(HD)));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
+  return e;
+}
+
+template <int HD>
+cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                      cudaStream_t s) {
+  cudaError_t e = set_attrs<HD>();
   if (e != cudaSuccess) return e;
-  const size_t msmem = sizeof(float) * 8 * a.max_chunks;
-  return launch_k(attn_merge_kernel<HD>, dim3(B * a.n_kv_heads, (a.max_rows + 7) / 8), dim3(256), msmem, s,
-                  a.pdl != 0, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * a.n_kv_heads * a.n_row_tiles, a.cl_size);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = attn_tc_smem(HD);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(a.cl_size);
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, q, k, v, a);
+}
+
+template <int HD>
+int max_clusters_hd(int cs) {
+  if (set_attrs<HD>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, cs);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = attn_tc_smem(HD);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace
 
-int attention_tc_chunk(int batch, int n_kv_heads, int max_seq_len, int sm_count) {
-  // keys per CTA: 256, doubled (up to 4096) while the grid would exceed two waves
-  int chunk = 256;
-  while (chunk < kMaxChunk &&
-         static_cast<long long>(batch) * n_kv_heads * ((max_seq_len + chunk - 1) / chunk) > 2LL * sm_count)
-    chunk *= 2;
-  return chunk;
+int attention_tc_cluster(long long items, int head_dim, int sm_count) {
+  // CTAs per (request, kv head, row tile): about two waves of CTAs over the SMs,
+  // at most kMaxCluster, halved while the device cannot hold the clusters one
+  // wave needs
+  long long want = (2LL * sm_count + items - 1) / items;
+  int cs = 1;
+  while (cs * 2 <= want && cs * 2 <= kMaxCluster) cs *= 2;
+  for (; cs > 1; cs /= 2) {
+    const int mc = head_dim == 128 ? max_clusters_hd<128>(cs) : max_clusters_hd<64>(cs);
+    const long long need = items < sm_count / cs ? items : sm_count / cs;
+    if (mc * 10LL >= need * 9) break;
+  }
+  return cs;
 }
 
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len) {
-  const long long max_chunks = (static_cast<long long>(max_seq_len) + 255) / 256;
-  return (head_dim == 64 || head_dim == 128) && page_size == 16 && max_rows <= 128 &&
-         max_chunks * 8 * sizeof(float) <= 200 * 1024;
+  (void)max_seq_len;
+  (void)max_rows;  // any block length: rows beyond one MMA tile go to further row tiles
+  return (head_dim == 64 || head_dim == 128) && page_size == 16;
 }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
                                 const CUtensorMap& v, cudaStream_t s) {
-  if (a.chunk < 256 || a.chunk > kMaxChunk || a.chunk % kSub || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
+  if (a.cl_size < 1 || a.cl_size > kMaxCluster || a.q_rows < 1 || a.q_rows * (a.n_heads / a.n_kv_heads) > 128 ||
+      a.n_row_tiles < 1 || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
     return cudaErrorInvalidValue;
   return a.head_dim == 128 ? launch_hd<128>(a, B, q, k, v, s) : launch_hd<64>(a, B, q, k, v, s);
 }

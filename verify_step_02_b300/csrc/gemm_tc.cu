@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "gemm_tc_plan.h"
 #include "internal.h"
@@ -13,26 +14,54 @@ namespace {
 
 using namespace tcg;
 
-template <bool PAIR>
+template <bool PAIR, bool CL>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
-  if (a.wdtype == SV_W12) {
+  if (a.wdtype == SV_W12 || CL) {
+    const bool w12 = a.wdtype == SV_W12;
     switch (a.tc_nt) {
-      case 32: return gemm_tc_launch<32, PAIR, true>(a, w, x, s);
-      case 64: return gemm_tc_launch<64, PAIR, true>(a, w, x, s);
+      case 32: return w12 ? gemm_tc_launch<32, PAIR, true, CL>(a, w, x, s) : gemm_tc_launch<32, PAIR, false, CL>(a, w, x, s);
+      case 64: return w12 ? gemm_tc_launch<64, PAIR, true, CL>(a, w, x, s) : gemm_tc_launch<64, PAIR, false, CL>(a, w, x, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.tc_nt) {
-    case 32: return gemm_tc_launch<32, PAIR, false>(a, w, x, s);
-    case 64: return gemm_tc_launch<64, PAIR, false>(a, w, x, s);
-    case 96: return gemm_tc_launch<96, PAIR, false>(a, w, x, s);
-    case 128: return gemm_tc_launch<128, PAIR, false>(a, w, x, s);
-    case 160: return gemm_tc_launch<160, PAIR, false>(a, w, x, s);
-    case 192: return gemm_tc_launch<192, PAIR, false>(a, w, x, s);
-    case 224: return gemm_tc_launch<224, PAIR, false>(a, w, x, s);
-    case 256: return gemm_tc_launch<256, PAIR, false>(a, w, x, s);
+    case 32: return gemm_tc_launch<32, PAIR, false, false>(a, w, x, s);
+    case 64: return gemm_tc_launch<64, PAIR, false, false>(a, w, x, s);
+    case 96: return gemm_tc_launch<96, PAIR, false, false>(a, w, x, s);
+    case 128: return gemm_tc_launch<128, PAIR, false, false>(a, w, x, s);
+    case 160: return gemm_tc_launch<160, PAIR, false, false>(a, w, x, s);
+    case 192: return gemm_tc_launch<192, PAIR, false, false>(a, w, x, s);
+    case 224: return gemm_tc_launch<224, PAIR, false, false>(a, w, x, s);
+    case 256: return gemm_tc_launch<256, PAIR, false, false>(a, w, x, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Resident clusters of cs CTAs for the cluster-split instantiation of a plan,
+// looked up once per (device, configuration).
+int max_clusters(int nt, bool pair, bool w12, int cs, int stages) {
+  struct Entry {
+    int dev, nt, pair, w12, cs, stages, n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.nt == nt && e.pair == pair && e.w12 == w12 && e.cs == cs && e.stages == stages) return e.n;
+  int n = 0;
+#define SV_MC(NT, P, W) n = gemm_tc_max_clusters<NT, P, W, true>(cs, stages)
+  if (nt == 32) {
+    if (pair) { if (w12) SV_MC(32, true, true); else SV_MC(32, true, false); }
+    else { if (w12) SV_MC(32, false, true); else SV_MC(32, false, false); }
+  } else if (nt == 64) {
+    if (pair) { if (w12) SV_MC(64, true, true); else SV_MC(64, true, false); }
+    else { if (w12) SV_MC(64, false, true); else SV_MC(64, false, false); }
+  }
+#undef SV_MC
+  cache.push_back({dev, nt, pair, w12, cs, stages, n});
+  return n;
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -114,6 +143,44 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
   a.tc_stages = w12 && a.tc_nt > kW12MaxNT ? 0 : tc_stages_for(a.tc_nt, pair2, a.tc_ks, w12);
   a.k_splits = 1;
   a.k_chunk = K;
+  a.cl_size = 0;
+  a.cl_tiles = 0;
+  // Small token tiles: the cluster split, when some (CTAs per cluster 2 .. 8, tiles
+  // per cluster) fits the device in one wave on at least 85% of the SMs (one SM
+  // streams only about its even share of HBM bandwidth with this pipeline depth)
+  // with per-CTA work within 1.2x of stream-K's: the fewest units per CTA wins,
+  // then the larger cluster (a smaller slice per rank, so more pipeline stages).
+  if (a.tc_nt > kClusterMaxNT || a.tc_stages < 2) return;
+  const long long ntt = static_cast<long long>(a.n_tiles) * a.m_tiles;
+  const long long sk_work = (U + a.grid_p - 1) / a.grid_p;
+  long long best_work = 0, best_ctas = 0;
+  int best_cs = 0, best_tc = 0, best_st = 0;
+  // power-of-two cluster sizes only: they tile the GPCs, so a whole wave of
+  // clusters still fits while the previous kernel's CTAs leave their SMs
+  for (int cs = 2; cs <= kClusterMaxSize && cs <= a.kb; cs *= 2) {
+    const int st_cl = tc_stages_for(a.tc_nt, pair2, a.tc_ks, w12, cs);
+    if (st_cl < 2) continue;
+    int mc = -1;
+    for (int tc = 1; tc <= 8; ++tc) {
+      const long long ncl = (ntt + tc - 1) / tc;
+      if (ncl * cs > sm_count || ncl * cs * 20 < 17LL * sm_count) continue;
+      if (mc < 0) mc = max_clusters(a.tc_nt, pair2, w12, cs, st_cl);
+      if (ncl > mc) continue;
+      const long long work = static_cast<long long>(tc) * ((a.kb + cs - 1) / cs), ctas = ncl * cs;
+      if (best_cs == 0 || work < best_work || (work == best_work && cs > best_cs)) {
+        best_work = work;
+        best_ctas = ctas;
+        best_cs = cs;
+        best_tc = tc;
+        best_st = st_cl;
+      }
+    }
+  }
+  if (best_cs == 0 || best_work * 5 > sk_work * 6) return;
+  a.cl_size = best_cs;
+  a.cl_tiles = best_tc;
+  a.grid_p = static_cast<int>(best_ctas);
+  a.tc_stages = best_st;
 }
 
 size_t gemm_tc_partial_floats(const GemmArgs& a) {
@@ -129,7 +196,9 @@ bool gemm_tc_supported(int wdtype, int pair, int ffn) {
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
   if (!gemm_tc_supported(a.wdtype, a.pair, a.ffn) || a.tc_stages < 2) return cudaErrorInvalidValue;
-  return a.x_kind == kXPair ? launch_pair<true>(a, w, x, s) : launch_pair<false>(a, w, x, s);
+  if (a.cl_size > 0)
+    return a.x_kind == kXPair ? launch_pair<true, true>(a, w, x, s) : launch_pair<false, true>(a, w, x, s);
+  return a.x_kind == kXPair ? launch_pair<true, false>(a, w, x, s) : launch_pair<false, false>(a, w, x, s);
 }
 
 }  // namespace sv

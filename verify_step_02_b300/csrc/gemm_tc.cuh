@@ -7,12 +7,23 @@
 // rows per tile, the MMA's M), and the block's tokens are its N (32 .. 256
 // columns). Every weight byte is read from HBM exactly once per launch.
 //
-// Work split ("stream-K"): the launch has P <= #SM CTAs and U = tiles x K
-// blocks of 64 units of work; CTA c takes units [c U / P, (c+1) U / P), so
-// every SM streams the same number of weight bytes. A tile whose K range is
-// shared by several CTAs is finished by the last of them to arrive, which sums
-// the partial tiles in CTA order (a fixed order: results do not depend on
-// timing) and runs the projection's epilogue. No CTA waits on another.
+// Two ways to spread the K range of the tiles over the SMs:
+//   stream-K   P <= #SM CTAs share U = tiles x K blocks units; CTA c takes
+//              units [c U / P, (c+1) U / P), so every SM streams the same
+//              bytes. A tile whose K range is shared by several CTAs is
+//              finished by the last of them to arrive, which sums the partial
+//              tiles (in global memory) in CTA order and runs the epilogue.
+//   cluster    (token tiles of at most 64 columns, the small projections)
+//              clusters of CS CTAs own whole tiles; the CTAs of a cluster split
+//              each tile's K blocks evenly. Each CTA leaves its partial tile in
+//              its own shared memory; then rank r sums a 1/CS share of the
+//              tile's tokens over the CS partials through distributed shared
+//              memory, in rank order (a reduce-scatter), and runs their
+//              epilogue from inputs it staged in shared memory while the
+//              weights streamed. The hand-off at the end of the product then
+//              needs no round trip through L2, which is what the end of a
+//              launch waits on, and each SM reduces and finishes 1/CS of it.
+// Both orders are fixed, so results do not depend on timing.
 //
 // Roles inside a CTA (384 threads; W12 weights: 512):
 //   warp 0     one thread issues TMA loads of the weight tile (two 64-row
@@ -21,7 +32,7 @@
 //   warp 1     allocates the TMEM accumulators (two buffers of NT columns) and
 //              one thread issues tcgen05.mma (M 128, N NT, K 16) per stage;
 //   warps 4-7  read finished accumulators out of TMEM (warp w reads lanes
-//              32 (w % 4) ..), and write partial tiles or run the epilogue;
+//              32 (w % 4) ..), and hand off partial tiles or run the epilogue;
 //              warps 8-11 share the reduction and the epilogue (bf16), or
 //              with warps 2, 3 and 12-15 rebuild the W12 tiles.
 // Every wait is bounded; a wait that runs out sets the status word's timeout
@@ -34,7 +45,6 @@
 #include "epilogue.cuh"
 #include "gemm_tc_plan.h"
 #include "internal.h"
-#include "prefetch.cuh"
 #include "tc_ptx.cuh"
 
 namespace sv {
@@ -54,7 +64,36 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
   return static_cast<int>(((x + 1) * P + U - 1) / U - 1);
 }
 
-template <int NT, bool PAIR, bool W12>
+// The units (tile, K block) of one CTA, in processing order: a contiguous
+// range of the tile-major order (stream-K), or every K block of the CTA's
+// slice [k0, k1) of each tile in [t0, t1) (cluster split).
+struct CtaUnits {
+  long long u0, n;   // stream-K: first unit; both: units of this CTA
+  long long t0;      // cluster: first tile
+  int k0, nk;        // cluster: first K block and K blocks per tile
+  int kb;            // K blocks of a whole tile
+  bool cl;
+  __device__ __forceinline__ void at(long long i, long long& t, int& kbi) const {
+    if (cl) {
+      const long long q = i / nk;
+      t = t0 + q;
+      kbi = k0 + static_cast<int>(i - q * nk);
+    } else {
+      const long long u = u0 + i;
+      t = u / kb;
+      kbi = static_cast<int>(u - t * kb);
+    }
+  }
+  // one past the last unit of the tile that unit i belongs to
+  __device__ __forceinline__ long long seg_end(long long i) const {
+    if (cl) return (i / nk + 1) * nk;
+    const long long t = (u0 + i) / kb;
+    const long long e = (t + 1) * kb - u0;
+    return e < n ? e : n;
+  }
+};
+
+template <int NT, bool PAIR, bool W12, bool CL>
 __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                    const GemmArgs a) {
@@ -74,28 +113,61 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   constexpr int EPT = W12 ? 128 : kEpiThreads;          // epilogue threads (W12: warps 8-11 rebuild weights)
   constexpr int NCONV = kTcThreadsW12 / 32 - 6;         // W12 rebuild warps: 2, 3, 8 .. 15
   static_assert(!W12 || KS == 128, "W12 tiles are 128 elements wide");
+  static_assert(!CL || NT <= kClusterMaxNT, "cluster split: token tiles of at most kClusterMaxNT columns");
+  // (the cluster split takes 2 .. 8 CTAs per cluster, so a rank's slice is at most 32 tokens)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.tc_stages;
   uint8_t* aring = smem + static_cast<size_t>(S) * STAGE;  // W12: rebuilt bf16 weight tiles, 2 x NSUB x 16 KB
+  // stream-K: Ys [128][33] and the launch's per-token data. Cluster split: the rank's
+  // token slice of SL columns: Ys [128][SL + 1], staged epilogue inputs Es [128][SL],
+  // and this CTA's partial tile Xp, row-major [row][NT + 4] (the pad keeps a warp's
+  // 16-byte accesses to distinct banks)
+  constexpr int XLD = NT + 4;
+  const int SL = CL ? cl_slice(NT, a.cl_size) : 32;
+  const int YLD = CL ? SL + 1 : kYsLd;
   float* Ys = reinterpret_cast<float*>(aring + (W12 ? kW12Ring * NSUB * kABytes : 0));
-  EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * kYsLd);
+  EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * YLD);
   TokData* tok = reinterpret_cast<TokData*>(esm + 1);
-  uint64_t* full = reinterpret_cast<uint64_t*>(tok + 1);
+  float* Xp = reinterpret_cast<float*>(esm + 1);
+  float* Es = Xp + kGemmBN * XLD;
+  uint64_t* full = CL ? reinterpret_cast<uint64_t*>(Es + kGemmBN * SL) : reinterpret_cast<uint64_t*>(tok + 1);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* afull = drain + 1;     // W12 ring: rebuilt tile ready
   uint64_t* aempty = afull + 2;    // W12 ring: tile consumed by the MMAs
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + 2);
+  uint64_t* xr_full = aempty + 2;  // cluster: every rank's partial of the current tile is in place
+  uint64_t* xr_free = xr_full + 1; // cluster: every rank has read this CTA's partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xr_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = a.grid_p, c = blockIdx.x;
   const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
-  const long long u0 = c * U / P, u1 = (c + 1) * U / P;
+  const int CS = CL ? a.cl_size : 1;
+  const int rank = CL ? static_cast<int>(cluster_ctarank()) : 0;
+  CtaUnits W;
+  W.kb = a.kb;
+  W.cl = CL;
+  if (CL) {
+    const long long ntt = static_cast<long long>(a.n_tiles) * a.m_tiles;
+    W.t0 = static_cast<long long>(c / CS) * a.cl_tiles;
+    const long long t1 = W.t0 + a.cl_tiles < ntt ? W.t0 + a.cl_tiles : ntt;
+    W.k0 = rank * a.kb / CS;
+    W.nk = (rank + 1) * a.kb / CS - W.k0;
+    W.u0 = 0;
+    W.n = (t1 > W.t0 ? t1 - W.t0 : 0) * W.nk;
+  } else {
+    W.u0 = c * U / P;
+    W.n = (c + 1) * U / P - W.u0;
+    W.t0 = 0;
+    W.k0 = 0;
+    W.nk = a.kb;
+  }
+  const long long NU = W.n;
   unsigned long long* const rec = a.trace ? a.trace + static_cast<size_t>(c) * kTraceWords : nullptr;
   if (rec && threadIdx.x == 0) {
     rec[0] = (static_cast<unsigned long long>(kTrGemm) << 48) | (static_cast<unsigned long long>(sm_id()) << 32) |
@@ -117,6 +189,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       mbar_init(acc_empty + i, 128);  // the TMEM-reading warpgroup
     }
     mbar_init(drain, 1);
+    mbar_init(xr_full, CS);  // one arrival per rank of the cluster: its partial is in place
+    mbar_init(xr_free, CS);  // one arrival per rank: it has read this CTA's partial
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -126,7 +200,11 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, TCOLS);
   tc_fence_before();
-  __syncthreads();
+  // cluster: every CTA's barriers exist before any rank arrives on them remotely
+  if (CL)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
@@ -135,19 +213,17 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-      // weight boxes, all sub-tiles back to back: each row's KS elements are
-      // requested together (contiguous bytes in HBM)
       const int w12_row_blocks = (a.n_rows + 63) / 64;
       // bytes one unit brings into its stage (W12: row halves past the matrix are not read)
-      auto unit_bytes = [&](long long u) -> uint32_t {
+      auto unit_bytes = [&](long long t) -> uint32_t {
         if (!W12) return STAGE;
-        const int nt = static_cast<int>(u / a.kb / a.m_tiles);
+        const int nt = static_cast<int>(t / a.m_tiles);
         const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : nt * kGemmBN + kGemmBN / 2;
         return STAGE - (r1 / 64 < w12_row_blocks ? 0 : 3 * 4096);
       };
-      auto load_w = [&](long long u, uint8_t* st, uint64_t* bar) {
-        const long long t = u / a.kb;
-        const int kb = static_cast<int>(u - t * a.kb);
+      // weight boxes, all sub-tiles back to back: each row's KS elements are
+      // requested together (contiguous bytes in HBM)
+      auto load_w = [&](long long t, int kb, uint8_t* st, uint64_t* bar) {
         const int nt = static_cast<int>(t / a.m_tiles);
         const int r0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
         const int r1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : r0 + kGemmBN / 2;
@@ -171,9 +247,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
           }
         }
       };
-      auto load_x = [&](long long u, uint8_t* st, uint64_t* bar) {
-        const long long t = u / a.kb;
-        const int kb = static_cast<int>(u - t * a.kb);
+      auto load_x = [&](long long t, int kb, uint8_t* st, uint64_t* bar) {
         const int mt = static_cast<int>(t - (t / a.m_tiles) * a.m_tiles);
 #pragma unroll
         for (int q = 0; q < NSUB; ++q) {
@@ -188,24 +262,35 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       };
       // The weights of the first stages do not depend on earlier kernels:
       // request them before waiting for those kernels, then the activations.
-      const long long npre = u1 - u0 < S ? u1 - u0 : S;
+      const long long npre = NU < S ? NU : S;
       for (long long i = 0; i < npre; ++i) {
+        long long t;
+        int kb;
+        W.at(i, t, kb);
         uint8_t* st = smem + static_cast<size_t>(i) * STAGE;
-        mbar_arrive_expect_tx(full + i, unit_bytes(u0 + i));
-        load_w(u0 + i, st, full + i);
+        mbar_arrive_expect_tx(full + i, unit_bytes(t));
+        load_w(t, kb, st, full + i);
       }
       pdl_wait();
       trace_mark(rec, 2);
-      for (long long i = 0; i < npre; ++i) load_x(u0 + i, smem + static_cast<size_t>(i) * STAGE, full + i);
+      for (long long i = 0; i < npre; ++i) {
+        long long t;
+        int kb;
+        W.at(i, t, kb);
+        load_x(t, kb, smem + static_cast<size_t>(i) * STAGE, full + i);
+      }
       int stage = static_cast<int>(npre % S);
       uint32_t phase = npre == S ? 1u : 0u;
       long long issued = npre;
-      for (long long u = u0 + npre; u < u1; ++u) {
+      for (long long i = npre; i < NU; ++i) {
         if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) break;
+        long long t;
+        int kb;
+        W.at(i, t, kb);
         uint8_t* st = smem + static_cast<size_t>(stage) * STAGE;
-        mbar_arrive_expect_tx(full + stage, unit_bytes(u));
-        load_w(u, st, full + stage);
-        load_x(u, st, full + stage);
+        mbar_arrive_expect_tx(full + stage, unit_bytes(t));
+        load_w(t, kb, st, full + stage);
+        load_x(t, kb, st, full + stage);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -222,10 +307,6 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
         }
       }
     }
-    // every load of this CTA is issued: HBM would go idle through the tail, so
-    // request the next product's first weights into L2
-    __syncwarp();
-    if (!*abort_flag) l2_prefetch_window(a.pf, c, P, lane);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -233,14 +314,13 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       int stage = 0, seg = 0, ai = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (long long u = u0; u < u1 && ok;) {
-        const long long t = u / a.kb;
-        const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+      for (long long i = 0; i < NU && ok;) {
+        const long long iend = W.seg_end(i);
         const int b = seg & 1;
         if (!mbar_wait(acc_empty + b, ((seg >> 1) & 1) ^ 1u, abort_flag, kWaitNs)) break;
         tc_fence_after();
         const uint32_t d = tmem + b * ACC;
-        for (long long v = u; v < uend; ++v) {
+        for (long long v = i; v < iend; ++v) {
           // W12: the rebuild warps saw this stage land before they filled the tile
           if (!mbar_wait(W12 ? afull + ai % kW12Ring : full + stage, W12 ? (ai / kW12Ring) & 1 : phase, abort_flag,
                          kWaitNs)) {
@@ -257,7 +337,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = smem_desc_sw128(sa + k * 32);
-              mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > u || q > 0 || k > 0) ? 1u : 0u);
+              mma_bf16(d, ad, smem_desc_sw128(sb + k * 32), idesc, (v > i || q > 0 || k > 0) ? 1u : 0u);
               if (PAIR && !FUSE) mma_bf16(d, ad, smem_desc_sw128(sb + BX + k * 32), idesc, 1u);
             }
           }
@@ -272,7 +352,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
         if (!ok) break;
         mma_commit(acc_full + b);
         ++seg;
-        u = uend;
+        i = iend;
       }
       trace_mark(rec, 4);
       // every MMA issued above has completed once `drain` flips
@@ -301,7 +381,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     int ai = 0;
-    for (long long u = u0; u < u1; ++u, ++ai) {
+    for (long long i = 0; i < NU; ++i, ++ai) {
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait(full + stage, phase, abort_flag, kWaitNs) &&
@@ -345,26 +425,43 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   } else if (warp >= 4 && warp < 4 + EPT / 32) {
     // ------------------------------------------------------------ epilogue
     // Warpgroup A (warps 4-7) reads the accumulators out of TMEM (warp w reads
-    // lanes 32 (w % 4) ..) and writes partial tiles; with two warpgroups both
-    // share the split reduction (16 columns each) and the tile epilogue.
+    // lanes 32 (w % 4) ..); with two warpgroups both share the reduction (16
+    // columns each) and the tile epilogue.
     pdl_wait();  // reads what earlier kernels wrote (h, norm statistics, row maps)
     const int et2 = threadIdx.x - 128;          // 0 .. EPT - 1
     const bool grpA = et2 < 128;
     const int et = et2 & 127;                   // tile row
     // per-token data of the whole launch, while the weights stream in
-    const TokData* td = a.M <= kTokMax ? tok : nullptr;
+    const TokData* td = !CL && a.M <= kTokMax ? tok : nullptr;
     if (td)
       for (int m = et2; m < a.M; m += EPT) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
     auto sync = [] { named_bar(1, EPT); };
     sync();
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int slot0_tile = static_cast<int>(u0 / a.kb);
+    const long long slot0_tile = NU > 0 ? (W.u0 / a.kb) : 0;
     int seg = 0;
-    for (long long u = u0; u < u1;) {
-      const long long t = u / a.kb;
-      const long long uend = u1 < (t + 1) * a.kb ? u1 : (t + 1) * a.kb;
+    for (long long i = 0; i < NU;) {
+      const long long iend = W.seg_end(i);
+      long long t;
+      int kb_first;
+      W.at(i, t, kb_first);
       const int nt = static_cast<int>(t / a.m_tiles), mt = static_cast<int>(t - (long long)nt * a.m_tiles);
+      const int m_base = mt * NT;
+      const int mtot = a.M - m_base < NT ? a.M - m_base : NT;
       const int b = seg & 1;
+      // the hand-off of the CTA's last tile goes into the timeline
+      unsigned long long* const trec = rec && iend == NU && et2 == 0 ? rec : nullptr;
+      if (CL) {
+        // the epilogue's global inputs of this rank's tokens (and their per-token data), into
+        // shared memory while the tile accumulates
+        const int sl = ((mtot + CS - 1) / CS + 3) / 4 * 4;
+        const int c0 = rank * sl, c1 = c0 + sl < mtot ? c0 + sl : mtot;
+        if (c0 < c1) {
+          for (int c = et2; c < c1 - c0; c += EPT) token_data(a.epi, m_base + c0 + c, esm->rstd[c], esm->pos[c], esm->kv[c]);
+          sync();  // the positions feed the staged RoPE rows
+          stage_epilogue_inputs(a, nt, m_base + c0, c1 - c0, Es, *esm, nullptr, et2, EPT);
+        }
+      }
       // one thread waits and broadcasts, so all threads agree on the outcome
       if (et2 == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
       sync();
@@ -372,97 +469,218 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       sync();
       if (!ok) break;
       tc_fence_after();
-      const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
-      const bool alone = cf == cl;
-      const int m_base = mt * NT;
-      const int mtot = a.M - m_base < NT ? a.M - m_base : NT;
-      const int slot = static_cast<int>(t) == slot0_tile ? 0 : 1;
-      // partial tiles are column-major ([token][tile row]) so that a warp's
-      // stores and the reducer's loads are 128-byte coalesced
-      float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
-      for (int ch = 0; ch * 32 < mtot; ++ch) {
-        float v[32];
+      trace_mark(trec, 7);
+      if constexpr (CL) {
+        // ---- cluster split, reduce-scatter: every rank leaves its partial in its own shared
+        // memory; rank r then sums tokens [c0, c1) of the tile (a 1/CS share, 4-aligned)
+        // from every rank's partial over DSMEM, in rank order, and runs their epilogue
+        const long long j = t - W.t0;  // tile index within the cluster
+        if (j >= 1) {  // every rank has read this CTA's partial of the previous tile
+          if (et2 == 0) *s_flag = mbar_wait_cluster(xr_free, static_cast<uint32_t>((j - 1) & 1), abort_flag, kWaitNs);
+          sync();
+          const bool okf = *s_flag != 0;
+          sync();
+          if (!okf) break;
+        }
         if (grpA) {
-          tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
-          if (FUSE) {  // the lo plane's products
-            float w[32];
-            tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += w[i];
-          }
-        }
-        if (alone) {
-          if (grpA) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) Ys[et * kYsLd + i] = v[i];
-          }
-          sync();
-          epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2, EPT,
-                        *esm, td, sync);
-          sync();
-        } else if (grpA) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) __stcg(mine + (ch * 32 + i) * kGemmBN, v[i]);
-        }
-      }
-      if (grpA) {
-        tc_fence_before();
-        mbar_arrive(acc_empty + b);
-      }
-      if (!alone) {
-        epilogue_prefetch(a, nt, m_base, mtot < 32 ? mtot : 32, et, td);
-        __threadfence();
-        sync();
-        if (et2 == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
-        sync();
-        const bool last = *s_flag != 0;
-        sync();
-        if (last) {
-          __threadfence();
-          // the contributors' slots, in CTA order (a fixed summation order): a
-          // tile is the first tile (slot 0) of every contributor after cf, and of
-          // cf when cf's range starts at the tile's first unit
-          const int ncon = cl - cf + 1;
-          const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
-          constexpr int RW = 32 / (EPT / 128);  // columns of a chunk each warpgroup sums
-          const int col0 = grpA ? 0 : RW;
-          constexpr int NB = W12 ? 1 : 4;  // contributors whose loads are in flight together
           for (int ch = 0; ch * 32 < mtot; ++ch) {
-            float s[RW];
+            float v[32];
+            tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
+            if (FUSE) {  // the lo plane's products
+              float w[32];
+              tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
 #pragma unroll
-            for (int i = 0; i < RW; ++i) s[i] = 0.f;
-            for (int j0 = 0; j0 < ncon; j0 += NB) {
-              float v[NB][RW];
-#pragma unroll
-              for (int jj = 0; jj < NB; ++jj) {
-                const int j = j0 + jj;
-                if (j < ncon) {
-                  const int sl = j == 0 ? sl_first : 0;
-                  const float* src = a.partials + (static_cast<size_t>(cf + j) * 2 + sl) * kGemmBN * NT + et;
-#pragma unroll
-                  for (int i = 0; i < RW; ++i) v[jj][i] = __ldcg(src + (ch * 32 + col0 + i) * kGemmBN);
-                }
-              }
-              // summed in CTA order, whatever the loads' completion order
-#pragma unroll
-              for (int jj = 0; jj < NB; ++jj)
-                if (j0 + jj < ncon) {
-#pragma unroll
-                  for (int i = 0; i < RW; ++i) s[i] += v[jj][i];
-                }
+              for (int k = 0; k < 32; ++k) v[k] += w[k];
             }
+            float4* xr = reinterpret_cast<float4*>(Xp + et * XLD + ch * 32);
 #pragma unroll
-            for (int i = 0; i < RW; ++i) Ys[et * kYsLd + col0 + i] = s[i];
+            for (int k = 0; k < 8; ++k) xr[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          }
+          tc_fence_before();
+          mbar_arrive(acc_empty + b);
+        }
+        trace_mark(trec, 12);
+        sync();
+        if (et2 == 0) {  // this rank's partial is in place: tell every rank
+          fence_acq_rel_cluster();
+          for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_full), static_cast<uint32_t>(r)));
+        }
+        trace_mark(trec, 8);
+        if (et2 == 0) *s_flag = mbar_wait_cluster(xr_full, static_cast<uint32_t>(j & 1), abort_flag, kWaitNs);
+        sync();
+        const bool okr = *s_flag != 0;
+        sync();
+        if (!okr) break;
+        trace_mark(trec, 9);
+        const int sl = ((mtot + CS - 1) / CS + 3) / 4 * 4;
+        const int c0 = rank * sl, c1 = c0 + sl < mtot ? c0 + sl : mtot;
+        // thread (row et, sub) sums the 4-column groups sub, sub + NSUBT, .. of [c0, c1),
+        // one chunk of 32 tokens at a time, with the loads of up to NR ranks in flight
+        constexpr int NSUBT = EPT / 128, GPT = 8 / NSUBT;  // column groups of a chunk per thread
+        constexpr int NR = W12 ? 1 : 4;
+        const int sub = et2 >> 7;
+        const uint32_t xb = smem_u32(Xp);
+        for (int cc = c0; cc < c1; cc += 32) {  // one pass: the slice is at most 32 columns
+          const int ncol = c1 - cc < 32 ? c1 - cc : 32;
+          float s[GPT][4];
+#pragma unroll
+          for (int g = 0; g < GPT; ++g)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s[g][k] = 0.f;
+          for (int r0 = 0; r0 < CS; r0 += NR) {
+            float4 v[NR][GPT];
+#pragma unroll
+            for (int rr = 0; rr < NR; ++rr)
+#pragma unroll
+              for (int g = 0; g < GPT; ++g) {
+                const int col = (sub + g * NSUBT) * 4;
+                if (r0 + rr < CS && col < ncol)
+                  v[rr][g] = ld_dsmem_f32x4(mapa_shared(xb, static_cast<uint32_t>(r0 + rr)) +
+                                            4u * (et * XLD + cc + col));
+              }
+#pragma unroll
+            for (int rr = 0; rr < NR; ++rr)
+#pragma unroll
+              for (int g = 0; g < GPT; ++g)
+                if (r0 + rr < CS && (sub + g * NSUBT) * 4 < ncol) {
+                  s[g][0] += v[rr][g].x;
+                  s[g][1] += v[rr][g].y;
+                  s[g][2] += v[rr][g].z;
+                  s[g][3] += v[rr][g].w;
+                }
+          }
+#pragma unroll
+          for (int g = 0; g < GPT; ++g) {
+            const int col = (sub + g * NSUBT) * 4;
+            if (col < ncol)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) Ys[et * YLD + col + k] = s[g][k];
+          }
+          trace_mark(trec, 13);
+          sync();
+          if (cc + 32 >= c1 && et2 == 0) {
+            // this rank has read every rank's partial of the tile (all loads completed
+            // before the barrier above): release them
+            for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_free), static_cast<uint32_t>(r)));
+          }
+          trace_mark(trec, 10);
+          epilogue_tile(a, nt, Ys, YLD, m_base + cc, ncol, et2, EPT, *esm, nullptr, sync, Es, true);
+          sync();
+          trace_mark(trec, 11);
+        }
+        if (c0 >= c1 && et2 == 0) {  // no tokens for this rank: it read nothing
+          for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_free), static_cast<uint32_t>(r)));
+        }
+      } else {
+        // ---- stream-K: partials through global memory, the last arriver sums them
+        const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
+        const bool alone = cf == cl;
+        const int slot = t == slot0_tile ? 0 : 1;
+        // partial tiles are column-major ([token][tile row]) so that a warp's
+        // stores and the reducer's loads are 128-byte coalesced
+        float* mine = a.partials + (static_cast<size_t>(c) * 2 + slot) * kGemmBN * NT + et;
+        for (int ch = 0; ch * 32 < mtot; ++ch) {
+          float v[32];
+          if (grpA) {
+            tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
+            if (FUSE) {  // the lo plane's products
+              float w[32];
+              tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] += w[k];
+            }
+          }
+          if (alone) {
+            if (grpA) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) Ys[et * kYsLd + k] = v[k];
+            }
             sync();
             epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2, EPT,
-                          *esm, td, sync);
+                          *esm, td, sync, nullptr);
             sync();
+            trace_mark(trec, 11);
+          } else if (grpA) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) __stcg(mine + (ch * 32 + k) * kGemmBN, v[k]);
           }
-          if (et2 == 0) a.counters[t] = 0u;
+        }
+        if (grpA) {
+          tc_fence_before();
+          mbar_arrive(acc_empty + b);
+        }
+        if (!alone) {
+          epilogue_prefetch(a, nt, m_base, mtot < 32 ? mtot : 32, et, td);
+          __threadfence();
+          sync();
+          trace_mark(trec, 8);
+          if (et2 == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
+          sync();
+          const bool last = *s_flag != 0;
+          trace_mark(trec, 9);
+          sync();
+          if (last) {
+            __threadfence();
+            // the contributors' slots, in CTA order (a fixed summation order): a
+            // tile is the first tile (slot 0) of every contributor after cf, and of
+            // cf when cf's range starts at the tile's first unit
+            const int ncon = cl - cf + 1;
+            const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
+            constexpr int RW = 32 / (EPT / 128);  // columns of a chunk each warpgroup sums
+            const int col0 = grpA ? 0 : RW;
+            constexpr int NB = W12 ? 1 : 4;  // contributors whose loads are in flight together
+            for (int ch = 0; ch * 32 < mtot; ++ch) {
+              float s[RW];
+#pragma unroll
+              for (int k = 0; k < RW; ++k) s[k] = 0.f;
+              for (int j0 = 0; j0 < ncon; j0 += NB) {
+                float v[NB][RW];
+#pragma unroll
+                for (int jj = 0; jj < NB; ++jj) {
+                  const int j = j0 + jj;
+                  if (j < ncon) {
+                    const int sl = j == 0 ? sl_first : 0;
+                    const float* src = a.partials + (static_cast<size_t>(cf + j) * 2 + sl) * kGemmBN * NT + et;
+#pragma unroll
+                    for (int k = 0; k < RW; ++k) v[jj][k] = __ldcg(src + (ch * 32 + col0 + k) * kGemmBN);
+                  }
+                }
+                // summed in CTA order, whatever the loads' completion order
+#pragma unroll
+                for (int jj = 0; jj < NB; ++jj)
+                  if (j0 + jj < ncon) {
+#pragma unroll
+                    for (int k = 0; k < RW; ++k) s[k] += v[jj][k];
+                  }
+              }
+#pragma unroll
+              for (int k = 0; k < RW; ++k) Ys[et * kYsLd + col0 + k] = s[k];
+              sync();
+              trace_mark(trec, 10);
+              epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2,
+                            EPT, *esm, td, sync, nullptr);
+              sync();
+              trace_mark(trec, 11);
+            }
+            if (et2 == 0) a.counters[t] = 0u;
+          }
         }
       }
       ++seg;
-      u = uend;
+      i = iend;
+    }
+    if (CL && NU > 0) {
+      // This CTA may leave once every rank has read its partial of the last tile
+      // (xr_free); every rank's arrival for that tile came before this CTA's own
+      // xr_full wait. After a normal run this has happened already; after a
+      // timed-out wait it is awaited, bounded.
+      if (et2 == 0) {
+        volatile int never = 0;
+        const long long ntc = NU / W.nk;
+        mbar_wait_cluster(xr_free, static_cast<uint32_t>((ntc - 1) & 1), &never, kWaitNs);
+        mbar_wait_cluster(xr_full, static_cast<uint32_t>((ntc - 1) & 1), &never, kWaitNs);
+      }
+      sync();
     }
     if (et2 == 0) trace_mark(rec, 5);
   }
@@ -479,43 +697,72 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   }
 }
 
-template <int NT, bool PAIR, bool W12>
+template <int NT, bool PAIR, bool W12, bool CL>
 cudaError_t gemm_tc_launch(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s) {
   constexpr int KS = tc_ks_for(NT, PAIR, W12);
-  const size_t smem = tc_smem_bytes(NT, PAIR, KS, a.tc_stages, W12);
+  const size_t smem = tc_smem_bytes(NT, PAIR, KS, a.tc_stages, W12, CL ? a.cl_size : 0);
   static bool attr_set[64] = {};  // per device: allow the largest configuration this kernel may use
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, W12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBudget + 2048);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, W12, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_k(gemm_tc_kernel<NT, PAIR, W12>, dim3(a.grid_p), dim3(W12 ? kTcThreadsW12 : kTcThreads), smem, s,
+  if (CL) {
+    if (a.cl_size < 1 || a.grid_p % a.cl_size) return cudaErrorInvalidValue;
+    return launch_k_cluster(gemm_tc_kernel<NT, PAIR, W12, CL>, dim3(a.grid_p), dim3(W12 ? kTcThreadsW12 : kTcThreads),
+                            smem, s, a.pdl != 0, a.cl_size, w, x, a);
+  }
+  return launch_k(gemm_tc_kernel<NT, PAIR, W12, CL>, dim3(a.grid_p), dim3(W12 ? kTcThreadsW12 : kTcThreads), smem, s,
                   a.pdl != 0, w, x, a);
+}
+
+// Clusters of `cs` CTAs of this instantiation that can be resident at once (0 on error).
+template <int NT, bool PAIR, bool W12, bool CL>
+int gemm_tc_max_clusters(int cs, int stages) {
+  constexpr int KS = tc_ks_for(NT, PAIR, W12);
+  const size_t smem = tc_smem_bytes(NT, PAIR, KS, stages, W12, CL ? cs : 0);
+  if (cudaFuncSetAttribute(gemm_tc_kernel<NT, PAIR, W12, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBudget + 2048) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(W12 ? kTcThreadsW12 : kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<NT, PAIR, W12, CL>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace tcg
 }  // namespace sv
 
 // Explicit instantiations for token tile NT (one translation unit per NT, so
-// the kernel variants compile in parallel). W12 tiles stop at kW12MaxNT.
-#define SV_GEMM_TC_INSTANTIATE(NT)                                                                               \
-  namespace sv {                                                                                                 \
-  namespace tcg {                                                                                                \
-  template cudaError_t gemm_tc_launch<NT, true, false>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&,  \
-                                                       cudaStream_t);                                            \
-  template cudaError_t gemm_tc_launch<NT, false, false>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, \
-                                                        cudaStream_t);                                           \
-  }                                                                                                              \
-  }
-#define SV_GEMM_TC_INSTANTIATE_W12(NT)                                                                          \
-  namespace sv {                                                                                                \
-  namespace tcg {                                                                                               \
-  template cudaError_t gemm_tc_launch<NT, true, true>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&,  \
-                                                      cudaStream_t);                                            \
-  template cudaError_t gemm_tc_launch<NT, false, true>(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, \
-                                                       cudaStream_t);                                           \
-  }                                                                                                             \
-  }
+// the kernel variants compile in parallel). W12 and the cluster split stop at
+// 64 columns.
+#define SV_GEMM_TC_INSTANTIATE_ONE(NT, PAIR, W12, CL)                                                            \
+  template cudaError_t sv::tcg::gemm_tc_launch<NT, PAIR, W12, CL>(const sv::GemmArgs&, const CUtensorMap&,       \
+                                                                  const CUtensorMap&, cudaStream_t);             \
+  template int sv::tcg::gemm_tc_max_clusters<NT, PAIR, W12, CL>(int, int);
+#define SV_GEMM_TC_INSTANTIATE(NT)                \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, true, false, false) \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, false, false, false)
+#define SV_GEMM_TC_INSTANTIATE_SMALL(NT)             \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, true, true, false)  \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, false, true, false) \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, true, false, true)  \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, false, false, true) \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, true, true, true)   \
+  SV_GEMM_TC_INSTANTIATE_ONE(NT, false, true, true)

@@ -2,4 +2,4 @@
 #include "gemm_tc.cuh"
 
 SV_GEMM_TC_INSTANTIATE(32)
-SV_GEMM_TC_INSTANTIATE_W12(32)
+SV_GEMM_TC_INSTANTIATE_SMALL(32)

@@ -21,6 +21,8 @@ constexpr int kSmemBudget = 225 * 1024;
 constexpr int kW12Planes = 3 * 2 * 4096;        // one W12 unit: 3 planes x 2 row halves x 4 KB
 constexpr int kW12Ring = 2;                     // rebuilt W12 weight tiles in flight
 constexpr int kW12MaxNT = 64;                   // widest token tile of the W12 variant
+constexpr int kClusterMaxNT = 64;               // widest token tile of the cluster split
+constexpr int kClusterMaxSize = 8;              // CTAs per cluster (the portable maximum)
 
 // One pipeline stage covers ks K-elements (ks / 64 swizzled sub-tiles of 64).
 // bf16 weights: per sub-tile the weight tile, then the x tile(s). W12 weights
@@ -30,17 +32,27 @@ constexpr int stage_bytes(int nt, bool pair, int ks, bool w12) {
   return w12 ? kW12Planes + (ks / 64) * nt * 128 * (pair ? 2 : 1) : (ks / 64) * (kABytes + nt * 128 * (pair ? 2 : 1));
 }
 
-constexpr size_t tc_smem_bytes(int nt, bool pair, int ks, int stages, bool w12) {
+// Token columns each rank of a cluster of cs CTAs reduces and finishes (a
+// multiple of 4, so the slice reads are 16-byte vectors).
+constexpr int cl_slice(int nt, int cs) { return ((nt + cs - 1) / cs + 3) / 4 * 4; }
+
+// cs > 0: the cluster split, whose epilogue works on a slice of the tokens: its
+// tile values Ys [128][slice + 1], its staged inputs Es [128][slice] and this
+// CTA's partial tile Xp [128][nt + 4] replace the stream-K Ys [128][33] and
+// the launch's per-token data.
+constexpr size_t tc_smem_bytes(int nt, bool pair, int ks, int stages, bool w12, int cs = 0) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair, ks, w12) +
-         (w12 ? static_cast<size_t>(kW12Ring) * (ks / 64) * kABytes : 0) + sizeof(float) * kGemmBN * kYsLd +
-         sizeof(EpiSmem) + sizeof(TokData) + sizeof(uint64_t) * (2 * stages + 9) + 16;
+         (w12 ? static_cast<size_t>(kW12Ring) * (ks / 64) * kABytes : 0) +
+         (cs > 0 ? sizeof(float) * kGemmBN * (cl_slice(nt, cs) + 1 + cl_slice(nt, cs) + nt + 4)
+                 : sizeof(float) * kGemmBN * kYsLd + sizeof(TokData)) +
+         sizeof(EpiSmem) + sizeof(uint64_t) * (2 * stages + 11) + 16;
 }
 
-constexpr int tc_stages_for(int nt, bool pair, int ks, bool w12) {
-  return (kSmemBudget - static_cast<int>(tc_smem_bytes(nt, pair, ks, 0, w12) + 16 * sizeof(uint64_t))) /
+constexpr int tc_stages_for(int nt, bool pair, int ks, bool w12, int cs = 0) {
+  return (kSmemBudget - static_cast<int>(tc_smem_bytes(nt, pair, ks, 0, w12, cs) + 16 * sizeof(uint64_t))) /
                      stage_bytes(nt, pair, ks, w12) > 8
              ? 8
-             : (kSmemBudget - static_cast<int>(tc_smem_bytes(nt, pair, ks, 0, w12) + 16 * sizeof(uint64_t))) /
+             : (kSmemBudget - static_cast<int>(tc_smem_bytes(nt, pair, ks, 0, w12, cs) + 16 * sizeof(uint64_t))) /
                    stage_bytes(nt, pair, ks, w12);
 }
 
@@ -53,9 +65,13 @@ constexpr int tc_ks_for(int nt, bool pair, bool w12) {
                                                         : 64;
 }
 
-// Launch of the kernel instantiation for token tile NT (gemm_tc_nt*.cu).
-template <int NT, bool PAIR, bool W12>
+// Launch of the kernel instantiation for token tile NT (gemm_tc_nt*.cu); CL:
+// the cluster split (a.cl_size CTAs per cluster, a.cl_tiles tiles each).
+template <int NT, bool PAIR, bool W12, bool CL>
 cudaError_t gemm_tc_launch(const GemmArgs& a, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t s);
+// Clusters of cs CTAs of that instantiation (with `stages` pipeline stages) that fit on the device at once.
+template <int NT, bool PAIR, bool W12, bool CL>
+int gemm_tc_max_clusters(int cs, int stages);
 
 }  // namespace tcg
 }  // namespace sv

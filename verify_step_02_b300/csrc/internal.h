@@ -11,12 +11,23 @@
 namespace sv {
 
 constexpr int kMaxBatch = 1024;       // largest batch a verify may take
+constexpr int kMaxGamma = 255;        // largest block beyond the anchor (drafts, or prefill rows)
 constexpr int kGemmBN = 128;          // weight rows per GEMM tile (both GEMM paths)
 constexpr int kFmaBM = 32;            // tokens per FMA GEMM tile
 constexpr int kFmaKC = 32;            // K step of the FMA GEMM
 
 // Device status word bits (sv_model_sync_status).
-enum : uint32_t { kStBadToken = 1u, kStBadPage = 2u, kStBadDraftProb = 4u, kStTimeout = 8u, kStBadPos = 16u };
+// kStBadPos and kStNoPage mean the block does not fit the request's KV capacity
+// (a position reaches max_seq_len, or a page index is past the page table);
+// the others are bad inputs or a timed-out wait.
+enum : uint32_t {
+  kStBadToken = 1u,
+  kStBadPage = 2u,
+  kStBadDraftProb = 4u,
+  kStTimeout = 8u,
+  kStBadPos = 16u,
+  kStNoPage = 32u,
+};
 
 enum EpiKind : int {
   kEpiStore = 0,   // y[m][n] = value                                  (sv_linear)
@@ -98,6 +109,7 @@ struct EpiSmem {
   long long kv[32];        // page-pool row of the token's slot for kv head 0, or -1
   float red[4][32];
   int redi[4][32];
+  float gain[kGemmBN];     // the tile rows' next-norm gain, when staged (stage_epilogue_inputs)
 };
 
 // Per-token epilogue data of a whole launch (block rows m < 256), computed once
@@ -109,33 +121,16 @@ struct TokData {
   long long kv[kTokMax];
 };
 
-// A window of a later matrix product's weights to bring into L2 while the
-// current kernel leaves HBM idle (its own loads are all issued; its tail, the
-// next launch's start and the dependency waits follow). It names the target
-// product's work split, so CTA c of the current kernel requests the units
-// [u0 + first, u0 + first + count) of the target's CTAs c, c + grid, ...,
-// which the target then reads from L2 instead of HBM.
-struct L2Window {
-  const void* w;           // target weights (nullptr: no window)
-  int wdtype;              // SV_BF16 or SV_W12
-  int K;
-  int n_rows;
-  int pair;                // PairKind of the target
-  int ffn;
-  int kb, ks, m_tiles;     // the target's K blocks per tile, K step, token tiles
-  long long U;             // the target's units (tiles x K blocks)
-  int grid_p;              // the target's CTAs
-  int w12_kt;
-  long long w12_plane;
-  int first, count;        // units of each target CTA's range
-};
-
 // Per-CTA timeline (sv_model_set_trace): a traced launch writes one record of
 // kTraceWords 64-bit words per CTA; word 0 = kind << 48 | smid << 32 | CTA,
 // words 1-6 = %globaltimer (ns) at the kernel's milestones (0 = not reached):
 // 1 start, 2 dependency wait returned, 3 first operands landed, 4 last MMA
-// issued, 5 epilogue done, 6 exit.
-constexpr int kTraceWords = 8;
+// issued, 5 epilogue done, 6 exit. The projection kernels add the steps of
+// their last tile's hand-off: 7 accumulator ready for the epilogue, 8 partial
+// tile stored and signalled, 9 arrival counted (stream-K) or every rank's
+// partial in place (cluster split, the tile's owner), 10 the partials summed
+// (last arriver or owner), 11 tile epilogue done.
+constexpr int kTraceWords = 16;
 enum TraceKind : int { kTrGemm = 1, kTrAttn = 2, kTrMerge = 3, kTrPrep = 4, kTrAccept = 5, kTrGemmFma = 6 };
 
 struct GemmArgs {
@@ -166,7 +161,8 @@ struct GemmArgs {
   int tc_stages;           // shared-memory pipeline depth
   int x_lo_row;            // row of the lo plane's first row in the x tensor map (kXPair)
   int pdl;                 // launched as a programmatic dependent of the previous kernel
-  L2Window pf;             // a later product's weights to request into L2 (tensor path)
+  int cl_size;             // tensor path, cluster split: CTAs per cluster (0: stream-K)
+  int cl_tiles;            // tensor path, cluster split: tiles per cluster
   unsigned long long* trace;  // this launch's per-CTA records, or nullptr
   Epi epi;
 };
@@ -188,17 +184,17 @@ struct AttnArgs {
   int max_chunks;
   int max_rows;            // (max_gamma + 1) * group
   int max_seq_len;         // a request whose block ends past this is skipped (status kStBadPos)
-  float* partials;         // chunk partials (layout per kernel; max_batch*n_kv*max_chunks*max_rows*(head_dim+2) floats)
-  long long ml_offset;     // tensor-core kernel: float offset of the (m, l) pairs after the O partials
+  float* partials;         // CUDA-core kernel: chunk partials (max_batch*n_kv*max_chunks*max_rows*(head_dim+2) floats)
   int q_lo_row;            // tensor-core kernel: first token row of q's lo plane in the q tensor map
   unsigned* counters;      // [B*n_kv]
   unsigned* status;
   int x_pair;
   int kv_bf16;
   int pdl;                 // launched as a programmatic dependent of the previous kernel
-  L2Window pf;             // the next product's weights to request into L2 once the K/V loads are issued
+  int cl_size;             // tensor-core kernel: CTAs per (request, kv head, row tile), one cluster
+  int q_rows;              // tensor-core kernel: block rows per row tile (q_rows * group <= 128)
+  int n_row_tiles;         // tensor-core kernel: row tiles per request (ceil((max_gamma + 1) / q_rows))
   unsigned long long* trace;  // per-CTA records of the attention launch, or nullptr
-  unsigned long long* trace_merge;  // per-CTA records of the merge launch, or nullptr
 };
 
 struct AcceptArgs {
@@ -220,6 +216,7 @@ struct AcceptArgs {
   int* next_token;
   unsigned* status;
   int pdl;
+  int commit_all;          // prefill: every row is committed and next_token = argmax of the last row
 };
 
 struct PrepParams {
@@ -252,6 +249,27 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// launch_k with thread-block clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---- launchers (defined in the .cu files) ----
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // Tensor path (tcgen05, gemm_tc.cu) for bf16 weights with bf16 or hi/lo-pair x.
@@ -270,7 +288,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtens
 // pages and at most 128 query rows per (request, kv head); KV maps: a layer's
 // pool as bf16 [n_pages * n_kv * 16][head_dim], 64 x 16 boxes.
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len);
-int attention_tc_chunk(int batch, int n_kv_heads, int max_seq_len, int sm_count);
+// CTAs per (request, kv head, row tile) for `items` of them (a power of two, 1 .. 16).
+int attention_tc_cluster(long long items, int head_dim, int sm_count);
 cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
 // q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
 cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
   __shared__ float red[32];
   __shared__ float seg_pref[kAccThreads];
   __shared__ int s_pick[2];
-  __shared__ int s_targ[64];
+  __shared__ int s_targ[kMaxGamma + 1];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();
@@ -147,7 +147,10 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
       if (lane == 0) s_targ[j] = bi;
     }
     __syncthreads();
-    while (k < L && toks[1 + k] == s_targ[k]) ++k;
+    if (a.commit_all)
+      k = L;  // prefill: the block is the prompt itself
+    else
+      while (k < L && toks[1 + k] == s_targ[k]) ++k;
     next = s_targ[k];
   } else {
     const float invT = 1.0f / a.temperature;

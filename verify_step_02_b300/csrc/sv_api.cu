@@ -98,6 +98,7 @@ struct sv_model {
   std::vector<const void*> map_k_ptr, map_v_ptr;
   std::vector<int> map_kv_pages;
   CUtensorMap map_q;
+  int q_rows = 1;  // block rows per attention row tile
   bool last_logits = false;
   int last_m = 0;
   Timing timing;
@@ -143,12 +144,29 @@ sv_status check_config(const sv_config* c) {
     return fail(SV_ERR_UNSUPPORTED, "d_model, ffn and n_heads*head_dim must be multiples of 16");
   if (c->weight_dtype < SV_F32 || c->weight_dtype > SV_W12) return fail(SV_ERR_INVALID_ARG, "bad weight_dtype");
   if (c->max_batch < 1 || c->max_batch > kMaxBatch) return fail(SV_ERR_INVALID_ARG, "max_batch must be 1..%d", kMaxBatch);
-  if (c->max_gamma < 0 || c->max_gamma > 63) return fail(SV_ERR_INVALID_ARG, "max_gamma must be 0..63");
+  if (c->max_gamma < 0 || c->max_gamma > kMaxGamma)
+    return fail(SV_ERR_INVALID_ARG, "max_gamma must be 0..%d", kMaxGamma);
   if (c->page_size < 1 || c->page_size > 256) return fail(SV_ERR_INVALID_ARG, "page_size must be 1..256");
   if (c->max_seq_len < 1 || c->max_seq_len > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "bad max_seq_len");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(SV_ERR_INVALID_ARG, "bad rms_eps or rope_theta");
-  if ((c->n_heads / c->n_kv_heads) * (c->max_gamma + 1) > 256)
-    return fail(SV_ERR_UNSUPPORTED, "(n_heads / n_kv_heads) * (max_gamma + 1) must be <= 256");
+  // float32 models run the CUDA-core attention, which holds a request's rows in shared memory
+  if (c->weight_dtype == SV_F32 &&
+      2LL * (c->n_heads / c->n_kv_heads) * (c->max_gamma + 1) * c->head_dim * 4 > 160 * 1024)
+    return fail(SV_ERR_UNSUPPORTED,
+                "float32 models: 2 * (n_heads / n_kv_heads) * (max_gamma + 1) * head_dim * 4 must be <= 160 KiB");
+  return SV_OK;
+}
+
+// Sampled acceptance divides the logits by T in float32: below kMinTemperature
+// z / T can overflow (and 1 / T does for T < ~3e-39), which would make every
+// probability NaN, so such temperatures are refused (T = 0 is greedy).
+constexpr float kMinTemperature = 1e-6f;
+
+sv_status check_temperature(float T) {
+  if (!(T >= 0.f) || std::isinf(T)) return fail(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (T > 0.f && T < kMinTemperature)
+    return fail(SV_ERR_INVALID_ARG, "temperature %g is below the smallest sampled temperature %g (use 0 for greedy)",
+                T, kMinTemperature);
   return SV_OK;
 }
 
@@ -197,66 +215,6 @@ unsigned long long* trace_slot(sv_model* m, long long ctas, int kind) {
   m->trace_launches.push_back(kind);
   m->trace_used += ctas;
   return p;
-}
-
-// Bytes of the next products' weights each kernel requests into L2 once its
-// own loads are issued (well inside the 126 MB L2, beside the streamed
-// weights, the KV and the activations).
-constexpr long long kPrefetchBytes = 32ll << 20;
-
-// A projection's tensor-core plan at block size M (tc false: the CUDA-core
-// path runs it, and nothing is prefetched for it).
-struct ProjPlan {
-  GemmArgs a;
-  bool tc = false;
-  long long unit_bytes = 0;  // weight bytes of one work unit
-  long long per_cta = 0;     // most units any CTA takes
-};
-
-ProjPlan plan_projection(const sv_model* m, int M, int n_units, int K, int pair, int ffn) {
-  ProjPlan p;
-  memset(&p.a, 0, sizeof p.a);
-  p.a.wdtype = m->cfg.weight_dtype;
-  p.a.x_kind = m->x_pair ? kXPair : kXF32;
-  p.a.ffn = ffn;
-  p.a.n_rows = pair == kPairSwiglu ? 2 * ffn : n_units;
-  if (!m->use_tc || !gemm_tc_supported(p.a.wdtype, pair, ffn)) return p;
-  plan_gemm_tc(p.a, M, n_units, K, pair, m->sm_count);
-  p.tc = p.a.tc_stages >= 2;
-  if (p.tc) {
-    const long long U = (long long)p.a.n_tiles * p.a.m_tiles * p.a.kb;
-    p.per_cta = (U + p.a.grid_p - 1) / p.a.grid_p;
-    p.unit_bytes = p.a.wdtype == SV_W12 ? 6LL * 4096 : (long long)kGemmBN * p.a.tc_ks * 2;
-  }
-  return p;
-}
-
-// Units [first, first + count) of every CTA range of projection `t` (weights
-// `w`), count bounded by `bytes`; *cursor advances past them.
-L2Window l2_window(const ProjPlan& t, const sv_matrix& w, int K, long long* cursor, long long bytes) {
-  L2Window pf;
-  memset(&pf, 0, sizeof pf);
-  if (!t.tc || *cursor >= t.per_cta) return pf;
-  long long n = bytes / ((long long)t.a.grid_p * t.unit_bytes);
-  if (n > t.per_cta - *cursor) n = t.per_cta - *cursor;
-  if (n <= 0) return pf;
-  pf.w = w.data;
-  pf.wdtype = t.a.wdtype;
-  pf.K = K;
-  pf.n_rows = t.a.n_rows;
-  pf.pair = t.a.pair;
-  pf.ffn = t.a.ffn;
-  pf.kb = t.a.kb;
-  pf.ks = t.a.tc_ks;
-  pf.m_tiles = t.a.m_tiles;
-  pf.U = (long long)t.a.n_tiles * t.a.m_tiles * t.a.kb;
-  pf.grid_p = t.a.grid_p;
-  pf.w12_kt = (K + 127) / 128;
-  pf.w12_plane = w12_plane_bytes(t.a.n_rows, K);
-  pf.first = static_cast<int>(*cursor);
-  pf.count = static_cast<int>(n);
-  *cursor += n;
-  return pf;
 }
 
 // ------------------------------------------------------------------ GEMM helpers
@@ -312,8 +270,7 @@ void gemm_tc_ws_need(int sm, int m_max, int n_units, int K, int pair, size_t* pa
 
 // wmap / xmap: the tensor maps of the weight and the x tensor (tensor path only).
 sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair, int kc, cudaStream_t s,
-                   const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr,
-                   const L2Window* pf = nullptr) {
+                   const char* what, const CUtensorMap* wmap = nullptr, const CUtensorMap* xmap = nullptr) {
   Timed t(m, kc, s);
   bool tc = m->use_tc && gemm_tc_supported(a.wdtype, pair, a.ffn);
   if (tc) {
@@ -322,7 +279,6 @@ sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair
   }
   if (tc) {
     a.x_lo_row = m->m_max;
-    if (pf) a.pf = *pf;
     a.trace = trace_slot(m, a.grid_p, kTrGemm);
     SV_CUDA(launch_gemm_tc(a, *wmap, *xmap, s), what);
   } else {
@@ -334,17 +290,18 @@ sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair
 
 sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, const sv_kv* kv, const float* probs,
                      float T, uint64_t seed, const long long* req_ids, int* acc_len, int* next_tok,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool commit_all = false) {
   const sv_config& c = m->cfg;
   if (B < 1 || B > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", B, c.max_batch);
   if (!tokens || !lens || !kv || !acc_len || !next_tok) return fail(SV_ERR_INVALID_ARG, "NULL argument");
   if (!kv->k || !kv->v || !kv->page_table || !kv->seq_len || kv->n_pages < 1 || kv->max_pages_per_seq < 1)
     return fail(SV_ERR_INVALID_ARG, "incomplete sv_kv");
-  if (!(T >= 0.f) || std::isinf(T)) return fail(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (sv_status st = check_temperature(T)) return st;
   if (T > 0.f && !probs) return fail(SV_ERR_INVALID_ARG, "draft_probs required when temperature > 0");
   for (int l = 0; l < c.n_layers; ++l)
     if (!kv->k[l] || !kv->v[l]) return fail(SV_ERR_INVALID_ARG, "NULL KV pool for layer %d", l);
   static thread_local PrepParams p;
+  int max_block = 1;  // the longest block (rows) of this call
   p.B = B;
   p.pdl = m->use_pdl;
   p.gamma_stride = c.max_gamma + 1;
@@ -353,22 +310,12 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     if (lens[r] < 0 || lens[r] > c.max_gamma)
       return fail(SV_ERR_INVALID_ARG, "verify_lens[%d] = %d outside 0..%d", r, lens[r], c.max_gamma);
     p.req_row0[r + 1] = p.req_row0[r] + lens[r] + 1;
+    max_block = std::max(max_block, lens[r] + 1);
   }
   const int M = p.req_row0[B];
   p.M = M;
   const int d = c.d_model, hd = c.head_dim, nq = c.n_heads * hd, N3 = nqkv(c);
   const bool keep = T > 0.f || (c.flags & SV_FLAG_KEEP_LOGITS);
-  // Every projection's plan at this M; each kernel then requests a window of
-  // the next product's weights into L2 (each window continues where the
-  // previous one for that product stopped, past the stages the product
-  // itself requests before its dependency wait).
-  const ProjPlan pl_qkv = plan_projection(m, M, N3, d, kPairNone, 0);
-  const ProjPlan pl_o = plan_projection(m, M, d, nq, kPairNone, 0);
-  const ProjPlan pl_gu = plan_projection(m, M, c.ffn, d, kPairSwiglu, c.ffn);
-  const ProjPlan pl_d = plan_projection(m, M, d, c.ffn, kPairNone, 0);
-  const ProjPlan pl_lm = plan_projection(m, M, c.vocab, d, kPairNone, 0);
-  auto first_units = [](const ProjPlan& t) { return (long long)(t.tc ? t.a.tc_stages : 0); };
-
   {
     Timed t(m, SV_KC_NORM, s);
     SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, m->req_row0, m->w.embed,
@@ -378,16 +325,6 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const sv_layer_weights& L = m->layers[l];
-    long long cur_o = first_units(pl_o), cur_gu = first_units(pl_gu), cur_d = first_units(pl_d);
-    const bool last = l + 1 == c.n_layers;
-    const ProjPlan& pl_next = last ? pl_lm : pl_qkv;
-    const sv_matrix& w_next = last ? m->w.lm_head : m->layers[l + 1].wqkv;
-    long long cur_next = first_units(pl_next);
-    const L2Window pf_qkv = l2_window(pl_o, L.wo, nq, &cur_o, kPrefetchBytes);
-    const L2Window pf_attn = l2_window(pl_gu, L.wgu, d, &cur_gu, kPrefetchBytes);
-    const L2Window pf_o = l2_window(pl_gu, L.wgu, d, &cur_gu, kPrefetchBytes);
-    const L2Window pf_gu = l2_window(pl_d, L.wd, c.ffn, &cur_d, kPrefetchBytes);
-    const L2Window pf_d = l2_window(pl_next, w_next, d, &cur_next, kPrefetchBytes);
     {  // QKV projection, RoPE, q out, k/v into the page slots
       GemmArgs a = gemm_base(m, L.wqkv, N3, d, m->u, m->u_plane);
       a.epi.kind = kEpiQkv;
@@ -411,7 +348,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.page_size = c.page_size;
       a.epi.n_pages = kv->n_pages;
       sv_status st =
-          run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm", &m->map_qkv[l], &m->map_u, &pf_qkv);
+          run_gemm(m, a, M, N3, d, kPairNone, SV_KC_GEMM, s, "qkv gemm", &m->map_qkv[l], &m->map_u);
       if (st) return st;
     }
     {
@@ -447,12 +384,12 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
-        a.chunk = attention_tc_chunk(B, c.n_kv_heads, c.max_seq_len, m->sm_count);
-        a.max_chunks = (c.max_seq_len + a.chunk - 1) / a.chunk;
-        a.ml_offset = (long long)c.max_batch * c.n_kv_heads * a.max_chunks * a.max_rows * hd;
-        a.pf = pf_attn;
-        a.trace = trace_slot(m, (long long)B * c.n_kv_heads * a.max_chunks, kTrAttn);
-        a.trace_merge = trace_slot(m, (long long)B * c.n_kv_heads * ((a.max_rows + 7) / 8), kTrMerge);
+        a.q_rows = m->q_rows;
+        a.max_rows = a.q_rows * (c.n_heads / c.n_kv_heads);
+        a.n_row_tiles = (max_block + a.q_rows - 1) / a.q_rows;
+        const long long items = (long long)B * c.n_kv_heads * a.n_row_tiles;
+        a.cl_size = attention_tc_cluster(items, hd, m->sm_count);
+        a.trace = trace_slot(m, items * a.cl_size, kTrAttn);
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
       } else {
@@ -469,7 +406,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.x_out = m->u;
       a.epi.x_out_plane = m->u_plane;
       a.epi.ss_out = m->ss;
-      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao, &pf_o);
+      sv_status st = run_gemm(m, a, M, d, nq, kPairNone, SV_KC_GEMM, s, "o gemm", &m->map_o[l], &m->map_ao);
       if (st) return st;
     }
     {
@@ -481,7 +418,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.ffn = c.ffn;
       a.epi.ss_in = m->ss;
       sv_status st = run_gemm(m, a, M, c.ffn, d, kPairSwiglu, SV_KC_GEMM, s, "gate/up gemm", &m->map_gu[l],
-                              &m->map_u, &pf_gu);
+                              &m->map_u);
       if (st) return st;
     }
     {
@@ -494,7 +431,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.x_out_plane = m->u_plane;
       a.epi.ss_out = m->ss;
       sv_status st =
-          run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act, &pf_d);
+          run_gemm(m, a, M, d, c.ffn, kPairNone, SV_KC_GEMM, s, "down gemm", &m->map_d[l], &m->map_act);
       if (st) return st;
     }
   }
@@ -529,6 +466,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     a.next_token = next_tok;
     a.status = m->status;
     a.pdl = m->use_pdl;
+    a.commit_all = commit_all ? 1 : 0;
     Timed t(m, SV_KC_ACCEPT, s);
     SV_CUDA(launch_accept(a, s), "accept");
   }
@@ -637,8 +575,10 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
     m->map_k_ptr.assign(c.n_layers, nullptr);
     m->map_v_ptr.assign(c.n_layers, nullptr);
     m->map_kv_pages.assign(c.n_layers, 0);
+    // q of one attention row tile: q_rows block rows x the group's heads <= 128 MMA rows
+    m->q_rows = std::min(c.max_gamma + 1, 128 / (c.n_heads / c.n_kv_heads));
     const cudaError_t qe = tc_encode_q_map(&m->map_q, m->q, M, c.n_heads, c.head_dim, c.n_heads / c.n_kv_heads,
-                                           c.max_gamma + 1);
+                                           m->q_rows);
     if (qe != cudaSuccess) {
       free_all(m);
       delete m;
@@ -696,6 +636,7 @@ void sv_model_destroy(sv_model* model) {
 sv_status sv_verify(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
                     const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
                     const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream) {
+  if (sv_status st = check_temperature(temperature)) return st;
   if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
   return run_verify(model, batch, tokens, verify_lens, kv, draft_probs, temperature, seed,
                     reinterpret_cast<const long long*>(request_ids), accepted_len, next_token,
@@ -705,6 +646,7 @@ sv_status sv_verify(sv_model* model, int32_t batch, const int32_t* tokens, const
 sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* verify_lens,
                          const sv_kv* kv, const float* draft_probs, float temperature, uint64_t seed,
                          const int64_t* request_ids, int32_t* accepted_len, int32_t* next_token, void* stream) {
+  if (sv_status st = check_temperature(temperature)) return st;
   if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
   const sv_config& c = model->cfg;
   if (batch < 1 || batch > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, c.max_batch);
@@ -737,6 +679,14 @@ sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, 
   return SV_OK;
 }
 
+sv_status sv_prefill(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* block_lens,
+                     const sv_kv* kv, int32_t* next_token, void* stream) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  if (!next_token) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  return run_verify(model, batch, tokens, block_lens, kv, nullptr, 0.f, 0, nullptr, model->d_out, next_token,
+                    static_cast<cudaStream_t>(stream), true);
+}
+
 sv_status sv_model_logits(sv_model* model, float* dst, int32_t rows, void* stream) {
   if (!model || !dst) return fail(SV_ERR_INVALID_ARG, "NULL argument");
   if (!model->last_logits) return fail(SV_ERR_INVALID_ARG, "the last verify kept no logits");
@@ -755,10 +705,16 @@ sv_status sv_model_sync_status(sv_model* model, void* stream) {
   SV_CUDA(cudaStreamSynchronize(s), "synchronize");
   SV_CUDA(cudaMemsetAsync(model->status, 0, sizeof(unsigned), s), "clear status");
   SV_CUDA(cudaStreamSynchronize(s), "synchronize");
-  if (word)
-    return fail(SV_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s", (word & kStBadToken) ? " token id out of range" : "",
-                (word & kStBadPage) ? " page id out of range" : "", (word & kStTimeout) ? " wait timed out" : "",
-                (word & kStBadPos) ? " a block position reaches max_seq_len" : "");
+  if (word) {
+    // a block that only overran its KV capacity is SV_ERR_KV_CAPACITY; anything else a failed check
+    const bool capacity_only = (word & ~(kStBadPos | kStNoPage)) == 0;
+    return fail(capacity_only ? SV_ERR_KV_CAPACITY : SV_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s%s%s",
+                (word & kStBadToken) ? " token id out of range" : "", (word & kStBadPage) ? " page id out of range" : "",
+                (word & kStTimeout) ? " wait timed out" : "",
+                (word & kStBadPos) ? " a block position reaches max_seq_len" : "",
+                (word & kStNoPage) ? " a block position is past the request's page table" : "",
+                (word & kStBadDraftProb) ? " bad draft probability" : "");
+  }
   return SV_OK;
 }
 
