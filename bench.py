@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
     ap.add_argument("--sweep-dtype", choices=["bf16", "w12"], default="bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cuda-core-gemm", action="store_true",
+                    help="with --sweep step: run the projections on the CUDA-core (FMA) kernel instead of tcgen05")
     ap.add_argument("--trace", action="store_true",
                     help="after the timed steps, run two traced steps and add a per-kernel timeline summary "
                          "(device %globaltimer per CTA) to the JSON line")
@@ -756,6 +758,7 @@ def run_sweep(args, local):
 
 # ------------------------------------------------------------------ step-cost table
 STEP_SWEEP_M = (1, 2, 4, 8, 16, 17, 24, 32, 48, 64, 96, 128, 192, 256)
+STEP_SWEEP_M_FMA = (1, 2, 4, 8, 16, 17)
 
 
 def run_sweep_step(args, local):
@@ -783,7 +786,8 @@ def run_sweep_step(args, local):
     ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, torch.bfloat16, fill="normal")
     seq = torch.full((max_b,), CONTEXT, dtype=torch.int32, device="cuda")
     kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
-    model = vs.Model(vs.make_config(shape, vs.SV_BF16, max_b, max_g, max_seq, PAGE), wdev)
+    flags = vs.SV_FLAG_CUDA_CORE_GEMM if args.cuda_core_gemm else 0
+    model = vs.Model(vs.make_config(shape, vs.SV_BF16, max_b, max_g, max_seq, PAGE, flags=flags), wdev)
     rng = np.random.default_rng(5)
     tok = torch.from_numpy(rng.integers(0, shape["vocab"], size=(max_b, max_g + 1)).astype(np.int32)).cuda()
     acc = torch.zeros(max_b, dtype=torch.int32, device="cuda")
@@ -792,7 +796,7 @@ def run_sweep_step(args, local):
     peak, peak_kind = measured_peaks()
     per_layer, wbytes, kv_row = step_bytes(shape)
     rows = {}
-    for M in STEP_SWEEP_M:
+    for M in (STEP_SWEEP_M_FMA if args.cuda_core_gemm else STEP_SWEEP_M):
         b = (M + max_g) // (max_g + 1)
         lens = [M // b - 1 + (1 if r < M % b else 0) for r in range(b)]
         for _ in range(args.warmup):
@@ -811,6 +815,7 @@ def run_sweep_step(args, local):
                         "hbm_frac": round(alg / (us * 1e-6) / 1e9 / peak, 4)}
     model.close()
     return {"sweep": "step", "model": "8B-class bf16, 36 layers", "context": CONTEXT, "layers": shape["n_layers"],
+            "gemm": "CUDA-core FMA" if args.cuda_core_gemm else "tcgen05 tensor cores",
             "table": rows, "ar_greedy_tokens_per_s": rows["1"]["steps_per_s"], "peak_gbs": peak,
             "peak_kind": peak_kind,
             "note": "M rows per step (requests of up to 64 rows); M = 1 is autoregressive greedy decoding"}

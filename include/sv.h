@@ -98,6 +98,11 @@ typedef struct {
  * loads) overlaps the end of that kernel. With this flag the step is slower,
  * but per-kernel event timing (sv_model_set_timing) adds up to the step. */
 #define SV_FLAG_NO_PDL 2
+/* Run every matrix product of the step on the CUDA cores (the warp-level FMA
+ * kernel that float32 models use) instead of the tensor cores, for bf16/W12
+ * models too. Same results within the bf16 tolerance; for measuring where
+ * the tensor-core path starts to pay (small M). */
+#define SV_FLAG_CUDA_CORE_GEMM 4
 
 /* A weight matrix [rows][cols] (the output-major layout y = x W^T).
  * F32/BF16: `data` is a dense row-major device array of that type.

@@ -20,7 +20,7 @@ lib = ctypes.CDLL(LIB_PATH)
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_NOT_REPRESENTABLE, SV_ERR_KV_CAPACITY = 0, 1, 2, 3
 SV_ERR_OUT_OF_MEMORY, SV_ERR_CUDA, SV_ERR_DEVICE_CHECK, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
 SV_F32, SV_BF16, SV_W12 = 0, 1, 2
-SV_FLAG_KEEP_LOGITS, SV_FLAG_NO_PDL = 1, 2
+SV_FLAG_KEEP_LOGITS, SV_FLAG_NO_PDL, SV_FLAG_CUDA_CORE_GEMM = 1, 2, 4
 TRACE_KINDS = {1: "gemm", 2: "attention", 3: "attn_merge"}
 KERNEL_CLASSES = ("gemm", "attention", "norm", "lm_head", "accept")
 

@@ -8,10 +8,12 @@
 // heads of one KV head (GQA group) and all block rows of the request share
 // each K/V tile read from HBM.
 //
-// Work item = (request, kv head, chunk of keys). Each item keeps a running
-// softmax (max m, sum l, unnormalized output O) over its keys, writes the
-// partial, and the last item of a (request, kv head) to arrive merges the
-// partials: out = sum_c O_c e^(m_c - M) / sum_c l_c e^(m_c - M), M = max_c m_c.
+// This CUDA-core kernel serves float32 models (bf16 caches run the tensor-core
+// attention). Work item = (request, kv head, chunk of 256 keys). Each item
+// keeps a running softmax (max m, sum l, unnormalized output O) over its keys
+// in tiles of 32, writes the partial, and the last item of a (request, kv
+// head) to arrive merges the partials:
+// out = sum_c O_c e^(m_c - M) / sum_c l_c e^(m_c - M), M = max_c m_c.
 // No item waits on another.
 #include "device_util.cuh"
 #include "internal.h"
@@ -21,16 +23,23 @@ namespace {
 
 constexpr int KT = 32;  // keys per inner tile
 
-template <typename KVT>
-__device__ __forceinline__ float kv_load(const KVT* p, long long i) {
-  if constexpr (sizeof(KVT) == 2)
-    return bf16_bits_to_f32(p[i]);
-  else
-    return p[i];
+// 16-byte asynchronous copy global -> shared (completes with cp.async.wait_group).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// float32 KV: the chunk's page ids once, then K/V tiles of KT keys by 16-byte
+// asynchronous copies into a double buffer (the next tile loads while this one
+// is used), rows padded to hd + 4 floats so a warp's 16-byte reads of
+// consecutive keys fall in distinct banks.
 template <typename KVT>
 __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
+  static_assert(sizeof(KVT) == 4, "the CUDA-core attention reads float32 caches");
   extern __shared__ __align__(16) float sm[];
   pdl_trigger();
   pdl_wait();
@@ -49,16 +58,29 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
   const int R = nrows * group;
   const int nq = a.n_heads * hd;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int LD = hd + 4;  // padded K/V row (floats)
 
-  float* Qs = sm;                         // [R][hd]
-  float* Os = Qs + a.max_rows * hd;       // [R][hd]
-  float* Ks = Os + a.max_rows * hd;       // [KT][hd + 1]
-  float* Vs = Ks + KT * (hd + 1);         // [KT][hd]
-  float* S = Vs + KT * hd;                // [R][KT]
-  float* mrow = S + a.max_rows * KT;      // [R]
-  float* lrow = mrow + a.max_rows;        // [R]
-  float* crow = lrow + a.max_rows;        // [R]
+  float* Qs = sm;                          // [R][hd]
+  float* Os = Qs + a.max_rows * hd;        // [R][hd]
+  float* Kb = Os + a.max_rows * hd;        // [2][KT][LD]
+  float* Vb = Kb + 2 * KT * LD;            // [2][KT][LD]
+  float* S = Vb + 2 * KT * LD;             // [R][KT]
+  float* mrow = S + a.max_rows * KT;       // [R]
+  float* lrow = mrow + a.max_rows;         // [R]
+  float* crow = lrow + a.max_rows;         // [R]
+  int* pages = reinterpret_cast<int*>(crow + a.max_rows);  // [chunk / page_size]
 
+  const int* ptab = a.page_table + (long long)r * a.max_pages;
+  const int npg = (kend - kbeg + a.page_size - 1) / a.page_size;
+  for (int i = tid; i < npg; i += blockDim.x) {
+    const int pidx = kbeg / a.page_size + i;
+    int page = pidx < a.max_pages ? ptab[pidx] : -1;
+    if (page < 0 || page >= a.n_pages) {
+      atomicOr(a.status, pidx >= a.max_pages ? kStNoPage : kStBadPage);
+      page = -1;
+    }
+    pages[i] = page;
+  }
   const float scale = rsqrtf(static_cast<float>(hd));
   for (int idx = tid; idx < R * hd; idx += blockDim.x) {
     const int rho = idx / hd, d = idx - rho * hd;
@@ -70,50 +92,68 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
     mrow[rho] = -INFINITY;
     lrow[rho] = 0.f;
   }
-  const KVT* kc = reinterpret_cast<const KVT*>(a.k_cache);
-  const KVT* vc = reinterpret_cast<const KVT*>(a.v_cache);
-  const int* ptab = a.page_table + (long long)r * a.max_pages;
-
-  for (int kt0 = kbeg; kt0 < kend; kt0 += KT) {
-    __syncthreads();
-    for (int idx = tid; idx < KT * hd; idx += blockDim.x) {
-      const int i = idx / hd, d = idx - i * hd;
-      const int key = kt0 + i;
-      float kv = 0.f, vv = 0.f;
-      if (key < kend) {
-        const int pidx = key / a.page_size;
-        const int page = pidx < a.max_pages ? ptab[pidx] : -1;
-        if (page >= 0 && page < a.n_pages) {
-          const long long off = (((long long)page * nkv + h) * a.page_size + (key - pidx * a.page_size)) * hd + d;
-          kv = kv_load(kc, off);
-          vv = kv_load(vc, off);
-        } else if (d == 0) {
-          atomicOr(a.status, pidx >= a.max_pages ? kStNoPage : kStBadPage);
-        }
+  __syncthreads();
+  const float* kc = reinterpret_cast<const float*>(a.k_cache);
+  const float* vc = reinterpret_cast<const float*>(a.v_cache);
+  const int q4 = hd / 4;  // 16-byte pieces per row
+  // tile t of the chunk into buffer b: keys past the chunk or on a bad page are zeros
+  auto load_tile = [&](int t, int b) {
+    float* kb = Kb + b * KT * LD;
+    float* vb = Vb + b * KT * LD;
+    for (int idx = tid; idx < KT * q4; idx += blockDim.x) {
+      const int i = idx / q4, d = (idx - i * q4) * 4;
+      const int key = kbeg + t * KT + i;
+      const int page = key < kend ? pages[(key - kbeg) / a.page_size] : -1;
+      if (page >= 0) {
+        const long long off = (((long long)page * nkv + h) * a.page_size + (key % a.page_size)) * hd + d;
+        cp_async16(kb + i * LD + d, kc + off);
+        cp_async16(vb + i * LD + d, vc + off);
+      } else {
+        *reinterpret_cast<float4*>(kb + i * LD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(vb + i * LD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      Ks[i * (hd + 1) + d] = kv;
-      Vs[i * hd + d] = vv;
+    }
+    cp_async_commit();
+  };
+  const int ntiles = (kend - kbeg + KT - 1) / KT;
+  load_tile(0, 0);
+  for (int t = 0; t < ntiles; ++t) {
+    const int b = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(t + 1, b ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const float* kb = Kb + b * KT * LD;
+    const float* vb = Vb + b * KT * LD;
+    const int kt0 = kbeg + t * KT;
     for (int idx = tid; idx < R * KT; idx += blockDim.x) {
       const int rho = idx / KT, i = idx - rho * KT;
       const int key = kt0 + i, j = rho / group;
-      float s = -INFINITY;
-      if (key < kend && key <= C + j) {
-        const float* q = Qs + rho * hd;
-        const float* k = Ks + i * (hd + 1);
+      float sc = -INFINITY;
+      if (key < kend && key <= C + j && pages[(key - kbeg) / a.page_size] >= 0) {
+        const float4* q = reinterpret_cast<const float4*>(Qs + rho * hd);
+        const float4* k = reinterpret_cast<const float4*>(kb + i * LD);
         float acc = 0.f;
-        for (int d = 0; d < hd; ++d) acc = fmaf(q[d], k[d], acc);
-        s = acc;
+        for (int d = 0; d < q4; ++d) {
+          const float4 qq = q[d], kk = k[d];
+          acc = fmaf(qq.x, kk.x, acc);
+          acc = fmaf(qq.y, kk.y, acc);
+          acc = fmaf(qq.z, kk.z, acc);
+          acc = fmaf(qq.w, kk.w, acc);
+        }
+        sc = acc;
       }
-      S[idx] = s;
+      S[idx] = sc;
     }
     __syncthreads();
     for (int rho = warp; rho < R; rho += blockDim.x >> 5) {
-      const float s = S[rho * KT + lane];
+      const float sv = S[rho * KT + lane];
       const float mold = mrow[rho];
-      const float mnew = fmaxf(mold, warp_max(s));
-      const float p = s == -INFINITY ? 0.f : expf(s - mnew);
+      const float mnew = fmaxf(mold, warp_max(sv));
+      const float p = sv == -INFINITY ? 0.f : expf(sv - mnew);
       const float corr = mold == -INFINITY ? 0.f : expf(mold - mnew);
       const float psum = warp_sum(p);
       S[rho * KT + lane] = p;
@@ -124,16 +164,25 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
       }
     }
     __syncthreads();
-    for (int idx = tid; idx < R * hd; idx += blockDim.x) {
-      const int rho = idx / hd, d = idx - rho * hd;
+    for (int idx = tid; idx < R * q4; idx += blockDim.x) {
+      const int rho = idx / q4, d = (idx - rho * q4) * 4;
       const float* p = S + rho * KT;
-      float o = Os[idx] * crow[rho];
+      float4 o = *reinterpret_cast<const float4*>(Os + rho * hd + d);
+      const float c = crow[rho];
+      o = make_float4(o.x * c, o.y * c, o.z * c, o.w * c);
 #pragma unroll 8
-      for (int i = 0; i < KT; ++i) o = fmaf(p[i], Vs[i * hd + d], o);
-      Os[idx] = o;
+      for (int i = 0; i < KT; ++i) {
+        const float pi = p[i];
+        const float4 vv = *reinterpret_cast<const float4*>(vb + i * LD + d);
+        o.x = fmaf(pi, vv.x, o.x);
+        o.y = fmaf(pi, vv.y, o.y);
+        o.z = fmaf(pi, vv.z, o.z);
+        o.w = fmaf(pi, vv.w, o.w);
+      }
+      *reinterpret_cast<float4*>(Os + rho * hd + d) = o;
     }
+    __syncthreads();  // the buffer is reloaded two tiles on
   }
-  __syncthreads();
 
   // partial of this chunk: per row [m, l, O[hd]]
   const int item = blockIdx.x;  // (r, h)
@@ -180,8 +229,9 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
 
 size_t attn_smem_bytes(const AttnArgs& a) {
   const int hd = a.head_dim;
-  return sizeof(float) * ((size_t)2 * a.max_rows * hd + KT * (hd + 1) + KT * hd + (size_t)a.max_rows * KT +
-                          3 * (size_t)a.max_rows);
+  return sizeof(float) * ((size_t)2 * a.max_rows * hd + 4 * KT * (hd + 4) + (size_t)a.max_rows * KT +
+                          3 * (size_t)a.max_rows) +
+         sizeof(int) * (a.chunk / a.page_size + 1);
 }
 
 }  // namespace
@@ -201,11 +251,8 @@ size_t attention_partial_floats(const AttnArgs& a, int max_batch) {
 cudaError_t launch_attention(const AttnArgs& a, int B, int kv_bf16, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(a);
   const dim3 grid(B * a.n_kv_heads, a.max_chunks);
-  if (kv_bf16) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fma_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_k(attn_fma_kernel<uint16_t>, grid, dim3(256), smem, s, a.pdl != 0, a);
+  if (kv_bf16) {  // bf16 caches run the tensor-core attention
+    return cudaErrorInvalidValue;
   } else {
     cudaError_t e =
         cudaFuncSetAttribute(attn_fma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

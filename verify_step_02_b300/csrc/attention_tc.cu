@@ -51,7 +51,7 @@ namespace {
 using namespace tc;
 
 constexpr int kSub = 64;                              // keys per sub-chunk
-constexpr int kStages = 3;                            // K/V ring depth
+constexpr int kStages = 5;                            // K/V ring depth
 constexpr int kPageBlock = 256;                       // page-table entries the producer holds at once
 constexpr int kMaxCluster = 16;                       // CTAs per (request, kv head)
 constexpr int kSetWarps = 8;                          // a softmax set: two warps per 32-lane TMEM group
@@ -110,9 +110,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t QB = 2 * NH * kTile;         // Q: hi and lo planes, NH halves of 128 rows x 128 B
   constexpr uint32_t KT = kSub * 128;             // a half-head tile of one sub-chunk: 64 keys x 128 B
   constexpr uint32_t KVB = 2 * NH * KT;           // one stage: K (NH halves), then V (NH halves)
-  constexpr uint32_t PB = 2 * kTile;              // one set's P: hi and lo planes, 128 rows x 64 keys bf16
-  constexpr uint32_t KV_OFF = QB, P_OFF = QB + kStages * KVB;
-  constexpr uint32_t PM_OFF = P_OFF + 2 * PB;     // partial row maxima, bf16 [set][hf][128]
+  constexpr uint32_t KV_OFF = QB;
+  constexpr uint32_t PM_OFF = KV_OFF + kStages * KVB;  // partial row maxima, bf16 [set][hf][128]
+  // once every MMA is done the K/V ring holds the CTA's partial (O, then (m, l)) and
+  // the merge's scratch: the two sets' (m, l), then the cluster merge's weights
+  constexpr uint32_t XCH_OFF = KV_OFF + 128 * HD * 4 + 128 * 8;
+  constexpr uint32_t WTS_OFF = XCH_OFF + 4 * 128 * 8;
+  constexpr uint32_t MLS_OFF = WTS_OFF + 128 * 16 * 4;
+  static_assert(MLS_OFF + 128 * 16 * 8 <= KV_OFF + kStages * KVB, "merge scratch must fit the K/V ring");
   constexpr uint32_t BAR_OFF = PM_OFF + 2 * 2 * 2 * 128 + 4 * 16;  // + the pair wait flags
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -188,8 +193,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S buffers at columns 0 and 64; set b's O at 128 + b * HD
-  const uint32_t tS = tmem, tO = tmem + 128;
+  // S buffers at columns 0 and 64; set b's O at 128 + b * HD; set b's P (hi, lo: 32
+  // columns each, two bf16 keys per column) at 128 + 2 HD + 64 b
+  const uint32_t tS = tmem, tO = tmem + 128, tP = tmem + 128 + 2 * HD;
 
   if (nsub == 0) {
     // no keys in this CTA's range: an empty partial
@@ -295,14 +301,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       auto issue_pv = [&](int j) {
         const int st = j % kStages, b = j & 1;
-        const uint32_t pb = smem_u32(smem + P_OFF + b * PB);
+        const uint32_t pt = tP + b * 64;  // P_j (hi, then lo) in TMEM: the MMA's A operand
         const uint32_t v = smem_u32(smem + KV_OFF + st * KVB + NH * KT);
         const uint32_t to = tO + b * HD;
 #pragma unroll
         for (int ks = 0; ks < kSub / 16; ++ks) {
           const uint64_t bd = smem_desc_sw128_mn(v + ks * 2048, KT, 1024);
-          mma_bf16(to, smem_desc_sw128(pb + ks * 32), bd, idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
-          mma_bf16(to, smem_desc_sw128(pb + kTile + ks * 32), bd, idesc_o, 1u);
+          mma_bf16_ts(to, pt + ks * 8, bd, idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(to, pt + 32 + ks * 8, bd, idesc_o, 1u);
         }
         mma_commit(kv_empty + st);  // K_j / V_j no longer needed
         mma_commit(pv_done + b);    // P_j no longer needed, O_b complete through j
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int lim = live ? C + j0 + rho / group : -1;  // last key this row may see
     const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t to = tO + set * HD;
-    uint8_t* pt = smem + P_OFF + set * PB;
+    const uint32_t tp = tP + set * 64 + lane_base;  // this row's P columns (set's hi at +0, lo at +32)
     // partial maxima of the two warps of a row, truncated to bf16 so both warps
     // take the same maximum: [set][hf][128]
     uint16_t* pmax = reinterpret_cast<uint16_t*>(smem + PM_OFF);
@@ -428,14 +434,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
       }
       if (!idle) {
-        // P_j row rho: 16-byte chunk 4 hf + q holds keys 32 hf + 8 q .. + 7 (hi and lo tiles)
+        // P_j row rho into TMEM: keys 32 hf + 2 i and + 1 in column 16 hf + i (hi and lo)
+        uint32_t ph[16], pl[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 hi, lo;
           split8(v + 8 * q, hi, lo);
-          *reinterpret_cast<uint4*>(pt + sw128(rho, hf * 4 + q)) = hi;
-          *reinterpret_cast<uint4*>(pt + kTile + sw128(rho, hf * 4 + q)) = lo;
+          ph[4 * q] = hi.x, ph[4 * q + 1] = hi.y, ph[4 * q + 2] = hi.z, ph[4 * q + 3] = hi.w;
+          pl[4 * q] = lo.x, pl[4 * q + 1] = lo.y, pl[4 * q + 2] = lo.z, pl[4 * q + 3] = lo.w;
         }
+        tmem_st16u(tp + hf * 16, ph);
+        tmem_st16u(tp + 32 + hf * 16, pl);
       }
       if (j >= set + 2 && __any_sync(0xffffffffu, corr != 1.f)) {
         // this warp rescales O_set's dims hf * HD / 2 .. + HD / 2
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     int okw = 0;
     if (lane == 0) okw = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
     okw = __shfl_sync(0xffffffffu, okw, 0);
-    float2* xch = reinterpret_cast<float2*>(smem + P_OFF);  // P is free once O is complete: [set][hf][128]
+    float2* xch = reinterpret_cast<float2*>(smem + XCH_OFF);  // [set][hf][128]
     if (okw) xch[(set * 2 + hf) * 128 + rho] = make_float2(m, l);
     named_bar(9, kRowThreads);
     if (okw) {
@@ -524,8 +533,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rpr = (R + CS - 1) / CS;
     const int rr0 = rank * rpr, rr1 = rr0 + rpr < R ? rr0 + rpr : R;
     const uint32_t os_addr = smem_u32(Os), ml_addr = smem_u32(ML);
-    float* wts = reinterpret_cast<float*>(smem + P_OFF);            // [rpr][kMaxCluster]
-    float2* mls = reinterpret_cast<float2*>(smem + P_OFF + 16384);   // [rpr][kMaxCluster]
+    float* wts = reinterpret_cast<float*>(smem + WTS_OFF);    // [rpr][kMaxCluster]
+    float2* mls = reinterpret_cast<float2*>(smem + MLS_OFF);  // [rpr][kMaxCluster]
     const int nrr = rr1 - rr0;
     // every rank's (m, l) of this rank's rows, all loads in flight
     for (int it = tid; it < nrr * CS; it += kAttnThreads) {
@@ -586,8 +595,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 size_t attn_tc_smem(int hd) {
-  const size_t nh = hd / 64, q = 2 * nh * kTile, kv = 2 * nh * kSub * 128, pb = 2 * kTile;
-  return 1024 + q + kStages * kv + 2 * pb + 2 * 2 * 2 * 128 + 4 * 16 + (2 * kStages + 9) * 8 + 32;
+  const size_t nh = hd / 64, q = 2 * nh * kTile, kv = 2 * nh * kSub * 128;
+  return 1024 + q + kStages * kv + 2 * 2 * 2 * 128 + 4 * 16 + (2 * kStages + 9) * 8 + 32;
 }
 
 template <int HD>

@@ -145,12 +145,12 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
   a.k_chunk = K;
   a.cl_size = 0;
   a.cl_tiles = 0;
-  // Small token tiles: the cluster split, when some (CTAs per cluster 2 .. 8, tiles
+  // Small token tiles: the cluster split, when some (CTAs per cluster 2 .. 8, one tile
   // per cluster) fits the device in one wave on at least 85% of the SMs (one SM
   // streams only about its even share of HBM bandwidth with this pipeline depth)
   // with per-CTA work within 1.2x of stream-K's: the fewest units per CTA wins,
   // then the larger cluster (a smaller slice per rank, so more pipeline stages).
-  if (a.tc_nt > kClusterMaxNT || a.tc_stages < 2) return;
+  if (a.tc_nt > kClusterMaxNT || a.m_tiles != 1 || a.tc_stages < 2) return;
   const long long ntt = static_cast<long long>(a.n_tiles) * a.m_tiles;
   const long long sk_work = (U + a.grid_p - 1) / a.grid_p;
   long long best_work = 0, best_ctas = 0;
@@ -161,7 +161,9 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
     const int st_cl = tc_stages_for(a.tc_nt, pair2, a.tc_ks, w12, cs);
     if (st_cl < 2) continue;
     int mc = -1;
-    for (int tc = 1; tc <= 8; ++tc) {
+    // one tile per cluster: with several, every tile's hand-off waits for the slowest
+    // rank and the epilogue falls behind the MMAs (measured slower than stream-K)
+    for (int tc = 1; tc <= 1; ++tc) {
       const long long ncl = (ntt + tc - 1) / tc;
       if (ncl * cs > sm_count || ncl * cs * 20 < 17LL * sm_count) continue;
       if (mc < 0) mc = max_clusters(a.tc_nt, pair2, w12, cs, st_cl);

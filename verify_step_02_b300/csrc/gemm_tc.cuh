@@ -13,16 +13,16 @@
 //              bytes. A tile whose K range is shared by several CTAs is
 //              finished by the last of them to arrive, which sums the partial
 //              tiles (in global memory) in CTA order and runs the epilogue.
-//   cluster    (token tiles of at most 64 columns, the small projections)
-//              clusters of CS CTAs own whole tiles; the CTAs of a cluster split
-//              each tile's K blocks evenly. Each CTA leaves its partial tile in
-//              its own shared memory; then rank r sums a 1/CS share of the
-//              tile's tokens over the CS partials through distributed shared
-//              memory, in rank order (a reduce-scatter), and runs their
-//              epilogue from inputs it staged in shared memory while the
-//              weights streamed. The hand-off at the end of the product then
-//              needs no round trip through L2, which is what the end of a
-//              launch waits on, and each SM reduces and finishes 1/CS of it.
+//   cluster    (token tiles of at most 64 columns, one weight tile per cluster:
+//              the O and down projections) the CS CTAs of a cluster split the
+//              tile's K blocks evenly. Each rank stores a 1/CS share of its
+//              partial tile's tokens straight into the shared memory of the
+//              rank that finishes those tokens (asynchronous stores counted on
+//              that rank's mbarrier); rank r sums the CS shares in rank order
+//              (a reduce-scatter) and runs their epilogue from inputs it
+//              staged in shared memory while the weights streamed. The
+//              hand-off at the end of the product then needs no round trip
+//              through L2, which is what the end of a launch waits on.
 // Both orders are fixed, so results do not depend on timing.
 //
 // Roles inside a CTA (384 threads; W12 weights: 512):
@@ -121,16 +121,15 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   uint8_t* aring = smem + static_cast<size_t>(S) * STAGE;  // W12: rebuilt bf16 weight tiles, 2 x NSUB x 16 KB
   // stream-K: Ys [128][33] and the launch's per-token data. Cluster split: the rank's
   // token slice of SL columns: Ys [128][SL + 1], staged epilogue inputs Es [128][SL],
-  // and this CTA's partial tile Xp, row-major [row][NT + 4] (the pad keeps a warp's
-  // 16-byte accesses to distinct banks)
-  constexpr int XLD = NT + 4;
+  // and Rx [CS][128][SL], the slices of every rank's partial tile that the ranks
+  // store into this CTA's shared memory
   const int SL = CL ? cl_slice(NT, a.cl_size) : 32;
   const int YLD = CL ? SL + 1 : kYsLd;
   float* Ys = reinterpret_cast<float*>(aring + (W12 ? kW12Ring * NSUB * kABytes : 0));
   EpiSmem* esm = reinterpret_cast<EpiSmem*>(Ys + kGemmBN * YLD);
   TokData* tok = reinterpret_cast<TokData*>(esm + 1);
-  float* Xp = reinterpret_cast<float*>(esm + 1);
-  float* Es = Xp + kGemmBN * XLD;
+  float* Rx = reinterpret_cast<float*>(esm + 1);
+  float* Es = Rx + (CL ? a.cl_size : 0) * kGemmBN * SL;
   uint64_t* full = CL ? reinterpret_cast<uint64_t*>(Es + kGemmBN * SL) : reinterpret_cast<uint64_t*>(tok + 1);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
@@ -138,9 +137,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint64_t* afull = drain + 1;     // W12 ring: rebuilt tile ready
   uint64_t* aempty = afull + 2;    // W12 ring: tile consumed by the MMAs
-  uint64_t* xr_full = aempty + 2;  // cluster: every rank's partial of the current tile is in place
-  uint64_t* xr_free = xr_full + 1; // cluster: every rank has read this CTA's partial
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xr_free + 1);
+  uint64_t* rx_full = aempty + 2;  // cluster: every rank's slice for this CTA has landed (transaction bytes)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rx_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_flag = abort_flag + 1;
 
@@ -189,8 +187,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       mbar_init(acc_empty + i, 128);  // the TMEM-reading warpgroup
     }
     mbar_init(drain, 1);
-    mbar_init(xr_full, CS);  // one arrival per rank of the cluster: its partial is in place
-    mbar_init(xr_free, CS);  // one arrival per rank: it has read this CTA's partial
+    mbar_init(rx_full, 1);  // this CTA's own arrival (with the bytes it expects)
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -435,6 +432,14 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     const TokData* td = !CL && a.M <= kTokMax ? tok : nullptr;
     if (td)
       for (int m = et2; m < a.M; m += EPT) token_data(a.epi, m, tok->rstd[m], tok->pos[m], tok->kv[m]);
+    if (CL) {
+      // the cluster split has one token tile (M <= NT <= 64), so this rank's tokens are the
+      // same for every tile: their per-token data once, into the epilogue's scratch
+      const int mt0 = a.M < NT ? a.M : NT;
+      const int sl = ((mt0 + CS - 1) / CS + 3) / 4 * 4;
+      const int c0 = rank * sl, c1 = c0 + sl < mt0 ? c0 + sl : mt0;
+      for (int c = et2; c < c1 - c0; c += EPT) token_data(a.epi, c0 + c, esm->rstd[c], esm->pos[c], esm->kv[c]);
+    }
     auto sync = [] { named_bar(1, EPT); };
     sync();
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -452,15 +457,10 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       // the hand-off of the CTA's last tile goes into the timeline
       unsigned long long* const trec = rec && iend == NU && et2 == 0 ? rec : nullptr;
       if (CL) {
-        // the epilogue's global inputs of this rank's tokens (and their per-token data), into
-        // shared memory while the tile accumulates
+        // the epilogue's global inputs of this rank's tokens, into shared memory while the tile accumulates
         const int sl = ((mtot + CS - 1) / CS + 3) / 4 * 4;
         const int c0 = rank * sl, c1 = c0 + sl < mtot ? c0 + sl : mtot;
-        if (c0 < c1) {
-          for (int c = et2; c < c1 - c0; c += EPT) token_data(a.epi, m_base + c0 + c, esm->rstd[c], esm->pos[c], esm->kv[c]);
-          sync();  // the positions feed the staged RoPE rows
-          stage_epilogue_inputs(a, nt, m_base + c0, c1 - c0, Es, *esm, nullptr, et2, EPT);
-        }
+        if (c0 < c1) stage_epilogue_inputs(a, nt, m_base + c0, c1 - c0, Es, *esm, nullptr, et2, EPT);
       }
       // one thread waits and broadcasts, so all threads agree on the outcome
       if (et2 == 0) *s_flag = mbar_wait(acc_full + b, (seg >> 1) & 1, abort_flag, kWaitNs) ? 1 : 0;
@@ -471,105 +471,76 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       tc_fence_after();
       trace_mark(trec, 7);
       if constexpr (CL) {
-        // ---- cluster split, reduce-scatter: every rank leaves its partial in its own shared
-        // memory; rank r then sums tokens [c0, c1) of the tile (a 1/CS share, 4-aligned)
-        // from every rank's partial over DSMEM, in rank order, and runs their epilogue
-        const long long j = t - W.t0;  // tile index within the cluster
-        if (j >= 1) {  // every rank has read this CTA's partial of the previous tile
-          if (et2 == 0) *s_flag = mbar_wait_cluster(xr_free, static_cast<uint32_t>((j - 1) & 1), abort_flag, kWaitNs);
-          sync();
-          const bool okf = *s_flag != 0;
-          sync();
-          if (!okf) break;
-        }
-        if (grpA) {
-          for (int ch = 0; ch * 32 < mtot; ++ch) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v);
-            if (FUSE) {  // the lo plane's products
-              float w[32];
-              tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] += w[k];
-            }
-            float4* xr = reinterpret_cast<float4*>(Xp + et * XLD + ch * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) xr[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-          }
-          tc_fence_before();
-          mbar_arrive(acc_empty + b);
-        }
-        trace_mark(trec, 12);
-        sync();
-        if (et2 == 0) {  // this rank's partial is in place: tell every rank
-          fence_acq_rel_cluster();
-          for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_full), static_cast<uint32_t>(r)));
-        }
-        trace_mark(trec, 8);
-        if (et2 == 0) *s_flag = mbar_wait_cluster(xr_full, static_cast<uint32_t>(j & 1), abort_flag, kWaitNs);
-        sync();
-        const bool okr = *s_flag != 0;
-        sync();
-        if (!okr) break;
-        trace_mark(trec, 9);
+        // ---- cluster split (one tile per cluster), reduce-scatter by pushes: every rank
+        // stores the token slice [c0_r, c1_r) of its partial straight into rank r's shared
+        // memory (st.async, counted on r's rx_full); rank r sums the CS slices in rank
+        // order from its own shared memory and runs their epilogue
         const int sl = ((mtot + CS - 1) / CS + 3) / 4 * 4;
         const int c0 = rank * sl, c1 = c0 + sl < mtot ? c0 + sl : mtot;
-        // thread (row et, sub) sums the 4-column groups sub, sub + NSUBT, .. of [c0, c1),
-        // one chunk of 32 tokens at a time, with the loads of up to NR ranks in flight
-        constexpr int NSUBT = EPT / 128, GPT = 8 / NSUBT;  // column groups of a chunk per thread
-        constexpr int NR = W12 ? 1 : 4;
-        const int sub = et2 >> 7;
-        const uint32_t xb = smem_u32(Xp);
-        for (int cc = c0; cc < c1; cc += 32) {  // one pass: the slice is at most 32 columns
-          const int ncol = c1 - cc < 32 ? c1 - cc : 32;
-          float s[GPT][4];
+        const int ncol4 = c1 > c0 ? (c1 - c0 + 3) / 4 * 4 : 0;  // columns this rank receives
+        if (et2 == 0 && ncol4 > 0)
+          mbar_arrive_expect_tx(rx_full, static_cast<uint32_t>(CS * kGemmBN * ncol4 * 4));
+        if (grpA) {
+          float v[2][32];
 #pragma unroll
-          for (int g = 0; g < GPT; ++g)
+          for (int ch = 0; ch < NT / 32; ++ch)
+            if (ch * 32 < mtot) {
+              tmem_ld32(tmem + lane_base + b * ACC + ch * 32, v[ch]);
+              if (FUSE) {  // the lo plane's products
+                float w[32];
+                tmem_ld32(tmem + lane_base + b * ACC + NT + ch * 32, w);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) s[g][k] = 0.f;
-          for (int r0 = 0; r0 < CS; r0 += NR) {
-            float4 v[NR][GPT];
-#pragma unroll
-            for (int rr = 0; rr < NR; ++rr)
-#pragma unroll
-              for (int g = 0; g < GPT; ++g) {
-                const int col = (sub + g * NSUBT) * 4;
-                if (r0 + rr < CS && col < ncol)
-                  v[rr][g] = ld_dsmem_f32x4(mapa_shared(xb, static_cast<uint32_t>(r0 + rr)) +
-                                            4u * (et * XLD + cc + col));
+                for (int k = 0; k < 32; ++k) v[ch][k] += w[k];
               }
+            }
+          tc_fence_before();
+          mbar_arrive(acc_empty + b);
+          // token group c .. c + 3 (c a multiple of 4) goes to rank c / sl, slot (c % sl) / 4
+          const uint32_t rx = smem_u32(Rx) + 4u * ((rank * kGemmBN + et) * SL), rxf = smem_u32(rx_full);
 #pragma unroll
-            for (int rr = 0; rr < NR; ++rr)
+          for (int ch = 0; ch < NT / 32; ++ch)
 #pragma unroll
-              for (int g = 0; g < GPT; ++g)
-                if (r0 + rr < CS && (sub + g * NSUBT) * 4 < ncol) {
-                  s[g][0] += v[rr][g].x;
-                  s[g][1] += v[rr][g].y;
-                  s[g][2] += v[rr][g].z;
-                  s[g][3] += v[rr][g].w;
-                }
-          }
-#pragma unroll
-          for (int g = 0; g < GPT; ++g) {
-            const int col = (sub + g * NSUBT) * 4;
-            if (col < ncol)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) Ys[et * YLD + col + k] = s[g][k];
+            for (int q = 0; q < 8; ++q) {
+              const int c = ch * 32 + 4 * q;
+              if (c < mtot) {
+                const int r = c / sl;
+                st_async_v4(mapa_shared(rx, static_cast<uint32_t>(r)) + 4u * (c - r * sl),
+                            make_float4(v[ch][4 * q], v[ch][4 * q + 1], v[ch][4 * q + 2], v[ch][4 * q + 3]),
+                            mapa_shared(rxf, static_cast<uint32_t>(r)));
+              }
+            }
+        }
+        trace_mark(trec, 8);
+        if (ncol4 > 0) {
+          if (et2 == 0) *s_flag = mbar_wait_cluster(rx_full, 0u, abort_flag, kWaitNs);
+          sync();
+          const bool okr = *s_flag != 0;
+          sync();
+          if (!okr) break;
+          trace_mark(trec, 9);
+          // thread (row et, sub) sums the 4-column groups sub, sub + NSUBT, .. in rank order
+          constexpr int NSUBT = EPT / 128;
+          const int sub = et2 >> 7;
+          for (int g = sub; g * 4 < ncol4; g += NSUBT) {
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < CS; ++r) {
+              const float4 q = *reinterpret_cast<const float4*>(Rx + (r * kGemmBN + et) * SL + 4 * g);
+              s4.x += q.x;
+              s4.y += q.y;
+              s4.z += q.z;
+              s4.w += q.w;
+            }
+            Ys[et * YLD + 4 * g] = s4.x;
+            Ys[et * YLD + 4 * g + 1] = s4.y;
+            Ys[et * YLD + 4 * g + 2] = s4.z;
+            Ys[et * YLD + 4 * g + 3] = s4.w;
           }
           trace_mark(trec, 13);
           sync();
-          if (cc + 32 >= c1 && et2 == 0) {
-            // this rank has read every rank's partial of the tile (all loads completed
-            // before the barrier above): release them
-            for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_free), static_cast<uint32_t>(r)));
-          }
           trace_mark(trec, 10);
-          epilogue_tile(a, nt, Ys, YLD, m_base + cc, ncol, et2, EPT, *esm, nullptr, sync, Es, true);
+          epilogue_tile(a, nt, Ys, YLD, m_base + c0, c1 - c0, et2, EPT, *esm, nullptr, sync, Es, true);
           sync();
           trace_mark(trec, 11);
-        }
-        if (c0 >= c1 && et2 == 0) {  // no tokens for this rank: it read nothing
-          for (int r = 0; r < CS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(xr_free), static_cast<uint32_t>(r)));
         }
       } else {
         // ---- stream-K: partials through global memory, the last arriver sums them
@@ -669,16 +640,14 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
       ++seg;
       i = iend;
     }
-    if (CL && NU > 0) {
-      // This CTA may leave once every rank has read its partial of the last tile
-      // (xr_free); every rank's arrival for that tile came before this CTA's own
-      // xr_full wait. After a normal run this has happened already; after a
-      // timed-out wait it is awaited, bounded.
-      if (et2 == 0) {
+    if (CL && NU > 0 && *abort_flag) {
+      // after a timed-out wait: this CTA leaves only once the slices other ranks
+      // store into it have landed (bounded); after a normal run they have
+      const int mt0 = a.M < NT ? a.M : NT;
+      const int sl = ((mt0 + CS - 1) / CS + 3) / 4 * 4;
+      if (et2 == 0 && rank * sl < mt0) {
         volatile int never = 0;
-        const long long ntc = NU / W.nk;
-        mbar_wait_cluster(xr_free, static_cast<uint32_t>((ntc - 1) & 1), &never, kWaitNs);
-        mbar_wait_cluster(xr_full, static_cast<uint32_t>((ntc - 1) & 1), &never, kWaitNs);
+        mbar_wait_cluster(rx_full, 0u, &never, kWaitNs);
       }
       sync();
     }

@@ -37,13 +37,13 @@ constexpr int stage_bytes(int nt, bool pair, int ks, bool w12) {
 constexpr int cl_slice(int nt, int cs) { return ((nt + cs - 1) / cs + 3) / 4 * 4; }
 
 // cs > 0: the cluster split, whose epilogue works on a slice of the tokens: its
-// tile values Ys [128][slice + 1], its staged inputs Es [128][slice] and this
-// CTA's partial tile Xp [128][nt + 4] replace the stream-K Ys [128][33] and
-// the launch's per-token data.
+// tile values Ys [128][slice + 1], its staged inputs Es [128][slice] and the
+// slices every rank pushes to it, Rx [cs][128][slice], replace the stream-K
+// Ys [128][33] and the launch's per-token data.
 constexpr size_t tc_smem_bytes(int nt, bool pair, int ks, int stages, bool w12, int cs = 0) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes(nt, pair, ks, w12) +
          (w12 ? static_cast<size_t>(kW12Ring) * (ks / 64) * kABytes : 0) +
-         (cs > 0 ? sizeof(float) * kGemmBN * (cl_slice(nt, cs) + 1 + cl_slice(nt, cs) + nt + 4)
+         (cs > 0 ? sizeof(float) * kGemmBN * (cl_slice(nt, cs) * (cs + 2) + 1)
                  : sizeof(float) * kGemmBN * kYsLd + sizeof(TokData)) +
          sizeof(EpiSmem) + sizeof(uint64_t) * (2 * stages + 11) + 16;
 }

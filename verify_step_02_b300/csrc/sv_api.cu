@@ -147,6 +147,10 @@ sv_status check_config(const sv_config* c) {
   if (c->max_gamma < 0 || c->max_gamma > kMaxGamma)
     return fail(SV_ERR_INVALID_ARG, "max_gamma must be 0..%d", kMaxGamma);
   if (c->page_size < 1 || c->page_size > 256) return fail(SV_ERR_INVALID_ARG, "page_size must be 1..256");
+  if (c->weight_dtype != SV_F32 && c->page_size != 16)
+    return fail(SV_ERR_UNSUPPORTED, "bf16/W12 models: page_size must be 16 (the tensor-core attention's page)");
+  if (c->weight_dtype == SV_F32 && 256 % c->page_size)
+    return fail(SV_ERR_UNSUPPORTED, "float32 models: page_size must divide 256 (the attention's key chunk)");
   if (c->max_seq_len < 1 || c->max_seq_len > (1 << 24)) return fail(SV_ERR_INVALID_ARG, "bad max_seq_len");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(SV_ERR_INVALID_ARG, "bad rms_eps or rope_theta");
   // float32 models run the CUDA-core attention, which holds a request's rows in shared memory
@@ -540,7 +544,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->req_row0, sizeof(int) * (c.max_batch + 1)));
   TRY(dalloc(m, &m->rope, sizeof(float2) * (size_t)c.max_seq_len * (c.head_dim / 2)));
   size_t part = 0, cnt = 0;
-  m->use_tc = cfg->weight_dtype == SV_BF16 || cfg->weight_dtype == SV_W12;
+  m->use_tc = (cfg->weight_dtype == SV_BF16 || cfg->weight_dtype == SV_W12) && !(cfg->flags & SV_FLAG_CUDA_CORE_GEMM);
   auto need = [&](int n_units, int K, int pair) {
     if (m->use_tc)
       gemm_tc_ws_need(m->sm_count, M, n_units, K, pair, &part, &cnt, cfg->weight_dtype);
