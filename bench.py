@@ -193,6 +193,13 @@ def traffic_record(kernel, workload, files):
 LAYER_KERNELS = ("qkv", "attention", "o", "gate_up", "down")
 
 
+# trace words past the common ones (1 start, 2 wait, 3 first operands, 4 last MMA, 6 exit)
+GEMM_MARKS = (("t_acc", 7), ("t_x", 12), ("t_stored", 8), ("t_counted", 9), ("t_summed", 13), ("t_reduced", 10),
+              ("t_epilogue", 11))
+ATTN_MARKS = (("s0_ready", 12), ("p0_ready", 13), ("kv_last", 10), ("p_last", 11), ("partial", 7),
+              ("cluster_synced", 8), ("merge_weights", 9))
+
+
 def trace_summary(records, launches, n_layers):
     """Per-kernel critical-path timeline of traced verify steps (microseconds).
 
@@ -217,8 +224,8 @@ def trace_summary(records, launches, n_layers):
         r = records[first:first + ctas].astype(np.float64)
         w = lambda k: r[:, k][r[:, k] > 0]
         starts, waits, mma0, mma1, exits = w(1), w(2), w(3), w(4), w(6)
-        tail = {n: w(k) for n, k in (("t_acc", 7), ("t_stored", 8), ("t_counted", 9), ("t_reduced", 10),
-                                      ("t_epilogue", 11), ("t_x", 12), ("t_summed", 13))}
+        marks = ATTN_MARKS if names[i] == "attention" else GEMM_MARKS
+        tail = {n: w(k) for n, k in marks}
         if len(exits) == 0:
             prev_exit = None
             continue
@@ -226,9 +233,7 @@ def trace_summary(records, launches, n_layers):
         j = i % per_step
         if prev_exit is not None and j >= nk:
             d = acc.setdefault(names[i], {k: [] for k in ("ctas", "start", "wait", "first_mma", "last_mma_median",
-                                                           "last_mma", "t_acc", "t_x", "t_stored",
-                                                           "t_counted", "t_summed", "t_reduced", "t_epilogue",
-                                                           "exit")})
+                                                           "last_mma", *(n for n, _ in marks), "exit")})
             d["ctas"].append(ctas)
             d["start"].append(starts.min() - prev_exit)
             if len(mma1):

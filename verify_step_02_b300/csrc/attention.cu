@@ -41,8 +41,8 @@ template <typename KVT>
 __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
   static_assert(sizeof(KVT) == 4, "the CUDA-core attention reads float32 caches");
   extern __shared__ __align__(16) float sm[];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int hd = a.head_dim, nkv = a.n_kv_heads, group = a.n_heads / nkv;
   const int r = blockIdx.x / nkv, h = blockIdx.x - r * nkv, chunk = blockIdx.y;
   const int C = a.seq_len[r];

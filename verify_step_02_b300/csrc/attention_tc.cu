@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
              static_cast<unsigned>(lin);
     trace_mark(rec, 1);
   }
-  pdl_trigger();
-  pdl_wait();
+  // The lengths, row ranges and page table read here and the cached keys the
+  // producer requests before its dependency wait were written two or more
+  // kernels back (every kernel triggers its dependents only after its own
+  // wait); the query tile and the block's own keys wait for the QKV product.
   const int nkv = a.n_kv_heads, group = a.n_heads / nkv;
   // blockIdx.x = (request, kv head, row tile): a row tile is a.q_rows block rows
   // (a.q_rows * group <= 128 MMA rows), so a long block spans several tiles
@@ -160,7 +162,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (tid == 0) trace_mark(rec, 6);
     return;
   }
-  if (tid == 0) trace_mark(rec, 2);
   const int T = C + j0 + ntok;  // keys any row of the tile may see
   // this CTA's keys [k0, k0 + nkeys): the T keys in CS ranges of a multiple of 64
   const int per = ((T + CS - 1) / CS + kSub - 1) / kSub * kSub;
@@ -197,8 +198,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // columns each, two bf16 keys per column) at 128 + 2 HD + 64 b
   const uint32_t tS = tmem, tO = tmem + 128, tP = tmem + 128 + 2 * HD;
 
+  if (warp != kRowWarps) {
+    pdl_wait();
+    pdl_trigger();
+    if (tid == 0) trace_mark(rec, 2);
+  }
   if (nsub == 0) {
     // no keys in this CTA's range: an empty partial
+    if (warp == kRowWarps) {
+      pdl_wait();
+      pdl_trigger();
+    }
     for (int rho = tid; rho < 128; rho += kAttnThreads) ML[rho] = make_float2(-INFINITY, 0.f);
   } else if (warp == kRowWarps) {
     // ------------------------------------------------------------ TMA producer
@@ -207,15 +217,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
-      const uint32_t qbox = 128u * group * a.q_rows;
-      mbar_arrive_expect_tx(q_full, 2 * NH * qbox);
-      const uint64_t polq = policy_evict_last();
-#pragma unroll
-      for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh)
-          tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0 + j0, q_full,
-                      polq);
     }
     // the range's page ids, kPageBlock at a time with all lookups in flight:
     // page i of the block sits in lane i % 32, register i / 32; -1 for a bad entry
@@ -239,9 +240,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     };
     const uint64_t pol = policy_evict_first();
     int issued = 0;
+    // sub-chunks whose keys all lie below C (cached before this step) go out
+    // before the dependency wait, up to the ring's depth
+    const int n_early = C - k0 >= kSub ? min(min(nsub, kStages), (C - k0) / kSub) : 0;
+    // the dependency wait, then the query tile (hi and lo planes)
+    auto load_q = [&]() {
+      pdl_wait();
+      pdl_trigger();
+      if (lane == 0) {
+        const uint32_t qbox = 128u * group * a.q_rows;
+        mbar_arrive_expect_tx(q_full, 2 * NH * qbox);
+        const uint64_t polq = policy_evict_last();
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh)
+            tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0 + j0,
+                        q_full, polq);
+      }
+    };
+    if (n_early == nsub) load_q();  // (then every sub-chunk is early: the query first)
     for (int j = 0; j < nsub; ++j) {
       const int st = j % kStages;
       const int pj = j * (kSub / 16);  // the sub-chunk's first page in the range
+      if (j == n_early) load_q();
       if (pj % kPageBlock == 0) load_pages(pj / kPageBlock);
       int ok = 1;
       if (lane == 0 && j >= kStages) ok = mbar_wait(kv_empty + st, (j / kStages - 1) & 1, abort_flag, kWaitNs);
@@ -317,6 +339,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int b = j & 1;
         ok = mbar_wait(kv_full + j % kStages, (j / kStages) & 1, abort_flag, kWaitNs);
         if (j == 0) trace_mark(rec, 3);
+        if (j == nsub - 1) trace_mark(rec, 10);
         // S buffer b was last read by set b for sub-chunk j - 2
         if (ok && j >= 2) ok = mbar_wait(p_ready + b, ((j >> 1) - 1) & 1, abort_flag, kWaitNs);
         if (!ok) break;
@@ -325,6 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j >= 1) {
           ok = mbar_wait(p_ready + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, kWaitNs);
           if (!ok) break;
+          if (j == 1) trace_mark(rec, 13);
           tc_fence_after();
           issue_pv(j - 1);
         }
@@ -333,6 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int j = nsub - 1;
         ok = mbar_wait(p_ready + (j & 1), (j >> 1) & 1, abort_flag, kWaitNs);
         if (ok) {
+          trace_mark(rec, 11);
           tc_fence_after();
           issue_pv(j);
           mma_commit(o_full);
@@ -374,6 +399,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               mbar_wait(s_full + set, (j >> 1) & 1, abort_flag, kWaitNs);
       __syncwarp();
       okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (j == 0 && warp == 0 && lane == 0) trace_mark(rec, 12);
       if (idle && !okw) {
         ok = false;
         break;

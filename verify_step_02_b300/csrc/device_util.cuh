@@ -9,9 +9,16 @@ namespace sv {
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // Programmatic dependent launch. pdl_trigger: this CTA lets the next kernel in
-// the stream start its independent prologue. pdl_wait: block until the
-// kernels before this one have completed and their writes are visible. Both
-// are no-ops for a kernel launched without the programmatic attribute.
+// the stream start its independent prologue (the first call in a CTA counts).
+// pdl_wait: block until the kernels before this one have completed and their
+// writes are visible. Both are no-ops for a kernel launched without the
+// programmatic attribute.
+//
+// Every kernel of the library triggers only after its own wait. Then at most
+// two kernels of a stream overlap, the running one (past its wait, so its
+// predecessor has completed) and the next one's prologue, and a prologue may
+// read anything written two or more kernels back (the row maps of the row
+// preparation, the committed lengths, the cached keys and values).
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   __shared__ __align__(16) float Ws[KC][WS_LD];
   __shared__ __align__(16) float Xs[KC][XS_LD];
   __shared__ __align__(16) float Ys[BN * YS_LD];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
   const int tid = threadIdx.x;
   const int tr = (tid & 15) * 8, tc = (tid >> 4) * 2;

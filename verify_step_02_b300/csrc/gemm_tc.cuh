@@ -204,7 +204,6 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -269,6 +268,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
         load_w(t, kb, st, full + i);
       }
       pdl_wait();
+      pdl_trigger();
       trace_mark(rec, 2);
       for (long long i = 0; i < npre; ++i) {
         long long t;
@@ -425,6 +425,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     // lanes 32 (w % 4) ..); with two warpgroups both share the reduction (16
     // columns each) and the tile epilogue.
     pdl_wait();  // reads what earlier kernels wrote (h, norm statistics, row maps)
+    pdl_trigger();
     const int et2 = threadIdx.x - 128;          // 0 .. EPT - 1
     const bool grpA = et2 < 128;
     const int et = et2 & 127;                   // tile row

@@ -20,8 +20,8 @@ __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, 
                                                             int max_seq_len, int weights_bf16, int x_pair,
                                                             unsigned* status) {
   __shared__ float red[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   if (m == 0)
     for (int i = threadIdx.x; i <= p.B; i += blockDim.x) req_row0_dev[i] = p.req_row0[i];
@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
   __shared__ int s_pick[2];
   __shared__ int s_targ[kMaxGamma + 1];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int row0 = a.req_row0[r], L = a.req_row0[r + 1] - row0 - 1;
   const int C = a.seq_len[r];
   const int* toks = a.tokens + (long long)r * a.gamma_stride;
