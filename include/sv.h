@@ -215,6 +215,36 @@ sv_status sv_verify_host(sv_model* model, int32_t batch, const int32_t* tokens, 
 sv_status sv_prefill(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* block_lens,
                      const sv_kv* kv, int32_t* next_token, void* stream);
 
+/*
+ * Greedy verification of a token tree per request (SpecPilot digest,
+ * "Reasons", names tree verification; this is the plain generalisation of
+ * the block verify). Request r's tree has n_drafts[r] + 1 nodes: node 0 is
+ * the anchor (the root), node i > 0 a draft whose parent is parents[r][i]
+ * (0 <= parents[r][i] < i, so parents precede children). One target forward
+ * runs over all nodes: node i sits at position C_r + depth(i) and attends to
+ * the cached positions and to its own ancestors. With t_i the greedy token
+ * after node i (argmax of its logits, lowest index on ties), node i is
+ * correct when its token equals t_{parent(i)}; the accepted path ends at the
+ * deepest node that is correct together with all its non-root ancestors (the
+ * lowest index among equally deep ones). Outputs: accepted_len[r] = that
+ * node's depth k, next_token[r] = t at its end, accepted_nodes[r][0..k] =
+ * the path's nodes, root first. Commit: the path's keys and values are moved
+ * to positions C_r .. C_r + k and seq_len[r] += k + 1.
+ *
+ * tokens [B][1 + max_gamma] and parents [B][1 + max_gamma]: device int32
+ * (parents[r][0] is ignored); n_drafts: HOST int32 [B], 0 .. min(max_gamma,
+ * 63) (at most 64 nodes per request); accepted_len, next_token [B] and
+ * accepted_nodes [B][1 + max_gamma]: device int32 out. The tree's rows use
+ * the KV slots C_r .. C_r + n_drafts[r] during the step, so the request must
+ * have that capacity. Temperature 0 only. A parent that does not precede its
+ * node is a device check (SV_ERR_DEVICE_CHECK on the next status read; the
+ * node is then treated as a chain row). Asynchronous on `stream`; other
+ * errors as sv_verify.
+ */
+sv_status sv_verify_tree(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* parents,
+                         const int32_t* n_drafts, const sv_kv* kv, int32_t* accepted_len, int32_t* next_token,
+                         int32_t* accepted_nodes, void* stream);
+
 /* Copy the float32 logits [M][vocab] of the last verify (rows in request
  * order, anchor row first) to device `dst`. Valid after a sampled verify, or
  * after any verify when the model was created with SV_FLAG_KEEP_LOGITS;

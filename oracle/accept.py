@@ -41,6 +41,37 @@ def greedy_accept(logits, drafts):
     return k, int(t[k])
 
 
+def greedy_accept_tree(logits, tokens, parents):
+    """Greedy acceptance over a token tree (SpecPilot digest, "Reasons", names tree
+    verification; the rule is the chain rule above applied along every root path).
+
+    logits [n, V] per node, tokens [n] (node 0 = the anchor), parents [n]
+    (parents[0] ignored, 0 <= parents[i] < i). With t_i = argmax z_i (lowest
+    index on ties), node i's draft is correct when tokens[i] = t_{parent(i)};
+    a node is accepted when it and every non-root ancestor are correct. The
+    accepted path ends at the deepest accepted node (the lowest index among
+    equally deep ones). Returns (accepted_len = its depth, next_token = t at
+    its end, path = its nodes, root first).
+    """
+    z = np.asarray(logits)
+    n = len(tokens)
+    t = [int(np.argmax(z[i])) for i in range(n)]
+    depth = [0] * n
+    ok = [True] + [False] * (n - 1)
+    for i in range(1, n):
+        p = int(parents[i])
+        depth[i] = depth[p] + 1
+        ok[i] = ok[p] and int(tokens[i]) == t[p]
+    end = 0
+    for i in range(1, n):
+        if ok[i] and depth[i] > depth[end]:
+            end = i
+    path = [end]
+    while path[-1] != 0:
+        path.append(int(parents[path[-1]]))
+    return depth[end], t[end], path[::-1]
+
+
 def softmax(z, temperature):
     s = np.asarray(z, dtype=np.float64) / temperature
     s = s - s.max(axis=-1, keepdims=True)

@@ -181,21 +181,64 @@ def forward_block(cfg, weights, ctx_k, ctx_v, tokens, start_pos, rowwise=True, l
     return out
 
 
+def tree_depths(parents):
+    """Depth of every node of a token tree (node 0, the anchor, is the root at depth 0).
+
+    parents[0] is ignored; every other node's parent precedes it (0 <= parents[i] < i).
+    """
+    depth = [0] * len(parents)
+    for i in range(1, len(parents)):
+        p = int(parents[i])
+        if not 0 <= p < i:
+            raise ValueError(f"node {i}: parent {p} must precede it")
+        depth[i] = depth[p] + 1
+    return depth
+
+
+def tree_path(parents, i):
+    """Nodes from the root to node i, root first."""
+    path = [i]
+    while path[-1] != 0:
+        path.append(int(parents[path[-1]]))
+    return path[::-1]
+
+
+def forward_tree(cfg, weights, ctx_k, ctx_v, tokens, parents, start_pos, rowwise=True):
+    """Forward one request's token tree (tree verification; SpecPilot digest, "Reasons").
+
+    The pages name tree verification without spelling it out; this is the
+    plain generalisation of the block forward: node i sits at position
+    C + depth(i) and attends to the cached positions and to its own ancestors
+    (root first, itself last), so each node computes exactly what the last
+    row of a block forward over its root-to-node path computes. Returns
+    (logits [n, V], new_k, new_v) indexed by node.
+    """
+    (out,) = forward_blocks(cfg, weights, [(ctx_k, ctx_v, tokens, start_pos, parents)], rowwise)
+    return out
+
+
 def forward_blocks(cfg, weights, requests, rowwise=True, layers_out=None):
     """forward_block for several independent requests, sharing each layer's weights.
 
-    requests: list of (ctx_k, ctx_v, tokens, start_pos); ctx_k / ctx_v only
-    need to support indexing by layer. The layer loop is outermost so a
-    layer's weights are fetched once; each request's arithmetic is exactly
-    that of forward_block (requests never mix). Returns a list of
+    requests: list of (ctx_k, ctx_v, tokens, start_pos) or (ctx_k, ctx_v,
+    tokens, start_pos, parents) for a token tree (see forward_tree); ctx_k /
+    ctx_v only need to support indexing by layer. The layer loop is outermost
+    so a layer's weights are fetched once; each request's arithmetic is
+    exactly that of forward_block (requests never mix). Returns a list of
     (logits, new_k, new_v).
     """
     c = cfg
     state = []
-    for ctx_k, ctx_v, tokens, start_pos in requests:
+    for req in requests:
+        ctx_k, ctx_v, tokens, start_pos = req[:4]
         tokens = np.asarray(tokens, dtype=np.int64)
         m = tokens.shape[0]
-        state.append({"m": m, "pos": start_pos + np.arange(m), "h": weights.embed(tokens), "k": [], "v": [],
+        parents = req[4] if len(req) > 4 and req[4] is not None else [-1] + list(range(m - 1))
+        depth = np.asarray(tree_depths(parents))
+        # block rows row j attends to after the cached keys: its root-to-node path
+        # (for a chain, rows 0 .. j)
+        vis = [tree_path(parents, j) for j in range(m)]
+        state.append({"m": m, "pos": start_pos + depth, "vis": vis, "h": weights.embed(tokens), "k": [], "v": [],
                       "ctx_k": ctx_k, "ctx_v": ctx_v})
     for l in range(c.n_layers):
         p = weights.layer(l)
@@ -212,7 +255,8 @@ def forward_blocks(cfg, weights, requests, rowwise=True, layers_out=None):
             keys = np.concatenate([ck, k], axis=0)
             vals = np.concatenate([cv, v], axis=0)
             n_ctx = ck.shape[0]
-            o = np.stack([attention_row(q[j], keys[:n_ctx + j + 1], vals[:n_ctx + j + 1]) for j in range(m)])
+            rows = [np.concatenate([np.arange(n_ctx), n_ctx + np.asarray(st["vis"][j])]) for j in range(m)]
+            o = np.stack([attention_row(q[j], keys[rows[j]], vals[rows[j]]) for j in range(m)])
             o = o.reshape(m, c.n_heads * c.head_dim)
             h = h + linear(o, p["wo"], rowwise)
             u = rmsnorm(h, p["mlp_norm"], c.rms_eps)

@@ -80,6 +80,40 @@ def commit(st, drafts, new_k, new_v, accepted_len, next_token):
     return st
 
 
+def verify_tree(cfg, weights, st, tokens, parents, rowwise=True):
+    """One greedy tree verify of one request: tokens[0] must be the anchor.
+
+    Returns (accepted_len, next_token, path, logits, new_k, new_v) with the
+    nodes' keys/values indexed by node.
+    """
+    if int(tokens[0]) != st.anchor:
+        raise ValueError("node 0 must hold the anchor")
+    logits, nk, nv = decoder.forward_tree(cfg, weights, st.k, st.v, tokens, parents, st.length, rowwise)
+    k, nxt, path = accept.greedy_accept_tree(logits, tokens, parents)
+    return k, nxt, path, logits, nk, nv
+
+
+def commit_tree(st, tokens, path, new_k, new_v, next_token):
+    """Append the accepted path's keys/values (root first: positions C .. C + k)."""
+    st.k = [np.concatenate([a, b[path]], axis=0) for a, b in zip(st.k, new_k)]
+    st.v = [np.concatenate([a, b[path]], axis=0) for a, b in zip(st.v, new_v)]
+    st.emitted.extend([int(tokens[i]) for i in path[1:]] + [int(next_token)])
+    st.anchor = int(next_token)
+    return st
+
+
+def spec_greedy_tree(cfg, weights, st, drafter, n_steps, rowwise=True):
+    """Speculative greedy loop over token trees; drafter(state) returns (tokens, parents)."""
+    st = st.copy()
+    lens = []
+    for _ in range(n_steps):
+        tokens, parents = drafter(st)
+        k, nxt, path, _, nk, nv = verify_tree(cfg, weights, st, tokens, parents, rowwise)
+        commit_tree(st, tokens, path, nk, nv, nxt)
+        lens.append(k)
+    return st, lens
+
+
 def ar_greedy(cfg, weights, st, n_tokens, rowwise=True):
     """Plain autoregressive greedy decoding: one row per step."""
     st = st.copy()

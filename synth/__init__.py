@@ -128,6 +128,42 @@ def greedy_mix_drafts(greedy, gamma, p, vocab, *stream):
     return np.where(keep, np.asarray(greedy[:gamma], dtype=np.int64), unif)
 
 
+def random_tree(n_nodes, max_children, *stream):
+    """Parents of a random token tree in topological order.
+
+    Node 0 is the root (parent -1); node i > 0 picks its parent uniformly among
+    the earlier nodes that have fewer than max_children children (1: a chain).
+    """
+    g = rng(*stream)
+    parents, kids = [-1], [0]
+    for i in range(1, n_nodes):
+        open_ = [j for j in range(i) if kids[j] < max_children]
+        p = int(open_[int(g.integers(0, len(open_)))])
+        parents.append(p)
+        kids[p] += 1
+        kids.append(0)
+    return np.asarray(parents, dtype=np.int32)
+
+
+def tree_drafts(parents, anchor, greedy, p, vocab, *stream):
+    """Node tokens for a tree: node 0 is the anchor; a node at depth d whose
+    parent's path follows the greedy continuation takes greedy[d-1] with
+    probability p, every other node a uniform token."""
+    g = rng(*stream)
+    tok, on, depth = [int(anchor)], [True], [0]
+    for i in range(1, len(parents)):
+        par = int(parents[i])
+        d = depth[par] + 1
+        depth.append(d)
+        if on[par] and d <= len(greedy) and g.random() < p:
+            t = int(greedy[d - 1])
+        else:
+            t = int(g.integers(0, vocab))
+        tok.append(t)
+        on.append(on[par] and d <= len(greedy) and t == int(greedy[d - 1]))
+    return np.asarray(tok, dtype=np.int64)
+
+
 def truncated_verify_lens(batch, gamma, threshold, *stream):
     """Per request: c_i ~ Beta(8, 2) i.i.d.; keep the drafts while prod_{j<=i} c_j >= threshold.
 

@@ -63,6 +63,16 @@ def classify_greedy(logits, drafts, k_gpu, next_gpu):
     return "mismatch"
 
 
+def classify_tree(logits, tokens, parents, k_gpu, next_gpu, path_gpu):
+    """'match', 'near_tie' or 'mismatch' for one request's greedy tree decision."""
+    k_o, n_o, path_o = accept.greedy_accept_tree(logits, tokens, parents)
+    if (k_o, n_o, path_o) == (int(k_gpu), int(next_gpu), [int(x) for x in path_gpu[:int(k_gpu) + 1]]):
+        return "match"
+    if any(top2_gap(logits[j]) <= MARGIN for j in range(len(tokens))):
+        return "near_tie"
+    return "mismatch"
+
+
 def classify_sampled(logits, drafts, q, temperature, seed, req, start, k_gpu, next_gpu):
     u_acc, u_res = accept.uniforms(seed, req, start, len(drafts))
     k_o, n_o = accept.sampled_accept(logits, drafts, q, temperature, u_acc, u_res)

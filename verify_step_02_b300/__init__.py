@@ -68,6 +68,7 @@ _SIGS = {
     "sv_verify_host": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _f32, _u64, _vp, _vp, _vp, _vp]),
     "sv_model_logits": (_i32, [_vp, _vp, _i32, _vp]),
     "sv_prefill": (_i32, [_vp, _i32, _vp, _vp, ctypes.POINTER(KV), _vp, _vp]),
+    "sv_verify_tree": (_i32, [_vp, _i32, _vp, _vp, _vp, ctypes.POINTER(KV), _vp, _vp, _vp, _vp]),
     "sv_model_sync_status": (_i32, [_vp, _vp]),
     "sv_model_set_timing": (_i32, [_vp, _i32]),
     "sv_model_timing": (_i32, [_vp, _vp, _vp]),
@@ -176,6 +177,13 @@ class Model:
         lens = np.ascontiguousarray(np.asarray(block_lens, dtype=np.int32))
         _check(lib.sv_prefill(self.handle, len(lens), _ptr(tokens), lens.ctypes.data_as(ctypes.c_void_p),
                               ctypes.byref(kv.struct), _ptr(next_token), _stream(stream)))
+
+    def verify_tree(self, tokens, parents, n_drafts, kv, accepted_len, next_token, accepted_nodes, stream=None):
+        """Greedy token-tree verify: tokens, parents, outputs device tensors; n_drafts host ints."""
+        n = np.ascontiguousarray(np.asarray(n_drafts, dtype=np.int32))
+        _check(lib.sv_verify_tree(self.handle, len(n), _ptr(tokens), _ptr(parents), n.ctypes.data_as(ctypes.c_void_p),
+                                  ctypes.byref(kv.struct), _ptr(accepted_len), _ptr(next_token),
+                                  _ptr(accepted_nodes), _stream(stream)))
 
     def verify_host(self, tokens, verify_lens, kv, draft_probs=None, temperature=0.0, seed=0, request_ids=None,
                     stream=None, out=None):

@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
       const int rho = idx / KT, i = idx - rho * KT;
       const int key = kt0 + i, j = rho / group;
       float sc = -INFINITY;
-      if (key < kend && key <= C + j && pages[(key - kbeg) / a.page_size] >= 0) {
+      // (a token tree row sees, of the block, only its ancestors and itself)
+      if (key < kend && key <= C + j && pages[(key - kbeg) / a.page_size] >= 0 &&
+          (!a.row_anc || key < C || ((a.row_anc[row0 + j] >> (key - C)) & 1ull))) {
         const float4* q = reinterpret_cast<const float4*>(Qs + rho * hd);
         const float4* k = reinterpret_cast<const float4*>(kb + i * LD);
         float acc = 0.f;

@@ -377,6 +377,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int rho = lg * 32 + lane;
     const bool live = rho < R;
     const int lim = live ? C + j0 + rho / group : -1;  // last key this row may see
+    // a token tree row sees, of the block keys, only its ancestors and itself (node < 64)
+    const bool tree = a.row_anc != nullptr;
+    const unsigned long long anc = tree && live ? a.row_anc[row0 + j0 + rho / group] : 0ull;
     const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t to = tO + set * HD;
     const uint32_t tp = tP + set * 64 + lane_base;  // this row's P columns (set's hi at +0, lo at +32)
@@ -426,7 +429,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const bool vis = kb + i <= lim && ((vmask >> (2 * hf + (i >> 4))) & 1u);
+            const bool vis = kb + i <= lim && ((vmask >> (2 * hf + (i >> 4))) & 1u) &&
+                             (!tree || kb + i < C || ((anc >> (kb + i - C)) & 1ull));
             v[i] = vis ? v[i] : -INFINITY;
             mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
           }

@@ -49,14 +49,16 @@ __device__ __forceinline__ void token_data(const Epi& e, int m, float& rs, int& 
   if (e.kind == kEpiQkv) {
     pos = e.row_pos[m];
     if (pos >= 0) {
-      const int r = e.row_req[m], pidx = pos / e.page_size;
+      // the KV slot: the position, or for a token tree node C + its index
+      const int slot = e.row_slot ? e.row_slot[m] : pos;
+      const int r = e.row_req[m], pidx = slot / e.page_size;
       const int page = pidx < e.max_pages ? e.page_table[static_cast<long long>(r) * e.max_pages + pidx] : -1;
       if (pidx >= e.max_pages)
         atomicOr(e.status, kStNoPage);
       else if (page < 0 || page >= e.n_pages)
         atomicOr(e.status, kStBadPage);
       else
-        kvo = static_cast<long long>(page) * e.n_kv_heads * e.page_size + (pos - pidx * e.page_size);
+        kvo = static_cast<long long>(page) * e.n_kv_heads * e.page_size + (slot - pidx * e.page_size);
     }
   }
 }

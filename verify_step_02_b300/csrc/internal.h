@@ -27,7 +27,12 @@ enum : uint32_t {
   kStTimeout = 8u,
   kStBadPos = 16u,
   kStNoPage = 32u,
+  kStBadTree = 64u,       // a token tree node whose parent does not precede it
 };
+
+// Token trees (sv_verify_tree): nodes per request, so that a node's ancestors
+// fit one 64-bit mask.
+constexpr int kMaxTreeNodes = 64;
 
 enum EpiKind : int {
   kEpiStore = 0,   // y[m][n] = value                                  (sv_linear)
@@ -61,7 +66,8 @@ struct Epi {
   int ldy;
   // kEpiQkv
   const int* row_req;      // [M] request of each row
-  const int* row_pos;      // [M] absolute position of each row
+  const int* row_pos;      // [M] absolute position of each row (RoPE)
+  const int* row_slot;     // [M] KV slot of each row (token tree: C + node), or nullptr: the position
   const float2* rope;      // [max_seq_len][head_dim/2] (cos, sin)
   int n_heads, n_kv_heads, head_dim;
   float* q_out;            // [M][n_heads*head_dim], float32
@@ -179,6 +185,8 @@ struct AttnArgs {
   int n_pages;
   const int* seq_len;      // [B] committed context C_r (before commit)
   const int* req_row0;     // [B+1] first block row of each request
+  const unsigned long long* row_anc;  // [M] token tree: bit i set = the request's block row i is visible
+                                      // (the row's ancestors and itself); nullptr: causal
   int n_heads, n_kv_heads, head_dim;
   int chunk;               // keys per work item
   int max_chunks;
@@ -217,6 +225,29 @@ struct AcceptArgs {
   unsigned* status;
   int pdl;
   int commit_all;          // prefill: every row is committed and next_token = argmax of the last row
+  const int* parents;      // token tree: [B][gamma_stride] parent of each node (greedy only), or nullptr
+  int* accepted_nodes;     // token tree: [B][gamma_stride] out, the accepted path's nodes, root first
+};
+
+// Token tree commit: move the accepted path's keys and values from their
+// nodes' slots C + node to C + depth (layers [l0, l0 + n) of one launch).
+constexpr int kCompactLayers = 64;
+struct CompactArgs {
+  int B;
+  int gamma_stride;
+  const int* seq_len;         // [B] after the commit (C + accepted_len + 1)
+  const int* accepted_len;    // [B]
+  const int* accepted_nodes;  // [B][gamma_stride]
+  const int* page_table;
+  int max_pages;
+  int page_size;
+  int n_pages;
+  int row_bytes;              // bytes of one position of one kv head (head_dim x element size)
+  int n_kv_heads;
+  int n;                      // layers in this launch
+  void* k[kCompactLayers];
+  void* v[kCompactLayers];
+  int pdl;
 };
 
 struct PrepParams {
@@ -224,6 +255,7 @@ struct PrepParams {
   int B;
   int M;
   int gamma_stride;
+  const int* parents;      // token tree: [B][gamma_stride] parent of each node, or nullptr (chain)
   int req_row0[kMaxBatch + 1];
 };
 
@@ -302,11 +334,13 @@ cudaError_t launch_attention(const AttnArgs& a, int B, int kv_dtype_bf16, cudaSt
 void plan_attention(AttnArgs& a, int max_batch, int max_seq_len, int max_gamma);
 size_t attention_partial_floats(const AttnArgs& a, int max_batch);
 // prep: weights_bf16 selects the embedding and gain type; x_pair the u output form.
+// With p.parents (a token tree) it also writes each row's KV slot and ancestor mask.
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
-                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
-                        float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16, int x_pair,
-                        unsigned* status, cudaStream_t s);
+                        int* row_slot, unsigned long long* row_anc, int* req_row0_dev, const void* embed,
+                        const void* gain, float* h, void* u, long long u_plane, float* ss, int n_ss, int d, int vocab,
+                        int max_seq_len, int weights_bf16, int x_pair, unsigned* status, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+cudaError_t launch_compact(const CompactArgs& a, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_w12_scan(const uint16_t* bf16, long long n, int base, unsigned* stats, cudaStream_t s);
 // W12 planes: 64-row x 128-element tiles of 4096 bytes (see sv.h).

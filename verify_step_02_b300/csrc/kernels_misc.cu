@@ -13,12 +13,15 @@ constexpr int kNormThreads = 256;
 // tensor h * g (the first layer's attention-norm gain) with the row's sum of
 // squares in ss[m][0] (the other tiles' slots zero): the QKV epilogue turns
 // that into the RMSNorm scale.
-__global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, const int* tokens, const int* seq_len,
-                                                            int* row_req, int* row_pos, int* req_row0_dev,
-                                                            const void* embed, const void* gain, float* h, void* u,
-                                                            long long u_plane, float* ss, int n_ss, int d, int vocab,
-                                                            int max_seq_len, int weights_bf16, int x_pair,
-                                                            unsigned* status) {
+//
+// A token tree (p.parents): row j of request r is node j; its RoPE position
+// is C + depth(j), its KV slot C + j, and row_anc[m] has bit i set for every
+// node i on the path from the root to node j (the block keys it may see).
+__global__ void __launch_bounds__(kNormThreads)
+    prep_kernel(const PrepParams p, const int* tokens, const int* seq_len, int* row_req, int* row_pos, int* row_slot,
+                unsigned long long* row_anc, int* req_row0_dev, const void* embed, const void* gain, float* h, void* u,
+                long long u_plane, float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16,
+                int x_pair, unsigned* status) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
@@ -37,15 +40,38 @@ __global__ void __launch_bounds__(kNormThreads) prep_kernel(const PrepParams p, 
     tok = 0;
   }
   if (threadIdx.x == 0) {
+    int depth = j;
+    if (p.parents) {
+      // walk to the root (parents strictly decrease: at most j steps); a bad
+      // parent is flagged and the node treated as a chain row
+      const int* par = p.parents + static_cast<long long>(r) * p.gamma_stride;
+      unsigned long long anc = 1ull << j;
+      depth = 0;
+      for (int i = j; i > 0;) {
+        const int q = par[i];
+        if (q < 0 || q >= i) {
+          atomicOr(status, kStBadTree);
+          depth = j;
+          anc = (2ull << j) - 1ull;
+          break;
+        }
+        anc |= 1ull << q;
+        i = q;
+        ++depth;
+      }
+      row_anc[m] = anc;
+    }
     // a row past the RoPE table / page budget gets position -1: the QKV
     // epilogue then writes nothing for it and the status word records it
-    int pos = seq_len[r] + j;
-    if (seq_len[r] < 0 || pos >= max_seq_len) {
+    const int C = seq_len[r];
+    int pos = C + depth, slot = C + j;  // (slot >= pos)
+    if (C < 0 || slot >= max_seq_len) {
       atomicOr(status, kStBadPos);
-      pos = -1;
+      pos = slot = -1;
     }
     row_req[m] = r;
     row_pos[m] = pos;
+    if (row_slot) row_slot[m] = slot;
   }
   float* hrow = h + (long long)m * d;
   float sq = 0.f;
@@ -147,11 +173,41 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
       if (lane == 0) s_targ[j] = bi;
     }
     __syncthreads();
-    if (a.commit_all)
-      k = L;  // prefill: the block is the prompt itself
-    else
-      while (k < L && toks[1 + k] == s_targ[k]) ++k;
-    next = s_targ[k];
+    if (a.parents) {
+      // token tree: node i is correct when its token is the target's greedy
+      // token after its parent; the accepted path ends at the deepest node
+      // whose every non-root ancestor and itself are correct (lowest index
+      // among equally deep ones)
+      if (tid == 0) {
+        const int* par = a.parents + static_cast<long long>(r) * a.gamma_stride;
+        unsigned long long okm = 1ull;  // bit i: node i accepted
+        int depth[kMaxTreeNodes];
+        depth[0] = 0;
+        int end = 0;
+        for (int i = 1; i <= L && i < kMaxTreeNodes; ++i) {
+          const int q = par[i];
+          const bool valid = q >= 0 && q < i;  // (a bad parent was flagged by the row preparation)
+          depth[i] = valid ? depth[q] + 1 : 0;
+          if (valid && ((okm >> q) & 1ull) && toks[i] == s_targ[q]) {
+            okm |= 1ull << i;
+            if (depth[i] > depth[end]) end = i;
+          }
+        }
+        k = depth[end];
+        next = s_targ[end];
+        int* out = a.accepted_nodes + static_cast<long long>(r) * a.gamma_stride;
+        for (int i = end, dd = k; dd >= 0; --dd) {
+          out[dd] = i;
+          i = dd > 0 ? par[i] : 0;
+        }
+      }
+    } else {
+      if (a.commit_all)
+        k = L;  // prefill: the block is the prompt itself
+      else
+        while (k < L && toks[1 + k] == s_targ[k]) ++k;
+      next = s_targ[k];
+    }
   } else {
     const float invT = 1.0f / a.temperature;
     const long long req = a.request_ids ? a.request_ids[r] : r;
@@ -198,6 +254,49 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptArgs a)
     a.accepted_len[r] = k;
     a.next_token[r] = next;
     a.seq_len[r] = C + k + 1;  // commit the anchor and the accepted drafts
+  }
+}
+
+// ------------------------------------------------------------------ tree commit
+constexpr int kCompactThreads = 256;
+
+// One CTA per (request, layer): for d = 1 .. k the accepted path's node p_d
+// moves from slot C + p_d to slot C + d (p_d >= d, so in increasing d no
+// source is overwritten before it is read: a slot C + e is written at step e
+// and read, if at all, at the step d < e whose node is e). Each thread moves
+// the same 16-byte pieces at every step, so its own program order keeps
+// every read of a slot before the later write of it.
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x, l = blockIdx.y;
+  const int k = a.accepted_len[r];
+  const int C = a.seq_len[r] - k - 1;
+  if (k <= 0 || k >= kMaxTreeNodes || C < 0) return;
+  const int* path = a.accepted_nodes + static_cast<long long>(r) * a.gamma_stride;
+  const int* ptab = a.page_table + static_cast<long long>(r) * a.max_pages;
+  const int pieces = a.row_bytes / 16;  // per kv head
+  const int n = pieces * a.n_kv_heads;
+  uint8_t* pools[2] = {static_cast<uint8_t*>(a.k[l]), static_cast<uint8_t*>(a.v[l])};
+  // byte offset of (slot, kv head 0) in a pool, or -1 for a slot without a valid page
+  auto slot_off = [&](int slot) -> long long {
+    const int pidx = slot / a.page_size;
+    const int page = pidx < a.max_pages ? ptab[pidx] : -1;
+    if (page < 0 || page >= a.n_pages) return -1;
+    return ((static_cast<long long>(page) * a.n_kv_heads) * a.page_size + (slot - pidx * a.page_size)) * a.row_bytes;
+  };
+  for (int dd = 1; dd <= k; ++dd) {
+    const int node = path[dd];
+    if (node == dd) continue;
+    if (node < dd || node >= kMaxTreeNodes) return;
+    const long long src = slot_off(C + node), dst = slot_off(C + dd);
+    if (src < 0 || dst < 0) return;
+    for (int i = threadIdx.x; i < 2 * n; i += kCompactThreads) {
+      const int pool = i >= n, e = i - pool * n, h = e / pieces, piece = e - h * pieces;
+      const long long ho = static_cast<long long>(h) * a.page_size * a.row_bytes + piece * 16;
+      const uint4 v = *reinterpret_cast<const uint4*>(pools[pool] + src + ho);
+      *reinterpret_cast<uint4*>(pools[pool] + dst + ho) = v;
+    }
   }
 }
 
@@ -295,16 +394,20 @@ __global__ void philox_kernel(unsigned long long seed, long long req, long long 
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& p, const int* tokens, const int* seq_len, int* row_req, int* row_pos,
-                        int* req_row0_dev, const void* embed, const void* gain, float* h, void* u, long long u_plane,
-                        float* ss, int n_ss, int d, int vocab, int max_seq_len, int weights_bf16, int x_pair,
-                        unsigned* status, cudaStream_t s) {
+                        int* row_slot, unsigned long long* row_anc, int* req_row0_dev, const void* embed,
+                        const void* gain, float* h, void* u, long long u_plane, float* ss, int n_ss, int d, int vocab,
+                        int max_seq_len, int weights_bf16, int x_pair, unsigned* status, cudaStream_t s) {
   return launch_k(prep_kernel, dim3(p.M), dim3(kNormThreads), 0, s, p.pdl != 0, p, tokens, seq_len, row_req, row_pos,
-                  req_row0_dev, embed, gain, h, u, u_plane, ss, n_ss, d, vocab, max_seq_len, weights_bf16, x_pair,
-                  status);
+                  row_slot, row_anc, req_row0_dev, embed, gain, h, u, u_plane, ss, n_ss, d, vocab, max_seq_len,
+                  weights_bf16, x_pair, status);
 }
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
   return launch_k(accept_kernel, dim3(a.B), dim3(kAccThreads), 0, s, a.pdl != 0, a);
+}
+
+cudaError_t launch_compact(const CompactArgs& a, cudaStream_t s) {
+  return launch_k(compact_kernel, dim3(a.B, a.n), dim3(kCompactThreads), 0, s, a.pdl != 0, a);
 }
 
 cudaError_t launch_rope_table(float2* table, int max_seq_len, int head_dim, float theta, cudaStream_t s) {

@@ -73,6 +73,8 @@ struct sv_model {
   float2* argmax_part = nullptr;
   int* row_req = nullptr;
   int* row_pos = nullptr;
+  int* row_slot = nullptr;             // token trees: KV slot of each row
+  unsigned long long* row_anc = nullptr;  // token trees: visible block rows of each row
   int* req_row0 = nullptr;
   float2* rope = nullptr;
   float* gemm_part = nullptr;
@@ -294,7 +296,8 @@ sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair
 
 sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, const sv_kv* kv, const float* probs,
                      float T, uint64_t seed, const long long* req_ids, int* acc_len, int* next_tok,
-                     cudaStream_t s, bool commit_all = false) {
+                     cudaStream_t s, bool commit_all = false, const int* parents = nullptr,
+                     int* acc_nodes = nullptr) {
   const sv_config& c = m->cfg;
   if (B < 1 || B > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", B, c.max_batch);
   if (!tokens || !lens || !kv || !acc_len || !next_tok) return fail(SV_ERR_INVALID_ARG, "NULL argument");
@@ -309,6 +312,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   p.B = B;
   p.pdl = m->use_pdl;
   p.gamma_stride = c.max_gamma + 1;
+  p.parents = parents;
   p.req_row0[0] = 0;
   for (int r = 0; r < B; ++r) {
     if (lens[r] < 0 || lens[r] > c.max_gamma)
@@ -322,7 +326,8 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
   const bool keep = T > 0.f || (c.flags & SV_FLAG_KEEP_LOGITS);
   {
     Timed t(m, SV_KC_NORM, s);
-    SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, m->req_row0, m->w.embed,
+    SV_CUDA(launch_prep(p, tokens, kv->seq_len, m->row_req, m->row_pos, parents ? m->row_slot : nullptr,
+                        m->row_anc, m->req_row0, m->w.embed,
                         m->layers[0].attn_norm, m->h, m->u, m->u_plane, m->ss, m->n_ss, d, c.vocab, c.max_seq_len,
                         m->wbf16, m->x_pair, m->status, s),
             "prep");
@@ -334,6 +339,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.epi.kind = kEpiQkv;
       a.epi.row_req = m->row_req;
       a.epi.row_pos = m->row_pos;
+      a.epi.row_slot = parents ? m->row_slot : nullptr;
       a.epi.rope = m->rope;
       a.epi.n_heads = c.n_heads;
       a.epi.n_kv_heads = c.n_kv_heads;
@@ -369,6 +375,7 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
       a.n_pages = kv->n_pages;
       a.seq_len = kv->seq_len;
       a.req_row0 = m->req_row0;
+      a.row_anc = parents ? m->row_anc : nullptr;
       a.n_heads = c.n_heads;
       a.n_kv_heads = c.n_kv_heads;
       a.head_dim = hd;
@@ -471,8 +478,36 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
     a.status = m->status;
     a.pdl = m->use_pdl;
     a.commit_all = commit_all ? 1 : 0;
+    a.parents = parents;
+    a.accepted_nodes = acc_nodes;
     Timed t(m, SV_KC_ACCEPT, s);
     SV_CUDA(launch_accept(a, s), "accept");
+  }
+  if (parents) {
+    // token tree: the accepted path's keys and values move to positions C .. C + k
+    CompactArgs a;
+    memset(&a, 0, sizeof a);
+    a.B = B;
+    a.gamma_stride = c.max_gamma + 1;
+    a.seq_len = kv->seq_len;
+    a.accepted_len = acc_len;
+    a.accepted_nodes = acc_nodes;
+    a.page_table = kv->page_table;
+    a.max_pages = kv->max_pages_per_seq;
+    a.page_size = c.page_size;
+    a.n_pages = kv->n_pages;
+    a.row_bytes = hd * (m->wbf16 ? 2 : 4);
+    a.n_kv_heads = c.n_kv_heads;
+    a.pdl = m->use_pdl;
+    Timed t(m, SV_KC_ACCEPT, s);
+    for (int l0 = 0; l0 < c.n_layers; l0 += kCompactLayers) {
+      a.n = std::min(kCompactLayers, c.n_layers - l0);
+      for (int i = 0; i < a.n; ++i) {
+        a.k[i] = kv->k[l0 + i];
+        a.v[i] = kv->v[l0 + i];
+      }
+      SV_CUDA(launch_compact(a, s), "tree commit");
+    }
   }
   m->last_logits = keep;
   m->last_m = M;
@@ -541,6 +576,8 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   TRY(dalloc(m, &m->argmax_part, sizeof(float2) * M * (size_t)m->lm_tiles));
   TRY(dalloc(m, &m->row_req, sizeof(int) * M));
   TRY(dalloc(m, &m->row_pos, sizeof(int) * M));
+  TRY(dalloc(m, &m->row_slot, sizeof(int) * M));
+  TRY(dalloc(m, &m->row_anc, sizeof(unsigned long long) * M));
   TRY(dalloc(m, &m->req_row0, sizeof(int) * (c.max_batch + 1)));
   TRY(dalloc(m, &m->rope, sizeof(float2) * (size_t)c.max_seq_len * (c.head_dim / 2)));
   size_t part = 0, cnt = 0;
@@ -691,6 +728,21 @@ sv_status sv_prefill(sv_model* model, int32_t batch, const int32_t* tokens, cons
                     static_cast<cudaStream_t>(stream), true);
 }
 
+sv_status sv_verify_tree(sv_model* model, int32_t batch, const int32_t* tokens, const int32_t* parents,
+                         const int32_t* n_drafts, const sv_kv* kv, int32_t* accepted_len, int32_t* next_token,
+                         int32_t* accepted_nodes, void* stream) {
+  if (!model) return fail(SV_ERR_INVALID_ARG, "model is NULL");
+  if (!parents || !n_drafts || !accepted_nodes) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  const sv_config& c = model->cfg;
+  if (batch < 1 || batch > c.max_batch) return fail(SV_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, c.max_batch);
+  const int lim = std::min(c.max_gamma, kMaxTreeNodes - 1);
+  for (int r = 0; r < batch; ++r)
+    if (n_drafts[r] < 0 || n_drafts[r] > lim)
+      return fail(SV_ERR_INVALID_ARG, "n_drafts[%d] = %d outside 0..%d", r, n_drafts[r], lim);
+  return run_verify(model, batch, tokens, n_drafts, kv, nullptr, 0.f, 0, nullptr, accepted_len, next_token,
+                    static_cast<cudaStream_t>(stream), false, parents, accepted_nodes);
+}
+
 sv_status sv_model_logits(sv_model* model, float* dst, int32_t rows, void* stream) {
   if (!model || !dst) return fail(SV_ERR_INVALID_ARG, "NULL argument");
   if (!model->last_logits) return fail(SV_ERR_INVALID_ARG, "the last verify kept no logits");
@@ -712,12 +764,13 @@ sv_status sv_model_sync_status(sv_model* model, void* stream) {
   if (word) {
     // a block that only overran its KV capacity is SV_ERR_KV_CAPACITY; anything else a failed check
     const bool capacity_only = (word & ~(kStBadPos | kStNoPage)) == 0;
-    return fail(capacity_only ? SV_ERR_KV_CAPACITY : SV_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s%s%s",
+    return fail(capacity_only ? SV_ERR_KV_CAPACITY : SV_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s%s%s%s",
                 (word & kStBadToken) ? " token id out of range" : "", (word & kStBadPage) ? " page id out of range" : "",
                 (word & kStTimeout) ? " wait timed out" : "",
                 (word & kStBadPos) ? " a block position reaches max_seq_len" : "",
                 (word & kStNoPage) ? " a block position is past the request's page table" : "",
-                (word & kStBadDraftProb) ? " bad draft probability" : "");
+                (word & kStBadDraftProb) ? " bad draft probability" : "",
+                (word & kStBadTree) ? " a tree node's parent does not precede it" : "");
   }
   return SV_OK;
 }
