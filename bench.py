@@ -932,6 +932,22 @@ def run_workload(args, world, rank, local):
     tim = model.timing()
     model.set_timing(False)
     clk = clocks.stop()
+    trace = None
+    if args.trace:  # device timeline of two more steps
+        n_layers = shape["n_layers"]
+        cap = 2 * (n_layers * (4 * 148 + 2 * 148) + 2 * 148)
+        recs = torch.zeros((cap, 16), dtype=torch.int64, device="cuda")
+        model.set_trace(recs)
+        for j in range(2):
+            run(args.warmup + args.steps + j)
+        torch.cuda.synchronize()
+        launches = model.trace_launches()
+        model.set_trace(None)
+        raw = recs.cpu().numpy().view(np.uint64)
+        trace = trace_summary(raw, launches, n_layers)
+        if args.trace_out:
+            np.savez_compressed(args.trace_out, records=raw, launches=np.array([l[:2] for l in launches]),
+                                kinds=np.array([l[2] for l in launches]))
     per_step = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
     t_ms = ev[0].elapsed_time(ev[-1])
     tokens = float((seq_end - seq_start).sum())  # accepted drafts + 1 per request per step
@@ -960,6 +976,7 @@ def run_workload(args, world, rank, local):
                 "peak_kind": peak_kind, "bound_ms": round(step_alg / (peak * 1e9) * 1e3, 4)},
         "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in tim.items()},
         "clocks": clk,
+        **({"trace": trace} if trace else {}),
     }
 
 

@@ -102,11 +102,30 @@ __device__ __forceinline__ uint32_t sw128(int row, int ch) {
   return static_cast<uint32_t>(row) * 128u + static_cast<uint32_t>((ch ^ (row & 7)) * 16);
 }
 
-template <int HD>
+// N consecutive TMEM columns of this thread's lane (N = 32, 16, 8).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
+  if constexpr (N == 32) tmem_ld32(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else tmem_ld8(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* v) {
+  if constexpr (N == 16) tmem_st16u(taddr, v);
+  else if constexpr (N == 8) tmem_st8u(taddr, v);
+  else tmem_st4u(taddr, v);
+}
+
+template <int HD, int QC>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const AttnArgs a) {
   constexpr int NH = HD / 64;                     // 64-dim halves of a head
+  // QC copies of the tile's query rows fill the 128 MMA rows (QL lanes each);
+  // copy c takes keys [c 64 / QC, (c + 1) 64 / QC) of every sub-chunk, so each
+  // softmax warp (two per TMEM lane group and set) handles NKW keys per row
+  constexpr int QL = 128 / QC;
+  constexpr int NKW = 32 / QC;
   constexpr uint32_t QB = 2 * NH * kTile;         // Q: hi and lo planes, NH halves of 128 rows x 128 B
   constexpr uint32_t KT = kSub * 128;             // a half-head tile of one sub-chunk: 64 keys x 128 B
   constexpr uint32_t KVB = 2 * NH * KT;           // one stage: K (NH halves), then V (NH halves)
@@ -248,15 +267,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       pdl_wait();
       pdl_trigger();
       if (lane == 0) {
+        // QC copies of the tile's rows, at MMA rows 0, QL, ..
         const uint32_t qbox = 128u * group * a.q_rows;
-        mbar_arrive_expect_tx(q_full, 2 * NH * qbox);
+        mbar_arrive_expect_tx(q_full, 2 * NH * qbox * QC);
         const uint64_t polq = policy_evict_last();
 #pragma unroll
-        for (int pl = 0; pl < 2; ++pl)
+        for (int cp = 0; cp < QC; ++cp)
 #pragma unroll
-          for (int hh = 0; hh < NH; ++hh)
-            tma_load_3d(smem + (pl * NH + hh) * kTile, &tmq, hh * 64, h * group, pl * a.q_lo_row + row0 + j0,
-                        q_full, polq);
+          for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh)
+              tma_load_3d(smem + (pl * NH + hh) * kTile + cp * QL * 128, &tmq, hh * 64, h * group,
+                          pl * a.q_lo_row + row0 + j0, q_full, polq);
       }
     };
     if (n_early == nsub) load_q();  // (then every sub-chunk is early: the query first)
@@ -371,15 +393,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ------------------------------------------------------------ rows: softmax, output
     // set = warp / 8 takes sub-chunks j = set (mod 2); warp w reads TMEM lanes
-    // 32 (w % 4) ..; one thread per row rho and key half hf = (w / 4) mod 2:
-    // keys 32 hf .. 32 hf + 31 of each of the set's sub-chunks
+    // 32 (w % 4) ..; one thread per TMEM lane rho (copy cp, tile row `row`) and
+    // key half hf = (w / 4) mod 2 of the copy's keys: NKW keys from kk0 of each
+    // of the set's sub-chunks
     const int set = warp >> 3, lg = warp & 3, hf = (warp >> 2) & 1;
     const int rho = lg * 32 + lane;
-    const bool live = rho < R;
-    const int lim = live ? C + j0 + rho / group : -1;  // last key this row may see
+    const int cp = rho / QL, row = rho - cp * QL;
+    const int kk0 = cp * (64 / QC) + hf * NKW;
+    const bool live = row < R;
+    const int lim = live ? C + j0 + row / group : -1;  // last key this row may see
     // a token tree row sees, of the block keys, only its ancestors and itself (node < 64)
     const bool tree = a.row_anc != nullptr;
-    const unsigned long long anc = tree && live ? a.row_anc[row0 + j0 + rho / group] : 0ull;
+    const unsigned long long anc = tree && live ? a.row_anc[row0 + j0 + row / group] : 0ull;
     const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t to = tO + set * HD;
     const uint32_t tp = tP + set * 64 + lane_base;  // this row's P columns (set's hi at +0, lo at +32)
@@ -391,7 +416,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float m = -INFINITY, l = 0.f;  // this set's running maximum; this warp's part of the sum
     bool ok = true;
     // a warp whose 32 rows are all padding only keeps the handshakes
-    const bool idle = lg * 32 >= R;
+    const bool idle = lg * 32 - (lg * 32 / QL) * QL >= R;
+    if (QC > 1) {
+      // a lane's P row holds only its copy's keys: the other columns stay zero
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.f;
+      tmem_st32(tP + set * 64 + (static_cast<uint32_t>(lg * 32) << 16) + hf * 32, z);
+    }
     constexpr float kLog2e = 1.4426950408889634f;
     for (int j = set; j < nsub; j += 2) {
       const int st = j % kStages;
@@ -408,8 +440,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       const uint32_t vmask = vmask_s[st];
-      const int kb = k0 + j * kSub + hf * 32;  // first key of this warp's half
-      float v[32];
+      const int kb = k0 + j * kSub + kk0;  // first key of this warp's slice
+      float v[NKW];
       float corr = 1.f;
       if (!idle) {
         // both warps of the row reach the pair barrier, and leave together if either failed
@@ -420,16 +452,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        tmem_ld32(tS + lane_base + set * kSub + hf * 32, v);
+        tmem_ld_cols<NKW>(tS + lane_base + set * kSub + kk0, v);
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (kb + 31 <= C && ((vmask >> (2 * hf)) & 3u) == 3u) {
+        constexpr uint32_t pgm = NKW >= 16 ? (1u << (NKW / 16)) - 1u : 1u;  // the slice's pages
+        if (kb + NKW - 1 <= C && ((vmask >> (kk0 >> 4)) & pgm) == pgm) {
           // every key is cached context on a loaded page: no mask
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
+          for (int i = 0; i < NKW; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const bool vis = kb + i <= lim && ((vmask >> (2 * hf + (i >> 4))) & 1u) &&
+          for (int i = 0; i < NKW; ++i) {
+            const bool vis = kb + i <= lim && ((vmask >> ((kk0 + i) >> 4)) & 1u) &&
                              (!tree || kb + i < C || ((anc >> (kb + i - C)) & 1ull));
             v[i] = vis ? v[i] : -INFINITY;
             mx4[i & 3] = fmaxf(mx4[i & 3], v[i]);
@@ -452,7 +485,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float ml2 = m == -INFINITY ? 0.f : m * kLog2e;
         float lp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < NKW; ++i) {
           v[i] = ex2_approx(fmaf(v[i], kLog2e, -ml2));
           lp4[i & 3] += v[i];
         }
@@ -464,17 +497,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
       }
       if (!idle) {
-        // P_j row rho into TMEM: keys 32 hf + 2 i and + 1 in column 16 hf + i (hi and lo)
-        uint32_t ph[16], pl[16];
+        // P_j row rho into TMEM: keys kk0 + 2 i and + 1 in column kk0 / 2 + i (hi, and lo 32 columns on)
+        uint32_t ph[NKW / 2], pl[NKW / 2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < NKW / 8; ++q) {
           uint4 hi, lo;
           split8(v + 8 * q, hi, lo);
           ph[4 * q] = hi.x, ph[4 * q + 1] = hi.y, ph[4 * q + 2] = hi.z, ph[4 * q + 3] = hi.w;
           pl[4 * q] = lo.x, pl[4 * q + 1] = lo.y, pl[4 * q + 2] = lo.z, pl[4 * q + 3] = lo.w;
         }
-        tmem_st16u(tp + hf * 16, ph);
-        tmem_st16u(tp + 32 + hf * 16, pl);
+        tmem_st_cols<NKW / 2>(tp + kk0 / 2, ph);
+        tmem_st_cols<NKW / 2>(tp + 32 + kk0 / 2, pl);
       }
       if (j >= set + 2 && __any_sync(0xffffffffu, corr != 1.f)) {
         // this warp rescales O_set's dims hf * HD / 2 .. + HD / 2
@@ -557,51 +590,59 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (CS > 1) cluster_sync();
   if (tid == 0) trace_mark(rec, 8);
   {
-    // rank i merges rows [i rpr, (i + 1) rpr) of the CS partials: first each row's
-    // weights e^(m_c - M) / sum_c l_c e^(m_c - M) (one thread per row, into the
-    // free P buffers), then the output rows, 4 dims per item
+    // rank i merges rows [i rpr, (i + 1) rpr) of the NP = CS QC partials (rank k,
+    // copy c: lane c QL + row of rank k): first each row's weights
+    // e^(m_p - M) / sum_p l_p e^(m_p - M) (one thread per row), then the output
+    // rows, 4 dims per item
+    constexpr int NPMAX = kMaxCluster * QC;
+    const int NP = CS * QC;
     const int rpr = (R + CS - 1) / CS;
     const int rr0 = rank * rpr, rr1 = rr0 + rpr < R ? rr0 + rpr : R;
     const uint32_t os_addr = smem_u32(Os), ml_addr = smem_u32(ML);
-    float* wts = reinterpret_cast<float*>(smem + WTS_OFF);    // [rpr][kMaxCluster]
-    float2* mls = reinterpret_cast<float2*>(smem + MLS_OFF);  // [rpr][kMaxCluster]
+    float* wts = reinterpret_cast<float*>(smem + WTS_OFF);    // [rpr][NP]
+    float2* mls = reinterpret_cast<float2*>(smem + MLS_OFF);  // [rpr][NP]
     const int nrr = rr1 - rr0;
-    // every rank's (m, l) of this rank's rows, all loads in flight
-    for (int it = tid; it < nrr * CS; it += kAttnThreads) {
-      const int rr = it / CS, k = it - rr * CS;
-      mls[rr * kMaxCluster + k] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * (rr0 + rr), static_cast<uint32_t>(k)));
+    // every partial's (m, l) of this rank's rows, all loads in flight
+    for (int it = tid; it < nrr * NP; it += kAttnThreads) {
+      const int rr = it / NP, p = it - rr * NP;
+      const uint32_t ln = static_cast<uint32_t>((p % QC) * QL + rr0 + rr);
+      mls[rr * NP + p] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * ln, static_cast<uint32_t>(p / QC)));
     }
     __syncthreads();
     for (int rr = tid; rr < nrr; rr += kAttnThreads) {
       float M = -INFINITY;
-      for (int k = 0; k < CS; ++k) M = fmaxf(M, mls[rr * kMaxCluster + k].x);
+      for (int p = 0; p < NP; ++p) M = fmaxf(M, mls[rr * NP + p].x);
       float L = 0.f;
-      for (int k = 0; k < CS; ++k) {
-        const float2 v = mls[rr * kMaxCluster + k];
+      for (int p = 0; p < NP; ++p) {
+        const float2 v = mls[rr * NP + p];
         const float w = v.x == -INFINITY ? 0.f : __expf(v.x - M);
-        wts[rr * kMaxCluster + k] = w;
+        wts[rr * NP + p] = w;
         L += v.y * w;
       }
       // L = 0 only for rows whose keys were all on bad pages (flagged): output 0
       const float inv = L > 0.f ? 1.0f / L : 0.f;
-      for (int k = 0; k < CS; ++k) wts[rr * kMaxCluster + k] *= inv;
+      for (int p = 0; p < NP; ++p) wts[rr * NP + p] *= inv;
     }
     __syncthreads();
     if (tid == 0) trace_mark(rec, 9);
     constexpr int D4 = HD / 4;
-    constexpr int KB = 8;  // ranks whose O loads are in flight together
+    constexpr int KB = 8;  // partials whose O loads are in flight together
+    static_assert(NPMAX % KB == 0, "partials in groups of KB");
     for (int it = tid; it < nrr * D4; it += kAttnThreads) {
       const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k0 = 0; k0 < CS; k0 += KB) {
+      for (int p0 = 0; p0 < NP; p0 += KB) {
         float4 o[KB];
 #pragma unroll
-        for (int kk = 0; kk < KB; ++kk)
-          if (k0 + kk < CS && wts[rr * kMaxCluster + k0 + kk] != 0.f)
-            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (rho * HD + d), static_cast<uint32_t>(k0 + kk)));
+        for (int kk = 0; kk < KB; ++kk) {
+          const int p = p0 + kk;
+          if (p < NP && wts[rr * NP + p] != 0.f)
+            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (((p % QC) * QL + rho) * HD + d),
+                                               static_cast<uint32_t>(p / QC)));
+        }
 #pragma unroll
         for (int kk = 0; kk < KB; ++kk) {
-          const float w = k0 + kk < CS ? wts[rr * kMaxCluster + k0 + kk] : 0.f;
+          const float w = p0 + kk < NP ? wts[rr * NP + p0 + kk] : 0.f;
           if (w != 0.f) {
             acc.x += o[kk].x * w;
             acc.y += o[kk].y * w;
@@ -629,23 +670,24 @@ size_t attn_tc_smem(int hd) {
   return 1024 + q + kStages * kv + 2 * 2 * 2 * 128 + 4 * 16 + (2 * kStages + 9) * 8 + 32;
 }
 
-template <int HD>
+template <int HD, int QC>
 cudaError_t set_attrs() {
   static bool attr_set[64] = {};  // per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && attr_set[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, QC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(attn_tc_smem(HD)));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<HD, QC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
   return e;
 }
 
-template <int HD>
+template <int HD, int QC>
 cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       cudaStream_t s) {
-  cudaError_t e = set_attrs<HD>();
+  cudaError_t e = set_attrs<HD, QC>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B * a.n_kv_heads * a.n_row_tiles, a.cl_size);
@@ -661,12 +703,12 @@ cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUte
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, q, k, v, a);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, QC>, q, k, v, a);
 }
 
 template <int HD>
 int max_clusters_hd(int cs) {
-  if (set_attrs<HD>() != cudaSuccess) return 0;
+  if (set_attrs<HD, 1>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, cs);
   cfg.blockDim = dim3(kAttnThreads);
@@ -679,7 +721,7 @@ int max_clusters_hd(int cs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD, 1>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -711,10 +753,16 @@ bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_s
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
                                 const CUtensorMap& v, cudaStream_t s) {
-  if (a.cl_size < 1 || a.cl_size > kMaxCluster || a.q_rows < 1 || a.q_rows * (a.n_heads / a.n_kv_heads) > 128 ||
-      a.n_row_tiles < 1 || !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
+  const int qc = a.q_copies;
+  if (a.cl_size < 1 || a.cl_size > kMaxCluster || a.q_rows < 1 || (qc != 1 && qc != 2 && qc != 4) ||
+      a.q_rows * (a.n_heads / a.n_kv_heads) * qc > 128 || a.n_row_tiles < 1 ||
+      !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))
     return cudaErrorInvalidValue;
-  return a.head_dim == 128 ? launch_hd<128>(a, B, q, k, v, s) : launch_hd<64>(a, B, q, k, v, s);
+  if (a.head_dim == 128)
+    return qc == 4 ? launch_hd<128, 4>(a, B, q, k, v, s)
+                   : qc == 2 ? launch_hd<128, 2>(a, B, q, k, v, s) : launch_hd<128, 1>(a, B, q, k, v, s);
+  return qc == 4 ? launch_hd<64, 4>(a, B, q, k, v, s)
+                 : qc == 2 ? launch_hd<64, 2>(a, B, q, k, v, s) : launch_hd<64, 1>(a, B, q, k, v, s);
 }
 
 }  // namespace sv

@@ -189,7 +189,8 @@ size_t gemm_tc_partial_floats(const GemmArgs& a) {
   return static_cast<size_t>(a.grid_p) * 2 * kGemmBN * a.tc_nt;
 }
 
-size_t gemm_tc_counter_count(const GemmArgs& a) { return static_cast<size_t>(a.n_tiles) * a.m_tiles; }
+// per tile: partials stored, then participants done (stream-K reduction)
+size_t gemm_tc_counter_count(const GemmArgs& a) { return 2 * static_cast<size_t>(a.n_tiles) * a.m_tiles; }
 
 bool gemm_tc_supported(int wdtype, int pair, int ffn) {
   // W12 row halves are whole 64-row plane tiles: gate|up needs ffn % 64 == 0

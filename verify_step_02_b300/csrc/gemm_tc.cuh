@@ -11,8 +11,11 @@
 //   stream-K   P <= #SM CTAs share U = tiles x K blocks units; CTA c takes
 //              units [c U / P, (c+1) U / P), so every SM streams the same
 //              bytes. A tile whose K range is shared by several CTAs is
-//              finished by the last of them to arrive, which sums the partial
-//              tiles (in global memory) in CTA order and runs the epilogue.
+//              finished by those of them whose ranges end inside it (the
+//              tile is their last work): once every contributor's partial
+//              tile is in global memory, each sums its own slice of the
+//              tile's tokens in CTA order and runs the slice's epilogue, so
+//              no single SM reads the whole tile's partials.
 //   cluster    (token tiles of at most 64 columns, one weight tile per cluster:
 //              the O and down projections) the CS CTAs of a cluster split the
 //              tile's K blocks evenly. Each rank stores a 1/CS share of its
@@ -92,6 +95,25 @@ struct CtaUnits {
     return e < n ? e : n;
   }
 };
+
+// Spin (bounded, like mbar_wait) until the counter at p reaches `target`; the
+// load has acquire semantics at GPU scope.
+__device__ __forceinline__ int wait_count(const unsigned* p, unsigned target, volatile int* abort, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return 1;
+    if ((i & 15u) == 15u) {
+      if (*abort) return 0;
+      if (global_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return 0;
+      }
+    }
+    __nanosleep(32);
+  }
+}
 
 template <int NT, bool PAIR, bool W12, bool CL>
 __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
           trace_mark(trec, 11);
         }
       } else {
-        // ---- stream-K: partials through global memory, the last arriver sums them
+        // ---- stream-K: partials through global memory, summed in token slices
         const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
         const bool alone = cf == cl;
         const int slot = t == slot0_tile ? 0 : 1;
@@ -582,29 +604,52 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
           mbar_arrive(acc_empty + b);
         }
         if (!alone) {
-          epilogue_prefetch(a, nt, m_base, mtot < 32 ? mtot : 32, et, td);
+          // Hand-off. A tile of one token chunk (at most 32 tokens) is summed by the
+          // last contributor to arrive, so the others leave at once. A wider tile is
+          // shared by its participants, the contributors whose ranges end inside it
+          // (the tile is their last work): cf .. lp, where lp = cl unless cl's range
+          // runs on past the tile. Once every partial is in, each sums its own token
+          // slice, so no single SM reads the whole tile's partials.
+          const bool share = mtot > 32;
+          const int ncon = cl - cf + 1;
+          const long long tend = (t + 1) * a.kb;
+          const int lp = static_cast<long long>(cl + 1) * U / P <= tend ? cl : cl - 1;
+          const bool part = share && static_cast<long long>(c + 1) * U / P <= tend;
+          const int npart = share ? lp - cf + 1 : 1;
+          const int ws = ((mtot + npart - 1) / npart + 3) / 4 * 4;
+          const int s0 = share ? (c - cf) * ws : 0, s1 = share ? (s0 + ws < mtot ? s0 + ws : mtot) : mtot;
+          if (!share || part) epilogue_prefetch(a, nt, m_base + s0, s1 - s0 < 32 ? s1 - s0 : 32, et, td);
           __threadfence();
           sync();
           trace_mark(trec, 8);
-          if (et2 == 0) *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(cl - cf) ? 1 : 0;
+          if (share) {
+            if (et2 == 0) {
+              atomicAdd(a.counters + t, 1u);
+              *s_flag = part ? wait_count(a.counters + t, static_cast<unsigned>(ncon), abort_flag, kWaitNs) : 0;
+            }
+          } else if (et2 == 0) {
+            *s_flag = atomicAdd(a.counters + t, 1u) == static_cast<unsigned>(ncon - 1) ? 1 : 0;
+          }
           sync();
-          const bool last = *s_flag != 0;
+          const bool reduce = *s_flag != 0;
+          sync();
           trace_mark(trec, 9);
-          sync();
-          if (last) {
+          if (reduce) {
             __threadfence();
             // the contributors' slots, in CTA order (a fixed summation order): a
             // tile is the first tile (slot 0) of every contributor after cf, and of
             // cf when cf's range starts at the tile's first unit
-            const int ncon = cl - cf + 1;
             const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
             constexpr int RW = 32 / (EPT / 128);  // columns of a chunk each warpgroup sums
             const int col0 = grpA ? 0 : RW;
             constexpr int NB = W12 ? 1 : 4;  // contributors whose loads are in flight together
-            for (int ch = 0; ch * 32 < mtot; ++ch) {
-              float s[RW];
+            for (int cc = s0; cc < s1; cc += 32) {
+              const int cn = s1 - cc < 32 ? s1 - cc : 32;
+              // the next chunk's epilogue inputs into L1 while this chunk's partials load
+              if (cc + 32 < s1) epilogue_prefetch(a, nt, m_base + cc + 32, s1 - cc - 32 < 32 ? s1 - cc - 32 : 32, et, td);
+              float sm_[RW];
 #pragma unroll
-              for (int k = 0; k < RW; ++k) s[k] = 0.f;
+              for (int k = 0; k < RW; ++k) sm_[k] = 0.f;
               for (int j0 = 0; j0 < ncon; j0 += NB) {
                 float v[NB][RW];
 #pragma unroll
@@ -614,7 +659,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
                     const int sl = j == 0 ? sl_first : 0;
                     const float* src = a.partials + (static_cast<size_t>(cf + j) * 2 + sl) * kGemmBN * NT + et;
 #pragma unroll
-                    for (int k = 0; k < RW; ++k) v[jj][k] = __ldcg(src + (ch * 32 + col0 + k) * kGemmBN);
+                    for (int k = 0; k < RW; ++k)
+                      v[jj][k] = col0 + k < cn ? __ldcg(src + (cc + col0 + k) * kGemmBN) : 0.f;
                   }
                 }
                 // summed in CTA order, whatever the loads' completion order
@@ -622,19 +668,28 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
                 for (int jj = 0; jj < NB; ++jj)
                   if (j0 + jj < ncon) {
 #pragma unroll
-                    for (int k = 0; k < RW; ++k) s[k] += v[jj][k];
+                    for (int k = 0; k < RW; ++k) sm_[k] += v[jj][k];
                   }
               }
 #pragma unroll
-              for (int k = 0; k < RW; ++k) Ys[et * kYsLd + col0 + k] = s[k];
+              for (int k = 0; k < RW; ++k) Ys[et * kYsLd + col0 + k] = sm_[k];
               sync();
               trace_mark(trec, 10);
-              epilogue_tile(a, nt, Ys, kYsLd, m_base + ch * 32, mtot - ch * 32 < 32 ? mtot - ch * 32 : 32, et2,
-                            EPT, *esm, td, sync, nullptr);
+              epilogue_tile(a, nt, Ys, kYsLd, m_base + cc, cn, et2, EPT, *esm, td, sync, nullptr);
               sync();
               trace_mark(trec, 11);
             }
-            if (et2 == 0) a.counters[t] = 0u;
+            if (!share) {
+              if (et2 == 0) a.counters[t] = 0u;
+            } else if (et2 == 0) {
+              // the last participant to finish clears the tile's counters for the next launch
+              __threadfence();
+              unsigned* done = a.counters + static_cast<size_t>(a.n_tiles) * a.m_tiles;
+              if (atomicAdd(done + t, 1u) == static_cast<unsigned>(npart - 1)) {
+                a.counters[t] = 0u;
+                done[t] = 0u;
+              }
+            }
           }
         }
       }

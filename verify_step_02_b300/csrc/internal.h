@@ -133,9 +133,13 @@ struct TokData {
 // 1 start, 2 dependency wait returned, 3 first operands landed, 4 last MMA
 // issued, 5 epilogue done, 6 exit. The projection kernels add the steps of
 // their last tile's hand-off: 7 accumulator ready for the epilogue, 8 partial
-// tile stored and signalled, 9 arrival counted (stream-K) or every rank's
-// partial in place (cluster split, the tile's owner), 10 the partials summed
-// (last arriver or owner), 11 tile epilogue done.
+// tile stored and signalled, 9 every contributor's partial in place (the
+// stream-K participants; cluster split: the slice's owner), 10 the partials of
+// the last token chunk summed, 11 tile epilogue done, 12 x tile landed, 13
+// the cluster shares summed. The attention adds 7 partial (m, l, O) in shared
+// memory, 8 the cluster's partials visible, 9 merge weights computed, 10 last
+// K/V stage landed, 11 last softmax done, 12 first scores ready, 13 first
+// softmax done.
 constexpr int kTraceWords = 16;
 enum TraceKind : int { kTrGemm = 1, kTrAttn = 2, kTrMerge = 3, kTrPrep = 4, kTrAccept = 5, kTrGemmFma = 6 };
 
@@ -202,6 +206,8 @@ struct AttnArgs {
   int cl_size;             // tensor-core kernel: CTAs per (request, kv head, row tile), one cluster
   int q_rows;              // tensor-core kernel: block rows per row tile (q_rows * group <= 128)
   int n_row_tiles;         // tensor-core kernel: row tiles per request (ceil((max_gamma + 1) / q_rows))
+  int q_copies;            // tensor-core kernel: copies of a tile's query rows in the 128 MMA rows
+                           // (1, 2 or 4; q_rows * group * q_copies <= 128), each taking 1/q_copies of the keys
   unsigned long long* trace;  // per-CTA records of the attention launch, or nullptr
 };
 

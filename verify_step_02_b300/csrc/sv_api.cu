@@ -99,8 +99,10 @@ struct sv_model {
   std::vector<CUtensorMap> map_k, map_v;
   std::vector<const void*> map_k_ptr, map_v_ptr;
   std::vector<int> map_kv_pages;
-  CUtensorMap map_q;
-  int q_rows = 1;  // block rows per attention row tile
+  // q maps for row tiles of q_rows[k] block rows, each tile's rows placed 1 << k
+  // times into the 128 MMA rows (0: that layout does not fit)
+  CUtensorMap map_q[3];
+  int q_rows[3] = {0, 0, 0};
   bool last_logits = false;
   int last_m = 0;
   Timing timing;
@@ -294,6 +296,28 @@ sv_status run_gemm(sv_model* m, GemmArgs& a, int M, int n_units, int K, int pair
   return SV_OK;
 }
 
+// Row-tile layout of the tensor-core attention for a call with block lengths
+// lens[r] + 1: k = 0, 1, 2 places each tile's rows 1 << k times into the MMA
+// rows, so that 1 << k TMEM lane groups share the softmax (each over 64 >> k
+// keys of a sub-chunk); fewer rows per tile may mean more tiles, each reading
+// the request's keys again. Cost per tile: K/V traffic (the larger part: a CTA's
+// key stream is bound by the loads it can keep in flight) plus a softmax share.
+int attention_layout(const sv_model* m, int B, const int* lens) {
+  int best = 0;
+  double best_cost = 0.0;
+  for (int k = 0; k < 3; ++k) {
+    if (m->q_rows[k] < 1) continue;
+    long long tiles = 0;
+    for (int r = 0; r < B; ++r) tiles += (lens[r] + m->q_rows[k]) / m->q_rows[k];
+    const double cost = static_cast<double>(tiles) * (0.6 + 0.4 / (1 << k));
+    if (k == 0 || cost < best_cost) {
+      best = k;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, const sv_kv* kv, const float* probs,
                      float T, uint64_t seed, const long long* req_ids, int* acc_len, int* next_tok,
                      cudaStream_t s, bool commit_all = false, const int* parents = nullptr,
@@ -395,14 +419,16 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
           m->map_kv_pages[l] = kv->n_pages;
         }
         a.q_lo_row = m->m_max;
-        a.q_rows = m->q_rows;
+        const int ko = attention_layout(m, B, lens);
+        a.q_rows = m->q_rows[ko];
+        a.q_copies = 1 << ko;
         a.max_rows = a.q_rows * (c.n_heads / c.n_kv_heads);
         a.n_row_tiles = (max_block + a.q_rows - 1) / a.q_rows;
         const long long items = (long long)B * c.n_kv_heads * a.n_row_tiles;
         a.cl_size = attention_tc_cluster(items, hd, m->sm_count);
         a.trace = trace_slot(m, items * a.cl_size, kTrAttn);
         Timed t(m, SV_KC_ATTENTION, s);
-        SV_CUDA(launch_attention_tc(a, B, m->map_q, m->map_k[l], m->map_v[l], s), "attention");
+        SV_CUDA(launch_attention_tc(a, B, m->map_q[ko], m->map_k[l], m->map_v[l], s), "attention");
       } else {
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention(a, B, m->wbf16, s), "attention");
@@ -616,14 +642,21 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
     m->map_k_ptr.assign(c.n_layers, nullptr);
     m->map_v_ptr.assign(c.n_layers, nullptr);
     m->map_kv_pages.assign(c.n_layers, 0);
-    // q of one attention row tile: q_rows block rows x the group's heads <= 128 MMA rows
-    m->q_rows = std::min(c.max_gamma + 1, 128 / (c.n_heads / c.n_kv_heads));
-    const cudaError_t qe = tc_encode_q_map(&m->map_q, m->q, M, c.n_heads, c.head_dim, c.n_heads / c.n_kv_heads,
-                                           m->q_rows);
-    if (qe != cudaSuccess) {
-      free_all(m);
-      delete m;
-      return fail(SV_ERR_CUDA, "q tensor map: %s", cudaGetErrorString(qe));
+    // q of one attention row tile: q_rows block rows x the group's heads, times the
+    // copies, <= 128 MMA rows
+    const int group = c.n_heads / c.n_kv_heads;
+    for (int k = 0; k < 3; ++k) {
+      m->q_rows[k] = std::min(c.max_gamma + 1, (128 >> k) / group);
+      if (m->q_rows[k] < 1) {
+        m->q_rows[k] = 0;
+        continue;
+      }
+      const cudaError_t qe = tc_encode_q_map(&m->map_q[k], m->q, M, c.n_heads, c.head_dim, group, m->q_rows[k]);
+      if (qe != cudaSuccess) {
+        free_all(m);
+        delete m;
+        return fail(SV_ERR_CUDA, "q tensor map: %s", cudaGetErrorString(qe));
+      }
     }
   }
   if (m->use_tc) {
