@@ -63,7 +63,7 @@ def parse():
                     help="after the timed steps, run two traced steps and add a per-kernel timeline summary "
                          "(device %globaltimer per CTA) to the JSON line")
     ap.add_argument("--trace-out", default=None, help="with --trace: also save the raw per-CTA records (.npz)")
-    ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "sampled"], default="8b",
+    ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "w12g", "sampled"], default="8b",
                     help="8b: the headline line (default); the others time the other verify configurations "
                          "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
                          "batch 64) and print their own line")
@@ -832,6 +832,8 @@ WORKLOADS = {
     "27b": "27B-class bf16 ragged verify: 64 layers, d 5120, 40 q / 8 kv heads; batch 32, contexts uniform "
            "512-8192 on shuffled 16-token pages, verify lengths 1-16 by confidence truncation; greedy",
     "w12": "8B-class verify with W12 weights (16-binade window): batch 1, gamma 16, context 4096; greedy",
+    "w12g": "8B-class verify with grouped W12 weights (N(0, 0.02) bf16 weights, per-64-row bases and escapes): "
+            "batch 1, gamma 16, context 4096; greedy",
     "sampled": "tiny fp32 sampled verify: batch 64, context 2048, gamma 8, T = 1, rejection sampling",
 }
 
@@ -867,6 +869,17 @@ def run_workload(args, world, rank, local):
         ctx = rng.integers(512, 8193, size=B)
         lens = synth.truncated_verify_lens(B, gamma, 0.3, 31, 0)
         wdev = sd.random_bf16_model(shape)
+    elif wl == "w12g":  # the random N(0, 0.02) bf16 model itself, packed losslessly
+        shape = shape_of("8b")
+        kind, wdtype, kvdt = "w12", vs.SV_W12, torch.bfloat16
+        B, gamma = 1, 16
+        ctx = np.full(B, CONTEXT)
+        lens = np.full(B, gamma)
+        wdev = sd.random_bf16_model(shape)
+        for lay in wdev["layers"]:
+            for name in ("wqkv", "wo", "wgu", "wd"):
+                lay[name] = vs.pack_w12_grouped(lay[name])
+        wdev["lm_head"] = vs.pack_w12_grouped(wdev["lm_head"])
     else:  # w12
         shape = shape_of("8b")
         kind, wdtype, kvdt = "w12", vs.SV_W12, torch.bfloat16

@@ -105,13 +105,20 @@ typedef struct {
 #define SV_FLAG_CUDA_CORE_GEMM 4
 
 /* A weight matrix [rows][cols] (the output-major layout y = x W^T).
- * F32/BF16: `data` is a dense row-major device array of that type.
+ * F32/BF16: `data` is a dense row-major device array of that type; the other
+ *      fields are unused (0 / NULL).
  * W12: `data` holds plane 0, plane 1, plane 2 back to back, each
  *      sv_w12_plane_bytes(rows, cols) bytes (see sv_pack_w12), and `base` is
- *      the tensor's exponent base. */
+ *      the tensor's exponent base; row_bases, esc_off and esc are NULL.
+ * Grouped W12 (sv_pack_w12_grouped): the same planes, `base` unused, and the
+ *      device arrays row_bases [sv_w12_row_blocks(rows)], esc_off
+ *      [sv_w12_tiles(rows, cols) + 1] and esc [esc_off[tiles]]. */
 typedef struct {
   const void* data;
   int32_t base;
+  const uint8_t* row_bases;
+  const int32_t* esc_off;
+  const uint32_t* esc;
 } sv_matrix;
 
 /* One decoder layer. Norm gains are float32 for SV_F32 models, bf16 otherwise. */
@@ -322,6 +329,37 @@ sv_status sv_pack_w12(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t*
 /* Rebuild device bf16 [rows][cols] from planes and base. Asynchronous. */
 sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64_t cols, uint16_t* bf16_out,
                         void* stream);
+
+/*
+ * Grouped W12: any bf16 tensor, bit-exact. The planes keep the layout above;
+ * each block of 64 rows (a plane tile's rows) has its own base, and the
+ * elements its 16-binade window cannot hold are escapes, listed with their
+ * exact pattern (and coded 0 in the planes):
+ *   row_bases[rb] = max(1, (max E over the block's normal elements) - 15), or
+ *     1 for a block without normal elements;
+ *   an element escapes iff it is not a normal number or E < row_bases[rb];
+ *   the escapes of plane tile (rb, kt) (tile i = rb * KT + kt, KT =
+ *   ceil(cols / 128)) are esc[esc_off[i] .. esc_off[i + 1]), in row-major
+ *   order, each entry = row in block << 23 | column in tile << 16 | pattern.
+ * For N(0, 0.02) weights the escapes are the tail below 2^-16 of the block's
+ * largest magnitude (about 1e-4 of the elements) and exact zeros.
+ */
+int64_t sv_w12_row_blocks(int64_t rows);            /* ceil(rows / 64) */
+int64_t sv_w12_tiles(int64_t rows, int64_t cols);   /* row blocks x ceil(cols / 128) */
+
+/* Pack device bf16 [rows][cols]: planes (3 * sv_w12_plane_bytes), row_bases,
+ * esc_off as above (device, caller-allocated). The escapes go to `esc` (device,
+ * esc_capacity entries) and their number to *n_escapes (host). With esc NULL
+ * (capacity 0) only the count is computed; when the count exceeds the
+ * capacity, SV_ERR_INVALID_ARG (planes, bases and offsets are still written).
+ * Synchronizes `stream`. */
+sv_status sv_pack_w12_grouped(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t* planes, uint8_t* row_bases,
+                              int32_t* esc_off, uint32_t* esc, int64_t esc_capacity, int64_t* n_escapes,
+                              void* stream);
+
+/* Rebuild device bf16 [rows][cols] from grouped W12. Asynchronous. */
+sv_status sv_unpack_w12_grouped(const uint8_t* planes, const uint8_t* row_bases, const int32_t* esc_off,
+                                const uint32_t* esc, int64_t rows, int64_t cols, uint16_t* bf16_out, void* stream);
 
 /*
  * Skinny weight-streaming matrix product y[M][N] = x[M][K] W^T with the

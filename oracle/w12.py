@@ -72,6 +72,11 @@ def pack(bits):
     if bad:
         raise NotRepresentable(bad)
     code = (s << 11) | (off << 7) | m
+    return code_planes(code, rows, cols), base
+
+
+def code_planes(code, rows, cols):
+    """The three tiled planes of a [rows, cols] array of 12-bit codes."""
     rt, kt = -(-rows // TILE_ROWS), -(-cols // TILE_COLS)
     padded = np.zeros((rt * TILE_ROWS, kt * TILE_COLS), dtype=np.int64)
     padded[:rows, :cols] = code
@@ -83,11 +88,20 @@ def pack(bits):
         rowbytes = slots[:, 0::2] | (slots[:, 1::2] << 4)                # [rows_pad, cols_pad / 2]
         tiles = rowbytes.reshape(rt, TILE_ROWS, kt, TILE_COLS // 2).transpose(0, 2, 1, 3)
         planes[p] = tiles.reshape(-1).astype(np.uint8)
-    return planes, base
+    return planes
 
 
 def unpack(planes, base, rows, cols):
     """Inverse of pack: uint16 bf16 patterns [rows, cols]."""
+    code = plane_codes(planes, rows, cols)
+    s = code >> 11
+    e = ((code >> 7) & 0xF) + base
+    m = code & 0x7F
+    return ((s << 15) | (e << 7) | m).astype(np.uint16)
+
+
+def plane_codes(planes, rows, cols):
+    """Inverse of code_planes: the 12-bit codes [rows, cols]."""
     planes = np.asarray(planes, dtype=np.uint8)
     rt, kt = -(-rows // TILE_ROWS), -(-cols // TILE_COLS)
     slot_elem = (np.arange(kt * TILE_COLS) // 8) * 8 + SLOT_ELEMENT[np.arange(kt * TILE_COLS) % 8]
@@ -101,8 +115,56 @@ def unpack(planes, base, rows, cols):
         nib = np.empty_like(code)
         nib[:, slot_elem] = slots
         code |= nib << (4 * p)
-    code = code[:rows, :cols]
-    s = code >> 11
-    e = ((code >> 7) & 0xF) + base
-    m = code & 0x7F
-    return ((s << 15) | (e << 7) | m).astype(np.uint16)
+    return code[:rows, :cols]
+
+
+# ---------------------------------------------------------------- grouped W12
+# The per-tensor window fails on real weights (zeros, or tails that span more
+# than 16 binades). The grouped form keeps the planes above and adds, per block
+# of 64 rows (a plane tile's rows), its own base, and a list of escapes:
+#   base[rb] = max(1, (max E over the block's normal elements) - 15), or 1 for
+#   a block without normal elements; an element escapes when it is not a
+#   normal number or E < base[rb]; its code is 0 and the escape list holds
+#   its exact pattern. Escapes are grouped by plane tile (rb, kt), tiles in
+#   order rb * KT + kt, and within a tile in row-major order; entry =
+#   row in block << 23 | column in tile << 16 | bf16 pattern, and tile i's
+#   entries are esc[esc_off[i] .. esc_off[i + 1]].
+
+def pack_grouped(bits):
+    """Returns (planes, bases uint8 [row blocks], esc_off int32 [tiles + 1], esc uint32 [escapes])."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    s, e, m = fields(bits)
+    normal = representable_mask(bits)
+    rb_n, kt_n = -(-rows // TILE_ROWS), -(-cols // TILE_COLS)
+    bases = np.ones(rb_n, dtype=np.int64)
+    for rb in range(rb_n):
+        blk_e, blk_n = e[rb * TILE_ROWS:(rb + 1) * TILE_ROWS], normal[rb * TILE_ROWS:(rb + 1) * TILE_ROWS]
+        if blk_n.any():
+            bases[rb] = max(1, int(blk_e[blk_n].max()) - 15)
+    base_el = bases[np.arange(rows) // TILE_ROWS][:, None]
+    esc = ~normal | (e < base_el)
+    code = np.where(esc, 0, (s << 11) | ((e - base_el) << 7) | m)
+    planes = code_planes(code, rows, cols)
+    counts, entries = [], []
+    for rb in range(rb_n):
+        for kt in range(kt_n):
+            r0, c0 = rb * TILE_ROWS, kt * TILE_COLS
+            rr, cc = np.nonzero(esc[r0:r0 + TILE_ROWS, c0:c0 + TILE_COLS])   # row-major order
+            counts.append(len(rr))
+            entries += [(int(r) << 23) | (int(c) << 16) | int(bits[r0 + r, c0 + c]) for r, c in zip(rr, cc)]
+    esc_off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return planes, bases.astype(np.uint8), esc_off, np.asarray(entries, dtype=np.uint32)
+
+
+def unpack_grouped(planes, bases, esc_off, esc, rows, cols):
+    """Inverse of pack_grouped."""
+    code = plane_codes(planes, rows, cols)
+    base_el = np.asarray(bases, dtype=np.int64)[np.arange(rows) // TILE_ROWS][:, None]
+    out = ((code >> 11) << 15) | ((((code >> 7) & 0xF) + base_el) << 7) | (code & 0x7F)
+    kt_n = -(-cols // TILE_COLS)
+    for i in range(len(esc_off) - 1):
+        rb, kt = divmod(i, kt_n)
+        for ent in np.asarray(esc[esc_off[i]:esc_off[i + 1]], dtype=np.int64):
+            out[rb * TILE_ROWS + ((ent >> 23) & 63), kt * TILE_COLS + ((ent >> 16) & 127)] = ent & 0xFFFF
+    return out.astype(np.uint16)

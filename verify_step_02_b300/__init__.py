@@ -40,7 +40,18 @@ class Config(ctypes.Structure):
 
 
 class Matrix(ctypes.Structure):
-    _fields_ = [("data", ctypes.c_void_p), ("base", ctypes.c_int32)]
+    _fields_ = [("data", ctypes.c_void_p), ("base", ctypes.c_int32), ("row_bases", ctypes.c_void_p),
+                ("esc_off", ctypes.c_void_p), ("esc", ctypes.c_void_p)]
+
+
+def matrix(x):
+    """sv_matrix for a dense tensor, a W12 (planes, base) pair or a grouped W12
+    (planes, row_bases, esc_off, esc) tuple."""
+    if isinstance(x, tuple) and len(x) == 4:
+        return Matrix(x[0].data_ptr(), 0, x[1].data_ptr(), x[2].data_ptr(), x[3].data_ptr() if x[3].numel() else None)
+    if isinstance(x, tuple):
+        return Matrix(x[0].data_ptr(), int(x[1]), None, None, None)
+    return Matrix(x.data_ptr(), 0, None, None, None)
 
 
 class LayerWeights(ctypes.Structure):
@@ -77,6 +88,10 @@ _SIGS = {
     "sv_w12_plane_bytes": (_i64, [_i64, _i64]),
     "sv_pack_w12": (_i32, [_vp, _i64, _i64, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i64), _vp]),
     "sv_unpack_w12": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+    "sv_w12_row_blocks": (_i64, [_i64]),
+    "sv_w12_tiles": (_i64, [_i64, _i64]),
+    "sv_pack_w12_grouped": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, ctypes.POINTER(_i64), _vp]),
+    "sv_unpack_w12_grouped": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "sv_linear_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "sv_linear": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
     "sv_linear_noalloc": (_i32, [_i32, ctypes.POINTER(Matrix), _i32, _i32, _vp, _i32, _i32, _vp, _vp]),
@@ -131,17 +146,15 @@ class Model:
 
     weights: dict with "layers" (list of dicts: attn_norm, wqkv, wo, mlp_norm, wgu, wd),
     "embed", "final_norm", "lm_head"; tensors on the current CUDA device. For W12
-    models each matrix entry is a (planes_tensor, base) pair.
+    models each matrix entry is a (planes_tensor, base) pair (pack_w12) or a
+    grouped (planes, row_bases, esc_off, esc) tuple (pack_w12_grouped).
     """
 
     def __init__(self, config, weights, stream=None):
         self.config = config
         self._keep = weights
 
-        def mat(x):
-            if isinstance(x, tuple):
-                return Matrix(x[0].data_ptr(), int(x[1]))
-            return Matrix(x.data_ptr(), 0)
+        mat = matrix
 
         layers = weights["layers"]
         self._layers = (LayerWeights * len(layers))(*[
@@ -259,6 +272,32 @@ def pack_w12(bf16, stream=None):
     return planes, base.value
 
 
+def pack_w12_grouped(bf16, stream=None):
+    """bf16 device tensor [rows, cols] -> grouped W12 (planes [3, plane_bytes], row_bases, esc_off, esc)."""
+    import torch
+    rows, cols = bf16.shape
+    dev = bf16.device
+    planes = torch.empty((3, w12_plane_bytes(rows, cols)), dtype=torch.uint8, device=dev)
+    bases = torch.empty(int(lib.sv_w12_row_blocks(rows)), dtype=torch.uint8, device=dev)
+    off = torch.empty(int(lib.sv_w12_tiles(rows, cols)) + 1, dtype=torch.int32, device=dev)
+    n = ctypes.c_int64()
+    _check(lib.sv_pack_w12_grouped(_ptr(bf16), rows, cols, _ptr(planes), _ptr(bases), _ptr(off), None, 0,
+                                   ctypes.byref(n), _stream(stream)))
+    esc = torch.empty(max(n.value, 1), dtype=torch.int32, device=dev)
+    if n.value:
+        _check(lib.sv_pack_w12_grouped(_ptr(bf16), rows, cols, _ptr(planes), _ptr(bases), _ptr(off), _ptr(esc),
+                                       n.value, ctypes.byref(n), _stream(stream)))
+    return planes, bases, off, esc[:n.value]
+
+
+def unpack_w12_grouped(planes, bases, off, esc, rows, cols, stream=None):
+    import torch
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=planes.device)
+    _check(lib.sv_unpack_w12_grouped(_ptr(planes), _ptr(bases), _ptr(off), _ptr(esc) if esc.numel() else None,
+                                     rows, cols, _ptr(out), _stream(stream)))
+    return out
+
+
 def unpack_w12(planes, base, rows, cols, stream=None):
     import torch
     out = torch.empty((rows, cols), dtype=torch.bfloat16, device=planes.device)
@@ -278,7 +317,7 @@ def linear(wdtype, w, x, n, k, base=0, stream=None, workspace=None):
     if workspace is None or workspace.numel() < need:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=x.device)
     y = torch.empty((m, n), dtype=torch.float32, device=x.device)
-    mat = Matrix(w.data_ptr(), int(base))
+    mat = matrix(w) if isinstance(w, tuple) else Matrix(w.data_ptr(), int(base), None, None, None)
     _check(lib.sv_linear(int(wdtype), ctypes.byref(mat), int(n), int(k), _ptr(x), planes, m, _ptr(y),
                          _ptr(workspace), workspace.numel(), _stream(stream)))
     return y, workspace

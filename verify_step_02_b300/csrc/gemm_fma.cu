@@ -61,7 +61,8 @@ __device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, floa
     const uint2 p0 = __ldg(reinterpret_cast<const uint2*>(base));
     const uint2 p1 = __ldg(reinterpret_cast<const uint2*>(base + a.w12_plane));
     const uint2 p2 = __ldg(reinterpret_cast<const uint2*>(base + 2 * a.w12_plane));
-    const uint32_t ebase = static_cast<uint32_t>(a.w12_base) << 7;
+    // grouped W12: the row block's base, then the tile's escapes patched in
+    const uint32_t ebase = static_cast<uint32_t>(a.w12_bases ? __ldg(a.w12_bases + (row >> 6)) : a.w12_base) << 7;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t b0 = h ? p0.y : p0.x, b1 = h ? p1.y : p1.x, b2 = h ? p2.y : p2.x;
@@ -71,6 +72,19 @@ __device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, floa
         const uint32_t c = ((b2 >> sh) & 0xFu) << 8 | ((b1 >> sh) & 0xFu) << 4 | ((b0 >> sh) & 0xFu);
         const uint32_t bits = ((c & 0x7FFu) + ebase) | ((c & 0x800u) << 4);
         v[8 * h + e] = __uint_as_float(bits << 16);
+      }
+    }
+    if (a.w12_esc_off) {
+      const long long tile = (long long)(row >> 6) * a.w12_kt + (k >> 7);
+      const int o1 = __ldg(a.w12_esc_off + tile + 1), c0 = k & 127;
+      for (int i = __ldg(a.w12_esc_off + tile); i < o1; ++i) {
+        const uint32_t ent = __ldg(a.w12_esc + i);
+        const int r = ent >> 23 & 63, c = (ent >> 16 & 127) - c0;
+        if (r == (row & 63)) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)  // (a static index keeps v in registers)
+            if (c == j) v[j] = __uint_as_float((ent & 0xFFFFu) << 16);
+        }
       }
     }
   }

@@ -396,11 +396,36 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     // tile row is 64 bytes at r * 64 (the two 64-row halves are 4096 bytes apart)
     const int g = ct & 15, r0 = ct >> 4;
     const int q = g >> 3, c16 = g & 7;
-    const uint32_t b2 = (static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u;
+    // grouped W12: each 64-row half of the tile has its row block's base, and the
+    // unit's escapes are written over the rebuilt elements by the thread that
+    // rebuilt them (row r0 (mod 2 NCONV), group g), so no barrier is needed
+    const bool grouped = a.w12_bases != nullptr;
+    const int nrb = (a.n_rows + 63) / 64;
     int stage = 0;
     uint32_t phase = 0;
     int ai = 0;
     for (long long i = 0; i < NU; ++i, ++ai) {
+      uint32_t b2h[2] = {(static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u, 0u};
+      int eo[2] = {0, 0}, ee[2] = {0, 0};
+      b2h[1] = b2h[0];
+      if (grouped) {
+        long long t;
+        int kb;
+        W.at(i, t, kb);
+        const int nt = static_cast<int>(t / a.m_tiles);
+        const int rh0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
+        const int rh1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : rh0 + kGemmBN / 2;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rb = (hh ? rh1 : rh0) / 64;
+          if (rb < nrb) {
+            b2h[hh] = (static_cast<uint32_t>(__ldg(a.w12_bases + rb)) << 7) * 0x10001u;
+            const long long tile = static_cast<long long>(rb) * a.w12_kt + kb;
+            eo[hh] = __ldg(a.w12_esc_off + tile);
+            ee[hh] = __ldg(a.w12_esc_off + tile + 1);
+          }
+        }
+      }
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait(full + stage, phase, abort_flag, kWaitNs) &&
@@ -426,10 +451,20 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
         // ((c & 0x7FF) + (base << 7)) | (sign << 15) per 16-bit lane is one add: the
         // exponent sum base + e <= 254 (any code that packing accepted) stays below bit 15
         uint32_t o[4];
+        const uint32_t b2 = r < 64 ? b2h[0] : b2h[1];
 #pragma unroll
         for (int j = 0; j < 4; ++j) o[j] = cw4[j] + b2;
         *reinterpret_cast<uint4*>(aw + r * 128 + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        for (int e = eo[hh]; e < ee[hh]; ++e) {
+          const uint32_t ent = __ldg(a.w12_esc + e);
+          const int r = hh * 64 + static_cast<int>(ent >> 23 & 63u), col = static_cast<int>(ent >> 16 & 127u);
+          if (r % (NCONV * 2) == r0 && (col >> 3) == g)
+            *reinterpret_cast<uint16_t*>(aw + r * 128 + ((c16 ^ (r & 7)) << 4) + (col & 7) * 2) =
+                static_cast<uint16_t>(ent & 0xFFFFu);
+        }
       fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
       __syncwarp();
       if (lane == 0) {

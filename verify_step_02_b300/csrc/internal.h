@@ -149,6 +149,9 @@ struct GemmArgs {
   int w12_base;
   int w12_kt;              // W12: 128-element tiles per row
   long long w12_plane;     // W12 bytes per plane
+  const uint8_t* w12_bases;    // grouped W12: base per 64-row block (else nullptr: w12_base)
+  const int* w12_esc_off;      // grouped W12: escapes of plane tile i at w12_esc[off[i] .. off[i + 1])
+  const uint32_t* w12_esc;     //   (entry: row in block << 23 | column in tile << 16 | bf16 pattern)
   int n_rows;              // rows of W
   int K;
   const void* x;           // activations [M][K]
@@ -357,6 +360,14 @@ cudaError_t launch_w12_pack(const uint16_t* bf16, long long rows, long long cols
                             cudaStream_t s);
 cudaError_t launch_w12_unpack(const uint8_t* planes, int base, long long rows, long long cols, uint16_t* out,
                               cudaStream_t s);
+// grouped W12 (w12_grouped.cu)
+cudaError_t launch_w12g_bases(const uint16_t* bf16, long long rows, long long cols, uint8_t* bases, cudaStream_t s);
+cudaError_t launch_w12g_count(const uint16_t* bf16, long long rows, long long cols, const uint8_t* bases, int* cnt,
+                              cudaStream_t s);
+cudaError_t launch_w12g_pack(const uint16_t* bf16, long long rows, long long cols, const uint8_t* bases,
+                             const int* off, uint8_t* planes, uint32_t* esc, cudaStream_t s);
+cudaError_t launch_w12g_unpack(const uint8_t* planes, const uint8_t* bases, const int* off, const uint32_t* esc,
+                               long long rows, long long cols, uint16_t* out, cudaStream_t s);
 cudaError_t launch_philox(unsigned long long seed, long long req, long long pos0, int stream_id, int n, float* out,
                           cudaStream_t s);
 

@@ -52,7 +52,9 @@ extern "C" sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32
   if (x_planes != 1 && !(x_planes == 2 && wdtype != SV_F32))
     return reject(SV_ERR_INVALID_ARG, "x_planes must be 1, or 2 for bf16/W12 weights");
   if (M < 1 || M > 4096 || N < 1 || K < 16 || K % 16) return reject(SV_ERR_INVALID_ARG, "need 1<=M<=4096, N>=1, K%16==0");
-  if (wdtype == SV_W12 && (w->base < 1 || w->base > 254)) return reject(SV_ERR_INVALID_ARG, "bad W12 base");
+  if (wdtype == SV_W12 && !w->row_bases && (w->base < 1 || w->base > 254))
+    return reject(SV_ERR_INVALID_ARG, "bad W12 base");
+  if (wdtype == SV_W12 && w->row_bases && !w->esc_off) return reject(SV_ERR_INVALID_ARG, "grouped W12 without esc_off");
   int dev = 0, sm = 148;
   if (cudaGetDevice(&dev) != cudaSuccess) return reject(SV_ERR_CUDA, "cudaGetDevice failed");
   cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
@@ -61,6 +63,9 @@ extern "C" sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32
   a.wdtype = wdtype;
   a.w = w->data;
   a.w12_base = w->base;
+  a.w12_bases = w->row_bases;
+  a.w12_esc_off = w->esc_off;
+  a.w12_esc = w->esc;
   a.w12_kt = (K + 127) / 128;
   a.w12_plane = w12_plane_bytes(N, K);
   a.n_rows = N;

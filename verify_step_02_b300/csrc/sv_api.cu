@@ -234,6 +234,9 @@ GemmArgs gemm_base(sv_model* m, const sv_matrix& w, int n_rows, int K, const voi
   a.w12_base = w.base;
   a.w12_kt = (K + 127) / 128;
   a.w12_plane = w12_plane_bytes(n_rows, K);
+  a.w12_bases = w.row_bases;
+  a.w12_esc_off = w.esc_off;
+  a.w12_esc = w.esc;
   a.n_rows = n_rows;
   a.x = x;
   a.x_plane = x_plane;
@@ -555,10 +558,18 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   if (st) return st;
   if (!weights || !weights->embed || !weights->final_norm || !weights->lm_head.data || !weights->layers)
     return fail(SV_ERR_INVALID_ARG, "incomplete sv_weights");
+  // W12 matrices: a tensor-wide base in 1 .. 254, or grouped (row bases and escape offsets)
+  auto bad_w12 = [&](const sv_matrix& w) {
+    if (cfg->weight_dtype != SV_W12) return false;
+    return w.row_bases ? !w.esc_off : (w.base < 1 || w.base > 254);
+  };
+  if (bad_w12(weights->lm_head)) return fail(SV_ERR_INVALID_ARG, "bad W12 lm_head (base or grouped arrays)");
   for (int l = 0; l < cfg->n_layers; ++l) {
     const sv_layer_weights& L = weights->layers[l];
     if (!L.attn_norm || !L.mlp_norm || !L.wqkv.data || !L.wo.data || !L.wgu.data || !L.wd.data)
       return fail(SV_ERR_INVALID_ARG, "incomplete weights for layer %d", l);
+    if (bad_w12(L.wqkv) || bad_w12(L.wo) || bad_w12(L.wgu) || bad_w12(L.wd))
+      return fail(SV_ERR_INVALID_ARG, "bad W12 matrix in layer %d (base or grouped arrays)", l);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   sv_model* m = new sv_model();
@@ -906,6 +917,53 @@ sv_status sv_unpack_w12(const uint8_t* planes, int32_t base, int64_t rows, int64
   return SV_OK;
 }
 
+int64_t sv_w12_row_blocks(int64_t rows) { return rows < 1 ? 0 : (rows + 63) / 64; }
+int64_t sv_w12_tiles(int64_t rows, int64_t cols) {
+  return rows < 1 || cols < 1 ? 0 : ((rows + 63) / 64) * ((cols + 127) / 128);
+}
+
+sv_status sv_pack_w12_grouped(const uint16_t* bf16, int64_t rows, int64_t cols, uint8_t* planes, uint8_t* row_bases,
+                              int32_t* esc_off, uint32_t* esc, int64_t esc_capacity, int64_t* n_escapes,
+                              void* stream) {
+  if (!bf16 || !planes || !row_bases || !esc_off || !n_escapes) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (rows < 1 || cols < 1) return fail(SV_ERR_INVALID_ARG, "rows and cols must be positive");
+  if (esc_capacity < 0 || (esc_capacity > 0 && !esc)) return fail(SV_ERR_INVALID_ARG, "bad escape buffer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t tiles = sv_w12_tiles(rows, cols);
+  // per-tile escape counts into esc_off, their exclusive scan on the host, back to esc_off
+  SV_CUDA(launch_w12g_bases(bf16, rows, cols, row_bases, s), "w12 grouped bases");
+  SV_CUDA(launch_w12g_count(bf16, rows, cols, row_bases, esc_off, s), "w12 grouped count");
+  std::vector<int32_t> off(static_cast<size_t>(tiles) + 1);
+  SV_CUDA(cudaMemcpyAsync(off.data(), esc_off, sizeof(int32_t) * tiles, cudaMemcpyDeviceToHost, s), "read counts");
+  SV_CUDA(cudaStreamSynchronize(s), "synchronize");
+  long long total = 0;
+  for (int64_t i = 0; i < tiles; ++i) {
+    const long long c = off[i];
+    off[i] = static_cast<int32_t>(total);
+    total += c;
+  }
+  if (total > 0x7FFFFFFFll) return fail(SV_ERR_NOT_REPRESENTABLE, "too many escapes (%lld)", total);
+  off[tiles] = static_cast<int32_t>(total);
+  SV_CUDA(cudaMemcpyAsync(esc_off, off.data(), sizeof(int32_t) * (tiles + 1), cudaMemcpyHostToDevice, s),
+          "write offsets");
+  const bool fits = total <= esc_capacity;
+  SV_CUDA(launch_w12g_pack(bf16, rows, cols, row_bases, esc_off, planes, fits && total > 0 ? esc : nullptr, s),
+          "w12 grouped pack");
+  SV_CUDA(cudaStreamSynchronize(s), "synchronize");
+  *n_escapes = total;
+  if (!fits && esc) return fail(SV_ERR_INVALID_ARG, "%lld escapes exceed the capacity %lld", total, (long long)esc_capacity);
+  return SV_OK;
+}
+
+sv_status sv_unpack_w12_grouped(const uint8_t* planes, const uint8_t* row_bases, const int32_t* esc_off,
+                                const uint32_t* esc, int64_t rows, int64_t cols, uint16_t* bf16_out, void* stream) {
+  if (!planes || !row_bases || !esc_off || !bf16_out) return fail(SV_ERR_INVALID_ARG, "NULL argument");
+  if (rows < 1 || cols < 1) return fail(SV_ERR_INVALID_ARG, "rows and cols must be positive");
+  SV_CUDA(launch_w12g_unpack(planes, row_bases, esc_off, esc, rows, cols, bf16_out, static_cast<cudaStream_t>(stream)),
+          "unpack_w12_grouped");
+  return SV_OK;
+}
+
 size_t sv_linear_workspace_bytes(int32_t wdtype, int32_t M, int32_t N, int32_t K) {
   if (M < 1 || N < 1 || K < 1) return 0;
   int dev = 0, sm = 148;
@@ -934,7 +992,9 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   if (x_planes != 1 && !(x_planes == 2 && wdtype != SV_F32))
     return fail(SV_ERR_INVALID_ARG, "x_planes must be 1, or 2 for bf16/W12 weights");
   if (M < 1 || M > 4096 || N < 1 || K < 16 || K % 16) return fail(SV_ERR_INVALID_ARG, "need 1<=M<=4096, N>=1, K%%16==0");
-  if (wdtype == SV_W12 && (w->base < 1 || w->base > 254)) return fail(SV_ERR_INVALID_ARG, "bad W12 base");
+  if (wdtype == SV_W12 && !w->row_bases && (w->base < 1 || w->base > 254))
+    return fail(SV_ERR_INVALID_ARG, "bad W12 base");
+  if (wdtype == SV_W12 && w->row_bases && !w->esc_off) return fail(SV_ERR_INVALID_ARG, "grouped W12 without esc_off");
   const size_t need = sv_linear_workspace_bytes(wdtype, M, N, K);
   if (workspace_bytes < need) return fail(SV_ERR_INVALID_ARG, "workspace %zu < %zu bytes", workspace_bytes, need);
   int dev = 0, sm = 148;
@@ -945,6 +1005,9 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
   a.wdtype = wdtype;
   a.w = w->data;
   a.w12_base = w->base;
+  a.w12_bases = w->row_bases;
+  a.w12_esc_off = w->esc_off;
+  a.w12_esc = w->esc;
   a.w12_kt = (K + 127) / 128;
   a.w12_plane = w12_plane_bytes(N, K);
   a.n_rows = N;
