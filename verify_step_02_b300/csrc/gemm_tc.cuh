@@ -401,31 +401,38 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     // rebuilt them (row r0 (mod 2 NCONV), group g), so no barrier is needed
     const bool grouped = a.w12_bases != nullptr;
     const int nrb = (a.n_rows + 63) / 64;
+    // unit i's row-block bases and escape ranges, requested one unit ahead
+    auto unit_meta = [&](long long i, uint32_t* b2h, int* eo, int* ee) {
+      b2h[0] = b2h[1] = (static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u;
+      eo[0] = eo[1] = ee[0] = ee[1] = 0;
+      if (!grouped || i >= NU) return;
+      long long t;
+      int kb;
+      W.at(i, t, kb);
+      const int nt = static_cast<int>(t / a.m_tiles);
+      const int rh0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
+      const int rh1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : rh0 + kGemmBN / 2;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int rb = (hh ? rh1 : rh0) / 64;
+        if (rb < nrb) {
+          b2h[hh] = (static_cast<uint32_t>(__ldg(a.w12_bases + rb)) << 7) * 0x10001u;
+          const long long tile = static_cast<long long>(rb) * a.w12_kt + kb;
+          eo[hh] = __ldg(a.w12_esc_off + tile);
+          ee[hh] = __ldg(a.w12_esc_off + tile + 1);
+        }
+      }
+    };
+    uint32_t nb2[2];
+    int neo[2], nee[2];
+    unit_meta(0, nb2, neo, nee);
     int stage = 0;
     uint32_t phase = 0;
     int ai = 0;
     for (long long i = 0; i < NU; ++i, ++ai) {
-      uint32_t b2h[2] = {(static_cast<uint32_t>(a.w12_base) << 7) * 0x10001u, 0u};
-      int eo[2] = {0, 0}, ee[2] = {0, 0};
-      b2h[1] = b2h[0];
-      if (grouped) {
-        long long t;
-        int kb;
-        W.at(i, t, kb);
-        const int nt = static_cast<int>(t / a.m_tiles);
-        const int rh0 = a.pair == kPairSwiglu ? nt * (kGemmBN / 2) : nt * kGemmBN;
-        const int rh1 = a.pair == kPairSwiglu ? a.ffn + nt * (kGemmBN / 2) : rh0 + kGemmBN / 2;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int rb = (hh ? rh1 : rh0) / 64;
-          if (rb < nrb) {
-            b2h[hh] = (static_cast<uint32_t>(__ldg(a.w12_bases + rb)) << 7) * 0x10001u;
-            const long long tile = static_cast<long long>(rb) * a.w12_kt + kb;
-            eo[hh] = __ldg(a.w12_esc_off + tile);
-            ee[hh] = __ldg(a.w12_esc_off + tile + 1);
-          }
-        }
-      }
+      const uint32_t b2h[2] = {nb2[0], nb2[1]};
+      const int eo[2] = {neo[0], neo[1]}, ee[2] = {nee[0], nee[1]};
+      unit_meta(i + 1, nb2, neo, nee);
       int ok = 1;
       if (lane == 0)
         ok = mbar_wait(full + stage, phase, abort_flag, kWaitNs) &&
