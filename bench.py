@@ -283,10 +283,10 @@ def build_workload(steps_total, layers=36, flags=0):
     return shape, wdev, kv, model, table, cfg
 
 
-def greedy_reference(model, kv, anchor, n_tokens):
+def greedy_reference(model, kv, anchor, n_tokens, width=GAMMA + 1):
     """Greedy decoding with the same engine (one row per step, no drafts)."""
     import torch
-    tok = torch.zeros((1, GAMMA + 1), dtype=torch.int32, device="cuda")
+    tok = torch.zeros((1, width), dtype=torch.int32, device="cuda")
     acc = torch.zeros(1, dtype=torch.int32, device="cuda")
     nxt = torch.zeros(n_tokens, dtype=torch.int32, device="cuda")
     tok[0, 0] = anchor
@@ -296,18 +296,18 @@ def greedy_reference(model, kv, anchor, n_tokens):
     return [anchor] + [int(x) for x in nxt.cpu().numpy()]
 
 
-def make_plan(g, steps, vocab):
-    """Blocks [anchor, d_1..d_16] of each step, assuming the engine accepts exactly as greedy decoding."""
+def make_plan(g, steps, vocab, gamma=GAMMA, p_keep=P_KEEP):
+    """Blocks [anchor, d_1..d_gamma] of each step, assuming the engine accepts exactly as greedy decoding."""
     import synth
     blocks, expect = [], []
     off = 0  # index in g of the current anchor
     for s in range(steps):
-        want = g[off + 1: off + 1 + GAMMA]
-        if len(want) < GAMMA:
-            want = list(want) + [0] * (GAMMA - len(want))
-        drafts = synth.greedy_mix_drafts(want, GAMMA, P_KEEP, vocab, 40, s)
+        want = g[off + 1: off + 1 + gamma]
+        if len(want) < gamma:
+            want = list(want) + [0] * (gamma - len(want))
+        drafts = synth.greedy_mix_drafts(want, gamma, p_keep, vocab, 40, s)
         k = 0
-        while k < GAMMA and off + 1 + k < len(g) and drafts[k] == g[off + 1 + k]:
+        while k < gamma and off + 1 + k < len(g) and drafts[k] == g[off + 1 + k]:
             k += 1
         blocks.append([g[off]] + [int(x) for x in drafts])
         expect.append(k)
@@ -922,9 +922,18 @@ def run_workload(args, world, rank, local):
     rid = torch.arange(B, dtype=torch.int64, device="cuda")
     stream = torch.cuda.current_stream()
 
+    blocks_d = None
+    if wl == "tiny":
+        # the configuration's draft rule: draft i is the target's greedy token with probability
+        # 0.8^(i+1), from the same engine's greedy run (then the KV context is reset)
+        g = greedy_reference(model, kv, int(tok[0, 0].item()), steps_total * (gamma + 1) + gamma + 8, gamma + 1)
+        blocks, _ = make_plan(g, steps_total, V, gamma, 0.8)
+        blocks_d = torch.from_numpy(blocks).cuda()
+        seq.copy_(torch.from_numpy(ctx.astype(np.int32)))
+
     def run(i):
-        model.verify(tok, lens, kv, acc, nxt, draft_probs=probs, temperature=temperature, seed=1234 + i,
-                     request_ids=rid)
+        model.verify(tok if blocks_d is None else blocks_d[i:i + 1], lens, kv, acc, nxt, draft_probs=probs,
+                     temperature=temperature, seed=1234 + i, request_ids=rid)
 
     clocks = ClockSampler(local)
     for i in range(args.warmup):
@@ -983,7 +992,9 @@ def run_workload(args, world, rank, local):
         "metric": METRIC, "workload": wl, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "dtype": {"f32": "f32", "bf16": "bf16", "w12": "bf16 (W12 weights)"}[kind],
-        "data": "synthetic (random weights, random N(0,1) KV context, uniform random drafts)",
+        "data": "synthetic (random weights, random N(0,1) KV context, " + (
+            "greedy-mix drafts: the engine's greedy token w.p. 0.8^(i+1), else uniform)" if wl == "tiny"
+            else "uniform random drafts)"),
         "config": {"workload": WORKLOADS[wl], "batch": B, "gamma": gamma, "M": M, "layers": shape["n_layers"]},
         "verify_us": {"median": round(1e3 * statistics.median(per_step), 1),
                       "p90": round(1e3 * float(np.percentile(per_step, 90)), 1)},

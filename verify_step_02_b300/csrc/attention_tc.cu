@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t XCH_OFF = KV_OFF + 128 * HD * 4 + 128 * 8;
   constexpr uint32_t WTS_OFF = XCH_OFF + 4 * 128 * 8;
   constexpr uint32_t MLS_OFF = WTS_OFF + 128 * 16 * 4;
-  static_assert(MLS_OFF + 128 * 16 * 8 <= KV_OFF + kStages * KVB, "merge scratch must fit the K/V ring");
+  constexpr uint32_t MLR_OFF = MLS_OFF + 128 * 16 * 8;  // the cluster's merged (m, l) of this rank's rows
+  static_assert(MLR_OFF + 128 * 8 + 16 <= KV_OFF + kStages * KVB, "merge scratch must fit the K/V ring");
   constexpr uint32_t BAR_OFF = PM_OFF + 2 * 2 * 2 * 128 + 4 * 16;  // + the pair wait flags
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* vmask_s = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // [kStages]: pages loaded
 
-  const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+  const int lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   unsigned long long* const rec = a.trace ? a.trace + static_cast<size_t>(lin) * kTraceWords : nullptr;
   if (rec && threadIdx.x == 0) {
     rec[0] = (static_cast<unsigned long long>(kTrAttn) << 48) | (static_cast<unsigned long long>(sm_id()) << 32) |
@@ -183,8 +184,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   const int T = C + j0 + ntok;  // keys any row of the tile may see
   // this CTA's keys [k0, k0 + nkeys): the T keys in CS ranges of a multiple of 64
-  const int per = ((T + CS - 1) / CS + kSub - 1) / kSub * kSub;
-  const int k0 = rank * per;
+  // CC clusters per work item (grid z) split the keys further; their merged partials meet in
+  // global memory, where the last of them to arrive for a row slice finishes it
+  const int CC = gridDim.z, cc = blockIdx.z;
+  const int NR = CS * CC, ri = cc * CS + rank;
+  const int per = ((T + NR - 1) / NR + kSub - 1) / kSub * kSub;
+  const int k0 = ri * per;
   const int nkeys = T - k0 < per ? T - k0 : per;  // <= 0: no keys (an empty partial)
   const int nsub = nkeys > 0 ? (nkeys + kSub - 1) / kSub : 0;
   const int R = ntok * group;
@@ -619,9 +624,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         wts[rr * NP + p] = w;
         L += v.y * w;
       }
-      // L = 0 only for rows whose keys were all on bad pages (flagged): output 0
-      const float inv = L > 0.f ? 1.0f / L : 0.f;
+      // L = 0 only for rows whose keys were all on bad pages (flagged): output 0. With
+      // several clusters the sum stays unnormalized until their partials meet.
+      const float inv = CC > 1 ? 1.f : (L > 0.f ? 1.0f / L : 0.f);
       for (int p = 0; p < NP; ++p) wts[rr * NP + p] *= inv;
+      if (CC > 1) reinterpret_cast<float2*>(smem + MLR_OFF)[rr] = make_float2(M, L);
     }
     __syncthreads();
     if (tid == 0) trace_mark(rec, 9);
@@ -651,9 +658,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
+      if (CC > 1) {
+        const size_t slot = static_cast<size_t>(blockIdx.x) * CC + cc;
+        __stcg(reinterpret_cast<float4*>(a.xpart + (slot * 128 + rho) * HD + d), acc);
+        if (d == 0) __stcg(a.xml + slot * 128 + rho, reinterpret_cast<const float2*>(smem + MLR_OFF)[rr]);
+        continue;
+      }
       const int jrow = j0 + rho / group, g = rho % group;
       const long long orow = static_cast<long long>(row0 + jrow) * a.n_heads * HD + (h * group + g) * HD + d;
       store_x4(a.out, a.out_plane, orow, acc, a.x_pair);
+    }
+    if (CC > 1) {
+      // the last of the item's CC clusters to arrive for this rank's rows merges their partials
+      volatile int* s_last = reinterpret_cast<volatile int*>(smem + MLR_OFF + 128 * 8);
+      __threadfence();
+      __syncthreads();
+      unsigned* cnt = a.xcnt + static_cast<size_t>(blockIdx.x) * kMaxCluster + rank;
+      if (tid == 0) *s_last = atomicAdd(cnt, 1u) == static_cast<unsigned>(CC - 1) ? 1 : 0;
+      __syncthreads();
+      if (*s_last) {
+        __threadfence();
+        for (int it = tid; it < nrr * D4; it += kAttnThreads) {
+          const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
+          const size_t base = static_cast<size_t>(blockIdx.x) * CC;
+          float M = -INFINITY;
+          for (int c = 0; c < CC; ++c) M = fmaxf(M, __ldcg(a.xml + (base + c) * 128 + rho).x);
+          float L = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < CC; ++c) {  // in cluster order: a fixed summation order
+            const float2 ml = __ldcg(a.xml + (base + c) * 128 + rho);
+            const float w = ml.x == -INFINITY ? 0.f : __expf(ml.x - M);
+            if (w == 0.f) continue;
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(a.xpart + ((base + c) * 128 + rho) * HD + d));
+            L += ml.y * w;
+            acc.x += o.x * w;
+            acc.y += o.y * w;
+            acc.z += o.z * w;
+            acc.w += o.w * w;
+          }
+          const float inv = L > 0.f ? 1.0f / L : 0.f;
+          acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          const int jrow = j0 + rho / group, g = rho % group;
+          const long long orow = static_cast<long long>(row0 + jrow) * a.n_heads * HD + (h * group + g) * HD + d;
+          store_x4(a.out, a.out_plane, orow, acc, a.x_pair);
+        }
+        if (tid == 0) *cnt = 0u;
+      }
     }
   }
   if (tid == 0) trace_mark(rec, 5);
@@ -690,7 +740,7 @@ cudaError_t launch_hd(const AttnArgs& a, int B, const CUtensorMap& q, const CUte
   cudaError_t e = set_attrs<HD, QC>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(B * a.n_kv_heads * a.n_row_tiles, a.cl_size);
+  cfg.gridDim = dim3(B * a.n_kv_heads * a.n_row_tiles, a.cl_size, a.cl_count);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = attn_tc_smem(HD);
   cfg.stream = s;
@@ -730,6 +780,28 @@ int max_clusters_hd(int cs) {
 
 }  // namespace
 
+void attention_tc_split(long long items, int head_dim, int sm_count, int* cs_out, int* cc_out) {
+  int cs = attention_tc_cluster(items, head_dim, sm_count), cc = 1;
+  // few work items: several clusters per item (merged through global memory) so that
+  // about every SM streams keys; cs * cc CTAs per item, all clusters co-resident
+  if (items <= kCrossItems && items * cs * 2 <= sm_count) {
+    int best = cs, bcs = cs, bcc = 1;
+    for (int c = 2; c <= kMaxCrossClusters; c *= 2)
+      for (int s = 2; s <= 8; s *= 2) {
+        if (items * s * c > sm_count || s * c <= best) continue;
+        const int mc = head_dim == 128 ? max_clusters_hd<128>(s) : max_clusters_hd<64>(s);
+        if (mc < items * c) continue;  // every cluster of the launch resident at once
+        best = s * c;
+        bcs = s;
+        bcc = c;
+      }
+    cs = bcs;
+    cc = bcc;
+  }
+  *cs_out = cs;
+  *cc_out = cc;
+}
+
 int attention_tc_cluster(long long items, int head_dim, int sm_count) {
   // CTAs per (request, kv head, row tile): about two waves of CTAs over the SMs,
   // at most kMaxCluster, halved while the device cannot hold the clusters one
@@ -754,6 +826,9 @@ bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_s
 cudaError_t launch_attention_tc(const AttnArgs& a, int B, const CUtensorMap& q, const CUtensorMap& k,
                                 const CUtensorMap& v, cudaStream_t s) {
   const int qc = a.q_copies;
+  if (a.cl_count < 1 || a.cl_count > kMaxCrossClusters ||
+      (a.cl_count > 1 && (B * a.n_kv_heads * a.n_row_tiles > kCrossItems || !a.xpart || !a.xml || !a.xcnt)))
+    return cudaErrorInvalidValue;
   if (a.cl_size < 1 || a.cl_size > kMaxCluster || a.q_rows < 1 || (qc != 1 && qc != 2 && qc != 4) ||
       a.q_rows * (a.n_heads / a.n_kv_heads) * qc > 128 || a.n_row_tiles < 1 ||
       !attention_tc_supported(a.head_dim, a.page_size, a.max_rows, a.max_seq_len))

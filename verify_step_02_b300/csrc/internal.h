@@ -206,7 +206,11 @@ struct AttnArgs {
   int x_pair;
   int kv_bf16;
   int pdl;                 // launched as a programmatic dependent of the previous kernel
-  int cl_size;             // tensor-core kernel: CTAs per (request, kv head, row tile), one cluster
+  int cl_size;             // tensor-core kernel: CTAs per cluster (request, kv head, row tile)
+  int cl_count;            // tensor-core kernel: clusters per (request, kv head, row tile), 1 .. kMaxCrossClusters
+  float* xpart;            //   cl_count > 1: [item][cluster][128 rows][head_dim] unnormalized partial outputs
+  float2* xml;             //   [item][cluster][128 rows] their (max, sum)
+  unsigned* xcnt;          //   [item][16] arrivals per (item, rank), zero between launches
   int q_rows;              // tensor-core kernel: block rows per row tile (q_rows * group <= 128)
   int n_row_tiles;         // tensor-core kernel: row tiles per request (ceil((max_gamma + 1) / q_rows))
   int q_copies;            // tensor-core kernel: copies of a tile's query rows in the 128 MMA rows
@@ -331,6 +335,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap& w, const CUtens
 bool attention_tc_supported(int head_dim, int page_size, int max_rows, int max_seq_len);
 // CTAs per (request, kv head, row tile) for `items` of them (a power of two, 1 .. 16).
 int attention_tc_cluster(long long items, int head_dim, int sm_count);
+// Cluster size and clusters per item: several clusters per item only for few items (<= kCrossItems).
+constexpr int kCrossItems = 64;
+constexpr int kMaxCrossClusters = 4;
+void attention_tc_split(long long items, int head_dim, int sm_count, int* cs, int* cc);
 cudaError_t tc_encode_kv_map(CUtensorMap* m, const void* pool, int n_pages, int n_kv, int head_dim);
 // q as hi/lo bf16 planes [2][m_max][n_heads][head_dim]; box (64 dims, group heads, rows tokens)
 cudaError_t tc_encode_q_map(CUtensorMap* m, const void* q, int m_max, int n_heads, int head_dim, int group,

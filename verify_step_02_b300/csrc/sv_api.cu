@@ -81,6 +81,9 @@ struct sv_model {
   unsigned* gemm_cnt = nullptr;
   float* attn_part = nullptr;
   unsigned* attn_cnt = nullptr;
+  float* attn_xpart = nullptr;     // tensor-core attention: partials of several clusters per item
+  float2* attn_xml = nullptr;
+  unsigned* attn_xcnt = nullptr;
   unsigned* status = nullptr;
   // staging for sv_verify_host
   int* d_tokens = nullptr;
@@ -428,8 +431,11 @@ sv_status run_verify(sv_model* m, int B, const int* tokens, const int* lens, con
         a.max_rows = a.q_rows * (c.n_heads / c.n_kv_heads);
         a.n_row_tiles = (max_block + a.q_rows - 1) / a.q_rows;
         const long long items = (long long)B * c.n_kv_heads * a.n_row_tiles;
-        a.cl_size = attention_tc_cluster(items, hd, m->sm_count);
-        a.trace = trace_slot(m, items * a.cl_size, kTrAttn);
+        attention_tc_split(items, hd, m->sm_count, &a.cl_size, &a.cl_count);
+        a.xpart = m->attn_xpart;
+        a.xml = m->attn_xml;
+        a.xcnt = m->attn_xcnt;
+        a.trace = trace_slot(m, items * a.cl_size * a.cl_count, kTrAttn);
         Timed t(m, SV_KC_ATTENTION, s);
         SV_CUDA(launch_attention_tc(a, B, m->map_q[ko], m->map_k[l], m->map_v[l], s), "attention");
       } else {
@@ -640,6 +646,12 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
   plan_attention(aa, c.max_batch, c.max_seq_len, c.max_gamma);
   TRY(dalloc(m, &m->attn_part, sizeof(float) * attention_partial_floats(aa, c.max_batch)));
   TRY(dalloc(m, &m->attn_cnt, sizeof(unsigned) * c.max_batch * c.n_kv_heads));
+  if (m->wbf16) {  // the tensor-core attention's cross-cluster merge (few work items)
+    const size_t slots = (size_t)kCrossItems * kMaxCrossClusters * 128;
+    TRY(dalloc(m, &m->attn_xpart, sizeof(float) * slots * c.head_dim));
+    TRY(dalloc(m, &m->attn_xml, sizeof(float2) * slots));
+    TRY(dalloc(m, &m->attn_xcnt, sizeof(unsigned) * kCrossItems * 16));
+  }
   TRY(dalloc(m, &m->status, sizeof(unsigned) * 4));
   TRY(dalloc(m, &m->d_tokens, sizeof(int) * c.max_batch * (c.max_gamma + 1)));
   TRY(dalloc(m, &m->d_probs, sizeof(float) * (size_t)c.max_batch * std::max(c.max_gamma, 1) * c.vocab));
@@ -699,6 +711,7 @@ sv_status sv_model_create(const sv_config* cfg, const sv_weights* weights, void*
     }
   }
   cudaError_t e = cudaMemsetAsync(m->gemm_cnt, 0, sizeof(unsigned) * cnt, s);
+  if (e == cudaSuccess && m->attn_xcnt) e = cudaMemsetAsync(m->attn_xcnt, 0, sizeof(unsigned) * kCrossItems * 16, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->attn_cnt, 0, sizeof(unsigned) * c.max_batch * c.n_kv_heads, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(unsigned) * 4, s);
   if (e == cudaSuccess) e = launch_rope_table(m->rope, c.max_seq_len, c.head_dim, c.rope_theta, s);
