@@ -63,7 +63,7 @@ def parse():
                     help="after the timed steps, run two traced steps and add a per-kernel timeline summary "
                          "(device %globaltimer per CTA) to the JSON line")
     ap.add_argument("--trace-out", default=None, help="with --trace: also save the raw per-CTA records (.npz)")
-    ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "w12g", "sampled"], default="8b",
+    ap.add_argument("--workload", choices=["8b", "tiny", "27b", "w12", "w12g", "sampled", "tree"], default="8b",
                     help="8b: the headline line (default); the others time the other verify configurations "
                          "(tiny greedy, 27B-class ragged batch 32, W12 weights at the 8B-class shapes, sampled "
                          "batch 64) and print their own line")
@@ -313,6 +313,31 @@ def make_plan(g, steps, vocab, gamma=GAMMA, p_keep=P_KEEP):
         expect.append(k)
         off = min(off + k + 1, len(g) - 1)
     return np.array(blocks, np.int32), np.array(expect, np.int32)
+
+
+TREE_NODES = 32
+
+
+def make_tree_plan(g, steps, vocab):
+    """Token trees of each step and their parents; the anchor advances as greedy tree acceptance
+    would (the deepest node whose path spells the greedy continuation)."""
+    import synth
+    blocks, parents = [], []
+    off = 0  # index in g of the current anchor
+    for s in range(steps):
+        par = synth.random_tree(TREE_NODES, 3, 60, s)
+        want = [int(x) for x in g[off + 1: off + 1 + TREE_NODES]]
+        tok = synth.tree_drafts(par, g[off], want, 0.9, vocab, 61, s)
+        depth, ok, k = [0] * TREE_NODES, [True] + [False] * (TREE_NODES - 1), 0
+        for i in range(1, TREE_NODES):
+            depth[i] = depth[par[i]] + 1
+            ok[i] = ok[par[i]] and depth[i] <= len(want) and int(tok[i]) == want[depth[i] - 1]
+            if ok[i]:
+                k = max(k, depth[i])
+        blocks.append([int(t) for t in tok])
+        parents.append([int(p) for p in par])
+        off = min(off + k + 1, len(g) - 1)
+    return np.array(blocks, np.int32), np.array(parents, np.int32)
 
 
 def step_bytes(shape):
@@ -836,6 +861,8 @@ WORKLOADS = {
     "27b": "27B-class bf16 ragged verify: 64 layers, d 5120, 40 q / 8 kv heads; batch 32, contexts uniform "
            "512-8192 on shuffled 16-token pages, verify lengths 1-16 by confidence truncation; greedy",
     "w12": "8B-class verify with W12 weights (16-binade window): batch 1, gamma 16, context 4096; greedy",
+    "tree": "8B-class bf16 token-tree verify: batch 1, random 32-node trees (at most 3 children per node) whose "
+            "drafts follow the engine's greedy continuation w.p. 0.9 per node, context 4096; greedy",
     "w12g": "8B-class verify with grouped W12 weights (N(0, 0.02) bf16 weights, per-64-row bases and escapes): "
             "batch 1, gamma 16, context 4096; greedy",
     "sampled": "tiny fp32 sampled verify: batch 64, context 2048, gamma 8, T = 1, rejection sampling",
@@ -872,6 +899,13 @@ def run_workload(args, world, rank, local):
         B, gamma = 32, 16
         ctx = rng.integers(512, 8193, size=B)
         lens = synth.truncated_verify_lens(B, gamma, 0.3, 31, 0)
+        wdev = sd.random_bf16_model(shape)
+    elif wl == "tree":
+        shape = shape_of("8b")
+        kind, wdtype, kvdt = "bf16", vs.SV_BF16, torch.bfloat16
+        B, gamma = 1, TREE_NODES - 1
+        ctx = np.full(B, CONTEXT)
+        lens = np.full(B, gamma)
         wdev = sd.random_bf16_model(shape)
     elif wl == "w12g":  # the random N(0, 0.02) bf16 model itself, packed losslessly
         shape = shape_of("8b")
@@ -923,7 +957,14 @@ def run_workload(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     blocks_d = None
-    if wl == "tiny":
+    if wl == "tree":
+        g = greedy_reference(model, kv, int(tok[0, 0].item()), steps_total * 12 + 24, gamma + 1)
+        tblocks, tparents = make_tree_plan(g, steps_total, V)
+        blocks_d = torch.from_numpy(tblocks).cuda()
+        parents_d = torch.from_numpy(tparents).cuda()
+        nodes = torch.zeros((1, gamma + 1), dtype=torch.int32, device="cuda")
+        seq.copy_(torch.from_numpy(ctx.astype(np.int32)))
+    elif wl == "tiny":
         # the configuration's draft rule: draft i is the target's greedy token with probability
         # 0.8^(i+1), from the same engine's greedy run (then the KV context is reset)
         g = greedy_reference(model, kv, int(tok[0, 0].item()), steps_total * (gamma + 1) + gamma + 8, gamma + 1)
@@ -932,6 +973,9 @@ def run_workload(args, world, rank, local):
         seq.copy_(torch.from_numpy(ctx.astype(np.int32)))
 
     def run(i):
+        if wl == "tree":
+            model.verify_tree(blocks_d[i:i + 1], parents_d[i:i + 1], lens, kv, acc, nxt, nodes)
+            return
         model.verify(tok if blocks_d is None else blocks_d[i:i + 1], lens, kv, acc, nxt, draft_probs=probs,
                      temperature=temperature, seed=1234 + i, request_ids=rid)
 
