@@ -343,7 +343,7 @@ def make_tree_plan(g, steps, vocab):
     return np.array(blocks, np.int32), np.array(parents, np.int32)
 
 
-def graph_replay(model, kv, blocks_d, args, stream):
+def graph_replay(model, kv, blocks_d, args, stream, world):
     """The same steps replayed from one CUDA graph of a verify (captured after a warm-up call with
     the same shape); each step copies its block into the graph's input buffer first. Returns timing
     and whether the replays accepted exactly as the direct launches did."""
@@ -369,6 +369,7 @@ def graph_replay(model, kv, blocks_d, args, stream):
         tok.copy_(blocks_d[i:i + 1])
         g.replay()
         accs[i:i + 1].copy_(acc1)
+    barrier(world)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     ev[0].record(stream)
@@ -379,6 +380,7 @@ def graph_replay(model, kv, blocks_d, args, stream):
         accs[i:i + 1].copy_(acc1)
         ev[j + 1].record(stream)
     torch.cuda.synchronize()
+    barrier(world)
     ms = ev[0].elapsed_time(ev[-1]) / args.steps
     return {"ms_per_step": round(ms, 4), "accepted": accs.cpu().numpy().tolist(),
             "per_step": [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)],
@@ -438,7 +440,7 @@ def run_ours(args, world, rank, local):
     t_ms = ev[0].elapsed_time(ev[-1])
     graph = None
     if not args.no_graph:
-        graph = graph_replay(model, kv, blocks_d, args, stream)
+        graph = graph_replay(model, kv, blocks_d, args, stream, world)
     acc_np = acc.cpu().numpy()[args.warmup:]
     direct_ms = t_ms / args.steps
     if graph is not None and "accepted" in graph:
