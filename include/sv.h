@@ -188,6 +188,12 @@ void sv_model_destroy(sv_model* model);
  * Writes the K/V of all M rows into their page slots, then commits
  * seq_len[r] += k_r + 1 (rows past the accepted prefix are left to be
  * overwritten). Asynchronous on `stream`.
+ * CUDA graphs: every per-call choice is made on the host from B, verify_lens
+ * and the model, and only kernels are launched, so after one call with the
+ * same B, verify_lens, pointers and temperature, a call made while `stream`
+ * is being captured records the whole step (programmatic dependencies
+ * included); replaying it recomputes with the current contents of the
+ * captured buffers (tokens, seq_len, draft_probs, KV pools).
  * Errors: SV_ERR_INVALID_ARG (B, L_r, NULL pointers; a temperature that is
  *         negative, not finite, or positive but below 1e-6, where z / T
  *         could overflow in float32), SV_ERR_CUDA (launch failure).
