@@ -190,7 +190,8 @@ void sv_model_destroy(sv_model* model);
  * overwritten). Asynchronous on `stream`.
  * CUDA graphs: every per-call choice is made on the host from B, verify_lens
  * and the model, and only kernels are launched, so after one call with the
- * same B, verify_lens, pointers and temperature, a call made while `stream`
+ * same B, verify_lens, pointers, temperature and seed (all fixed in the graph),
+ * a call made while `stream`
  * is being captured records the whole step (programmatic dependencies
  * included); replaying it recomputes with the current contents of the
  * captured buffers (tokens, seq_len, draft_probs, KV pools).
