@@ -25,7 +25,7 @@ def noalloc(wdtype, w, base, x, n, k):
     planes = 2 if x.dim() == 3 else 1
     m = int(x.shape[-2])
     y = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
-    mat = vs.Matrix(w.data_ptr(), int(base))
+    mat = vs.matrix(w) if isinstance(w, tuple) else vs.Matrix(w.data_ptr(), int(base))
     st = vs.lib.sv_linear_noalloc(int(wdtype), ctypes.byref(mat), n, k, ctypes.c_void_p(x.data_ptr()), planes, m,
                                   ctypes.c_void_p(y.data_ptr()),
                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -41,13 +41,17 @@ def make(kind, m, n, k, rng):
     wd = vs.SV_BF16
     if kind == "w12":
         (w, base), wd = vs.pack_w12(w), vs.SV_W12
+    if kind == "w12g":   # grouped W12 of N(0, 0.02) weights with exact zeros (escapes)
+        wn = (torch.randn((n, k), generator=torch.Generator().manual_seed(n + k)) * 0.02).to(torch.bfloat16)
+        wn[torch.rand((n, k), generator=torch.Generator().manual_seed(k)) < 0.01] = 0
+        w, wd = vs.pack_w12_grouped(wn.cuda()), vs.SV_W12
     xf = torch.from_numpy(rng.standard_normal((m, k)).astype(np.float32)).cuda()
     hi = xf.to(torch.bfloat16)
     return wd, w, base, torch.stack([hi, (xf - hi.float()).to(torch.bfloat16)])
 
 
 @pytest.mark.parametrize("kind,m,n,k", [("f32", 5, 688, 256), ("bf16", 17, 6144, 4096), ("bf16", 64, 4096, 12288),
-                                        ("w12", 17, 1024, 256), ("w12", 256, 688, 256)])
+                                        ("w12", 17, 1024, 256), ("w12", 256, 688, 256), ("w12g", 17, 1024, 512)])
 def test_noalloc_matches_linear_twice(kind, m, n, k):
     rng = np.random.default_rng(m * 7 + n)
     wd, w, base, x = make(kind, m, n, k, rng)
