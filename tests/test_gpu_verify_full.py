@@ -169,3 +169,47 @@ def test_w12_8b_shapes_four_layers_and_lm_head():
     assert err <= LOGIT_TOL["bf16"], err
     report_decisions("w12 8b shapes", [classify_greedy(lo, block[1:], acc[0], nxt[0])], 1)
     model.close()
+
+
+def test_8b_token_tree_matches_oracle():
+    """A 32-node token tree at the 8B-class shapes (context 4096): every node's logits, the accepted
+    path and the committed keys/values against the oracle's tree forward."""
+    from oracle import accept
+    from helpers import classify_tree
+    shape = synth.SHAPES["8b"]
+    C, n = 4096, 32
+    wdev = sd.random_bf16_model(shape)
+    table, n_pages = synth.contiguous_page_table([C + n], PAGE, (C + n) // PAGE + 2)
+    ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, torch.bfloat16, fill="normal")
+    seq = torch.tensor([C], dtype=torch.int32, device="cuda")
+    kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
+    rng = np.random.default_rng(6)
+    anchor = int(rng.integers(0, shape["vocab"]))
+    model = vs.Model(vs.make_config(shape, vs.SV_BF16, 1, n - 1, C + 64, PAGE, flags=vs.SV_FLAG_KEEP_LOGITS), wdev)
+    chain = engine_greedy_chain(model, kv, [anchor], 8, n - 1)[0]
+    parents = synth.random_tree(n, 3, 90, 0)
+    tokens = synth.tree_drafts(parents, anchor, chain, 0.9, shape["vocab"], 91, 0)
+    ctx = DeviceContext(ks, table[0], C, PAGE), DeviceContext(vs_, table[0], C, PAGE)
+    cfg, W = device_oracle_weights(shape, wdev)
+    lo, nk, nv = decoder.forward_tree(cfg, W, ctx[0], ctx[1], tokens, parents, C, rowwise=False)
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nodes = torch.zeros((1, n), dtype=torch.int32, device="cuda")
+    model.verify_tree(torch.from_numpy(np.asarray([tokens], np.int32)).cuda(),
+                      torch.from_numpy(np.asarray([parents], np.int32)).cuda(), [n - 1], kv, acc, nxt, nodes)
+    lg = model.logits(n).cpu().numpy().astype(np.float64)
+    model.sync_status()
+    err = np.abs(lg - lo).max()
+    k = int(acc.item())
+    k_o, _, _ = accept.greedy_accept_tree(lo, tokens, parents)
+    print(f"[8b tree] {n} nodes: max |dlogit| {err:.4f}, accepted {k} (oracle {k_o})")
+    assert err <= LOGIT_TOL["bf16"], err
+    report_decisions("8b token tree", [classify_tree(lo, tokens, parents, k, int(nxt.item()),
+                                                     nodes.cpu().numpy()[0])], 1)
+    assert int(seq.item()) == C + k + 1
+    path = [int(x) for x in nodes.cpu().numpy()[0, :k + 1]]
+    pos = C + np.arange(k + 1)
+    for l in (0, shape["n_layers"] - 1):
+        gk = sd.read_positions(ks[l], table[0], pos, PAGE).float().cpu().numpy()
+        assert np.allclose(gk, nk[l][path], rtol=2 ** -7, atol=1e-2)
+    model.close()
