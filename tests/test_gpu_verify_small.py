@@ -208,3 +208,54 @@ def test_tiny_sampled_batch64_ctx2048():
     assert "mismatch" not in verdicts, verdicts
     assert verdicts.count("near_tie") <= 2
     assert acc.sum() > 0
+
+
+def test_bf16_gqa_sampled_batch():
+    """T = 0.8 rejection sampling on the tensor-core path (bf16 GQA model, ragged contexts): chain
+    drafts q_i = softmax((z_{i-1} + N(0, 1)) / T) from the oracle's target logits, d_i ~ q_i."""
+    from helpers import report_decisions
+    shape = dict(n_layers=2, d_model=512, n_heads=8, n_kv_heads=2, head_dim=128, ffn=1024, vocab=4096,
+                 rope_theta=1e6)
+    hw = synth.host_weights(shape, "w12window")
+    for lay in hw["layers"]:
+        for name in ("wqkv", "wo", "wgu", "wd"):
+            lay[name] = (lay[name].astype(np.int64) - (4 << 7)).astype(np.uint16)
+    cfg, W = oracle_weights(shape, hw, "bf16")
+    B, gamma, T, seed = 6, 5, 0.8, 777
+    rng = np.random.default_rng(29)
+    ctx = [int(c) for c in rng.integers(1, 200, size=B)]
+    states, drafts, probs, logits_o = [], [], [], []
+    for r, c in enumerate(ctx):
+        stt = spec.empty_state(cfg, int(rng.integers(0, cfg.vocab)), request_id=500 + r)
+        stt.k = [decoder.round_to_bf16(rng.standard_normal((c, 2, 128))) for _ in range(2)]
+        stt.v = [decoder.round_to_bf16(rng.standard_normal((c, 2, 128))) for _ in range(2)]
+        work = stt.copy()
+        block, zs, qs = [stt.anchor], [], []
+        for i in range(gamma + 1):
+            z, nk, nv = decoder.forward_block(cfg, W, work.k, work.v, [block[-1]], work.length)
+            zs.append(z[0])
+            work.k = [np.concatenate([a, b]) for a, b in zip(work.k, nk)]
+            work.v = [np.concatenate([a, b]) for a, b in zip(work.v, nv)]
+            if i == gamma:
+                break
+            ql = accept.softmax(z[0] + rng.standard_normal(cfg.vocab), T).astype(np.float32)
+            ql = ql / ql.sum(dtype=np.float64)
+            block.append(int(rng.choice(cfg.vocab, p=ql.astype(np.float64) / ql.astype(np.float64).sum())))
+            qs.append(ql.astype(np.float32))
+        states.append(stt)
+        drafts.append(block[1:])
+        probs.append(np.stack(qs))
+        logits_o.append(np.stack(zs))
+    model = make_model(shape, "bf16", gpu_weights(hw, "bf16"), B, gamma, 512)
+    ks, vs_, table, seq = build_kv(shape, states, PAGE, gamma, "bf16")
+    kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
+    acc, nxt, lg = run_step(model, states, drafts, gamma, kv, temperature=T, probs=np.stack(probs), seed=seed,
+                            req_ids=[500 + r for r in range(B)])
+    verdicts = []
+    for r in range(B):
+        lo = logits_o[r]
+        err = np.abs(lg[r * (gamma + 1):(r + 1) * (gamma + 1)] - lo).max()
+        assert err <= LOGIT_TOL["bf16"], (r, err)
+        verdicts.append(classify_sampled(lo, drafts[r], probs[r], T, seed, 500 + r, ctx[r], acc[r], nxt[r]))
+    report_decisions("bf16 GQA sampled, T 0.8", verdicts, 1)
+    assert np.array_equal(seq.cpu().numpy(), np.array(ctx) + acc + 1)
