@@ -638,7 +638,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
             trace_mark(trec, 11);
           } else if (grpA) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) __stcg(mine + (ch * 32 + k) * kGemmBN, v[k]);
+            for (int k = 0; k < 32; ++k)  // (only the tile's tokens: the reducers read no others)
+              if (ch * 32 + k < mtot) __stcg(mine + (ch * 32 + k) * kGemmBN, v[k]);
           }
         }
         if (grpA) {
