@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sweep", choices=["none", "gemm", "step"], default="none",
+    ap.add_argument("--sweep", choices=["none", "gemm", "step", "schedule"], default="none",
                     help="gemm: the skinny GEMM alone per projection shape; step: the whole verify step of the "
                          "8B-class model per block size M (the step-cost table a prefix scheduler takes)")
     ap.add_argument("--sweep-m", default="17", help="comma-separated block sizes M for --sweep gemm")
@@ -922,6 +922,89 @@ def run_sweep_step(args, local):
             "note": "M rows per step (requests of up to 64 rows); M = 1 is autoregressive greedy decoding"}
 
 
+SCHED_B, SCHED_G = 8, 16
+SCHED_M = (8, 16, 24, 32, 40, 48, 64, 80, 96, 112, 136)
+
+
+def run_sweep_schedule(args, local):
+    """The prefix scheduler on the device's own step costs (8B-class model, 8 requests at context 4096).
+
+    Measures T(M) for M = 8 .. 136 rows (the requests' lengths as even as possible), interpolates a
+    table for every M, draws per-draft confidences c ~ Beta(8, 2) (the 27B workload's draft model),
+    chooses the verify lengths with sv_schedule_prefix (with and without early stop), times the
+    chosen lengths on the device and compares the expected throughput tau / T with two fixed
+    rules: all 16 drafts, and drafts kept while the survival probability stays >= 0.3.
+    """
+    import torch
+
+    import synth
+    import synth.device as sd
+    import verify_step_02_b300 as vs
+    torch.cuda.set_device(local)
+    shape = dict(synth.SHAPES["8b"], n_layers=args.layers or 36)
+    B, G = SCHED_B, SCHED_G
+    reps = (len(SCHED_M) + 4) * (args.steps + args.warmup)
+    max_seq = (CONTEXT + reps + 128 + PAGE - 1) // PAGE * PAGE
+    wdev = sd.random_bf16_model(shape)
+    table, n_pages = synth.contiguous_page_table([max_seq] * B, PAGE, max_seq // PAGE + 1)
+    ks, vs_ = sd.kv_pools(shape, n_pages, PAGE, torch.bfloat16, fill="normal")
+    seq = torch.full((B,), CONTEXT, dtype=torch.int32, device="cuda")
+    kv = vs.KVCache(ks, vs_, torch.from_numpy(table).cuda(), seq)
+    model = vs.Model(vs.make_config(shape, vs.SV_BF16, B, G, max_seq, PAGE), wdev)
+    rng = np.random.default_rng(8)
+    tok = torch.from_numpy(rng.integers(0, shape["vocab"], size=(B, G + 1)).astype(np.int32)).cuda()
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step_us(lens):
+        for _ in range(args.warmup):
+            model.verify(tok, lens, kv, acc, nxt)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            model.verify(tok, lens, kv, acc, nxt)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        seq.fill_(CONTEXT)
+        return e0.elapsed_time(e1) / args.steps * 1e3
+
+    measured = {}
+    for M in SCHED_M:
+        lens = [M // B - 1 + (1 if r < M % B else 0) for r in range(B)]
+        measured[M] = step_us(lens)
+    ms = np.array(SCHED_M, dtype=np.float64)
+    table_us = np.interp(np.arange(1, SCHED_M[-1] + 1), ms, [measured[m] for m in SCHED_M])
+    conf = synth.rng(31, 1).beta(8.0, 2.0, size=(B, G)).astype(np.float32)
+    surv = np.cumprod(conf.astype(np.float64), axis=1)
+
+    def tau(lens):
+        return float(sum(1.0 + surv[r, :lens[r]].sum() for r in range(B)))
+
+    rules = {}
+    for name, lens in (("fixed gamma 16", [G] * B),
+                       ("survival >= 0.3", [max(1, int((surv[r] >= 0.3).sum())) for r in range(B)])):
+        rules[name] = [int(x) for x in lens]
+    for early in (False, True):
+        lens, _, _ = vs.schedule_prefix(conf, table_us.astype(np.float32), early_stop=early)
+        rules["scheduler" + (" (early stop)" if early else "")] = [int(x) for x in lens]
+    out = {}
+    for name, lens in rules.items():
+        M = int(sum(l + 1 for l in lens))
+        t_tab = float(table_us[M - 1])
+        t_dev = step_us(lens)
+        out[name] = {"verify_lens": lens, "M": M, "expected_tokens": round(tau(lens), 3),
+                     "table_us": round(t_tab, 1), "device_us": round(t_dev, 1),
+                     "expected_tokens_per_s": round(tau(lens) / (t_dev * 1e-6), 1)}
+    model.close()
+    return {"sweep": "schedule", "model": "8B-class bf16", "layers": shape["n_layers"], "batch": B, "gamma": G,
+            "context": CONTEXT, "step_us_measured": {str(m): round(v, 1) for m, v in measured.items()},
+            "rules": out,
+            "note": "expected tokens = sum_r (1 + sum_{j <= L_r} prod_{i <= j} c_{r,i}), c ~ Beta(8, 2); "
+                    "device_us times the chosen lengths on this GPU"}
+
+
 # ------------------------------------------------------------------ the other configurations
 WORKLOADS = {
     "tiny": "tiny fp32 greedy verify: 2 layers, d 256, 4 x 64 heads, vocab 1024; batch 1, gamma 4, context 64",
@@ -1126,6 +1209,8 @@ def main():
         res = run_sweep(args, local)
     elif args.sweep == "step":
         res = run_sweep_step(args, local)
+    elif args.sweep == "schedule":
+        res = run_sweep_schedule(args, local)
     elif args.workload != "8b" and args.impl == "ours":
         res = run_workload(args, world, rank, local)
     elif args.impl == "reference":
