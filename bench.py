@@ -343,28 +343,29 @@ def make_tree_plan(g, steps, vocab):
     return np.array(blocks, np.int32), np.array(parents, np.int32)
 
 
-def graph_replay(model, kv, blocks_d, args, stream, world):
+def graph_replay(model, kv, blocks_d, args, stream, world, gamma=GAMMA, context=CONTEXT):
     """The same steps replayed from one CUDA graph of a verify (captured after a warm-up call with
     the same shape); each step copies its block into the graph's input buffer first. Returns timing
-    and whether the replays accepted exactly as the direct launches did."""
+    and whether the replays accepted exactly as the direct launches did (one request of `gamma`
+    drafts whose KV context starts at `context` tokens)."""
     import torch
-    tok = torch.zeros((1, GAMMA + 1), dtype=torch.int32, device="cuda")
+    tok = torch.zeros((1, gamma + 1), dtype=torch.int32, device="cuda")
     acc1 = torch.zeros(1, dtype=torch.int32, device="cuda")
     nxt1 = torch.zeros(1, dtype=torch.int32, device="cuda")
     n = args.warmup + args.steps
     accs = torch.zeros(n, dtype=torch.int32, device="cuda")
-    kv.seq_len.fill_(CONTEXT)
+    kv.seq_len.fill_(context)
     tok.copy_(blocks_d[0:1])
-    model.verify(tok, [GAMMA], kv, acc1, nxt1)   # warm-up: first-call setup outside the capture
+    model.verify(tok, [gamma], kv, acc1, nxt1)   # warm-up: first-call setup outside the capture
     torch.cuda.synchronize()
-    kv.seq_len.fill_(CONTEXT)
+    kv.seq_len.fill_(context)
     g = torch.cuda.CUDAGraph()
     try:
         with torch.cuda.graph(g):
-            model.verify(tok, [GAMMA], kv, acc1, nxt1)
+            model.verify(tok, [gamma], kv, acc1, nxt1)
     except Exception as e:  # noqa: BLE001 - reported, not fatal
         return {"unavailable": f"capture failed: {e}"}
-    kv.seq_len.fill_(CONTEXT)   # the capture ran nothing; start from the same context
+    kv.seq_len.fill_(context)   # the capture ran nothing; start from the same context
     for i in range(args.warmup):
         tok.copy_(blocks_d[i:i + 1])
         g.replay()
@@ -1122,11 +1123,15 @@ def run_workload(args, world, rank, local):
         blocks_d = torch.from_numpy(blocks).cuda()
         seq.copy_(torch.from_numpy(ctx.astype(np.int32)))
 
+    # one request: every step's accepted count kept apart (compared with the graph replays)
+    acc_steps = torch.zeros(steps_total, dtype=torch.int32, device="cuda")
+
     def run(i):
         if wl == "tree":
             model.verify_tree(blocks_d[i:i + 1], parents_d[i:i + 1], lens, kv, acc, nxt, nodes)
             return
-        model.verify(tok if blocks_d is None else blocks_d[i:i + 1], lens, kv, acc, nxt, draft_probs=probs,
+        a_out = acc_steps[i:i + 1] if wl == "tiny" else acc
+        model.verify(tok if blocks_d is None else blocks_d[i:i + 1], lens, kv, a_out, nxt, draft_probs=probs,
                      temperature=temperature, seed=1234 + i, request_ids=rid)
 
     clocks = ClockSampler(local)
@@ -1144,6 +1149,20 @@ def run_workload(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     seq_end = seq.cpu().numpy().astype(np.int64)
+    graph = None
+    if wl == "tiny" and not args.no_graph:
+        # the same steps replayed from one CUDA graph of the verify; the headline when the
+        # replays accept exactly as the direct launches did
+        direct = acc_steps.cpu().numpy()[args.warmup:].tolist()
+        graph = graph_replay(model, kv, blocks_d, args, stream, world, gamma=gamma, context=int(ctx[0]))
+        if "accepted" in graph:
+            graph["same_decisions_as_direct"] = graph.pop("accepted")[args.warmup:] == direct
+            g_steps = graph.pop("per_step")
+            graph["direct_ms_per_step"] = round(ev[0].elapsed_time(ev[-1]) / args.steps, 4)
+            if graph["same_decisions_as_direct"]:
+                per_step_graph = g_steps
+                t_ms = graph["ms_per_step"] * args.steps
+        seq.copy_(torch.from_numpy(seq_end.astype(np.int32)))
     # per-kernel-class device time from an instrumented pass (events between launches)
     model.set_timing(True)
     for j in range(args.steps):
@@ -1169,7 +1188,10 @@ def run_workload(args, world, rank, local):
             np.savez_compressed(args.trace_out, records=raw, launches=np.array([l[:2] for l in launches]),
                                 kinds=np.array([l[2] for l in launches]))
     per_step = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
-    t_ms = ev[0].elapsed_time(ev[-1])
+    if graph is not None and graph.get("same_decisions_as_direct"):
+        per_step = per_step_graph
+    else:
+        t_ms = ev[0].elapsed_time(ev[-1])
     tokens = float((seq_end - seq_start).sum())  # accepted drafts + 1 per request per step
     value, t_max = aggregate(tokens, t_ms, world)
     if rank != 0:
@@ -1198,6 +1220,9 @@ def run_workload(args, world, rank, local):
                 "peak_kind": peak_kind, "bound_ms": round(step_alg / (peak * 1e9) * 1e3, 4)},
         "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in tim.items()},
         "clocks": clk,
+        "launch": "CUDA graph replay" if graph is not None and graph.get("same_decisions_as_direct")
+        else "direct launches",
+        **({"graph": graph} if graph else {}),
         **({"trace": trace} if trace else {}),
     }
 

@@ -41,18 +41,26 @@ template <typename KVT>
 __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
   static_assert(sizeof(KVT) == 4, "the CUDA-core attention reads float32 caches");
   extern __shared__ __align__(16) float sm[];
-  pdl_wait();
-  pdl_trigger();
+  // The lengths, row ranges, page table and the keys cached before this step
+  // were written two or more kernels back (every kernel triggers its dependents
+  // only after its own wait): they are read before the dependency wait; the
+  // queries and the block's own keys after it.
   const int hd = a.head_dim, nkv = a.n_kv_heads, group = a.n_heads / nkv;
   const int r = blockIdx.x / nkv, h = blockIdx.x - r * nkv, chunk = blockIdx.y;
   const int C = a.seq_len[r];
   const int row0 = a.req_row0[r], nrows = a.req_row0[r + 1] - row0;
   const int T = C + nrows;
   if (C < 0 || T > a.max_seq_len) {  // flagged by the row preparation; nothing is read or merged
+    pdl_wait();
+    pdl_trigger();
     return;
   }
   const int kbeg = chunk * a.chunk;
-  if (kbeg >= T) return;
+  if (kbeg >= T) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   const int kend = min(T, kbeg + a.chunk);
   const int nchunks = (T + a.chunk - 1) / a.chunk;
   const int R = nrows * group;
@@ -81,17 +89,6 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
     }
     pages[i] = page;
   }
-  const float scale = rsqrtf(static_cast<float>(hd));
-  for (int idx = tid; idx < R * hd; idx += blockDim.x) {
-    const int rho = idx / hd, d = idx - rho * hd;
-    const int j = rho / group, g = rho - j * group;
-    Qs[idx] = a.q[(long long)(row0 + j) * nq + (h * group + g) * hd + d] * scale;
-    Os[idx] = 0.f;
-  }
-  for (int rho = tid; rho < R; rho += blockDim.x) {
-    mrow[rho] = -INFINITY;
-    lrow[rho] = 0.f;
-  }
   __syncthreads();
   const float* kc = reinterpret_cast<const float*>(a.k_cache);
   const float* vc = reinterpret_cast<const float*>(a.v_cache);
@@ -115,8 +112,25 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
     }
     cp_async_commit();
   };
+  // the first tile goes out before the wait when all its keys are cached context
+  const bool early = kbeg + KT <= C;
+  if (early) load_tile(0, 0);
+  pdl_wait();
+  pdl_trigger();
+  const float scale = rsqrtf(static_cast<float>(hd));
+  for (int idx = tid; idx < R * hd; idx += blockDim.x) {
+    const int rho = idx / hd, d = idx - rho * hd;
+    const int j = rho / group, g = rho - j * group;
+    Qs[idx] = a.q[(long long)(row0 + j) * nq + (h * group + g) * hd + d] * scale;
+    Os[idx] = 0.f;
+  }
+  for (int rho = tid; rho < R; rho += blockDim.x) {
+    mrow[rho] = -INFINITY;
+    lrow[rho] = 0.f;
+  }
+  __syncthreads();
   const int ntiles = (kend - kbeg + KT - 1) / KT;
-  load_tile(0, 0);
+  if (!early) load_tile(0, 0);
   for (int t = 0; t < ntiles; ++t) {
     const int b = t & 1;
     if (t + 1 < ntiles) {
@@ -186,6 +200,17 @@ __global__ void __launch_bounds__(256) attn_fma_kernel(const AttnArgs a) {
     __syncthreads();  // the buffer is reloaded two tiles on
   }
 
+  if (nchunks == 1) {
+    // the only chunk: its running softmax is the row's, normalized here
+    for (int idx = tid; idx < R * hd; idx += blockDim.x) {
+      const int rho = idx / hd, d = idx - rho * hd;
+      const int j = rho / group, g = rho - j * group;
+      const float L = lrow[rho];
+      store_x(a.out, a.out_plane, (long long)(row0 + j) * nq + (h * group + g) * hd + d, L > 0.f ? Os[idx] / L : 0.f,
+              a.x_pair);
+    }
+    return;
+  }
   // partial of this chunk: per row [m, l, O[hd]]
   const int item = blockIdx.x;  // (r, h)
   const int stride = hd + 2;

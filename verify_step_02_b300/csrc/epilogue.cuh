@@ -378,14 +378,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, float* 
 // a fixed order, so results do not depend on arrival order — resets the
 // counter and returns true with the sum in ys.
 __device__ __forceinline__ bool splitk_reduce(const GemmArgs& a, int tile_id, int split, const float* mine,
-                                              float* ys, int ldys, int rows, int cols) {
+                                              float* ys, int ldys, int rows, int cols, int live) {
   __shared__ unsigned s_last;
   const int tid = threadIdx.x, nthr = blockDim.x;
   float* base = a.partials + (long long)tile_id * a.k_splits * rows * cols;
   float* dst = base + (long long)split * rows * cols;
-  for (int idx = tid; idx < rows * cols; idx += nthr) {
-    const int t = idx / cols, c = idx - t * cols;
-    __stcg(dst + idx, mine[t * ldys + c]);
+  // only the tile's live token columns (the rest is padding past the block)
+  const int n = rows * live;
+  for (int idx = tid; idx < n; idx += nthr) {
+    const int t = idx / live, c = idx - t * live;
+    __stcg(dst + t * cols + c, mine[t * ldys + c]);
   }
   __threadfence();
   __syncthreads();
@@ -393,10 +395,19 @@ __device__ __forceinline__ bool splitk_reduce(const GemmArgs& a, int tile_id, in
   __syncthreads();
   if (!s_last) return false;
   __threadfence();
-  for (int idx = tid; idx < rows * cols; idx += nthr) {
+  constexpr int U = 8;  // partials whose loads are in flight together, summed in split order
+  const long long pstride = (long long)rows * cols;
+  for (int idx = tid; idx < n; idx += nthr) {
+    const int t = idx / live, c = idx - t * live;
+    const float* p = base + t * cols + c;
     float s = 0.f;
-    for (int sp = 0; sp < a.k_splits; ++sp) s += __ldcg(base + (long long)sp * rows * cols + idx);
-    const int t = idx / cols, c = idx - t * cols;
+    for (int sp0 = 0; sp0 < a.k_splits; sp0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = sp0 + u < a.k_splits ? __ldcg(p + (sp0 + u) * pstride) : 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) s += v[u];
+    }
     ys[t * ldys + c] = s;
   }
   if (tid == 0) a.counters[tile_id] = 0u;

@@ -95,8 +95,6 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   __shared__ __align__(16) float Ws[KC][WS_LD];
   __shared__ __align__(16) float Xs[KC][XS_LD];
   __shared__ __align__(16) float Ys[BN * YS_LD];
-  pdl_wait();
-  pdl_trigger();
   const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
   const int tid = threadIdx.x;
   const int tr = (tid & 15) * 8, tc = (tid >> 4) * 2;
@@ -110,20 +108,26 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   const int wrow = weight_row(a, nt, lrow);
   const int xtok = tid >> 3, xkk = (tid & 7) * 4;          // X loader: one token, 4 k
   const int xm = m0 + xtok;
+  // this thread's 16 weights of the K step at k0, one step ahead of the products
+  float wv16[16];
+  auto fetch_w = [&](int k0) {
+    const int k = k0 + lkk;
+    if (wrow >= 0 && k < kend) {
+      load_w16<WT>(a, wrow, k, wv16);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wv16[i] = 0.f;
+    }
+  };
+  // the weights are never written by the step: the first step's are requested
+  // before waiting for the kernels that produce x
+  fetch_w(kbeg);
+  pdl_wait();
+  pdl_trigger();
 
   for (int k0 = kbeg; k0 < kend; k0 += KC) {
-    {
-      float v[16];
-      const int k = k0 + lkk;
-      if (wrow >= 0 && k < kend) {
-        load_w16<WT>(a, wrow, k, v);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) Ws[lkk + i][lrow] = v[i];
-    }
+    for (int i = 0; i < 16; ++i) Ws[lkk + i][lrow] = wv16[i];
     {
       const int k = k0 + xkk;
 #pragma unroll
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
       }
     }
     __syncthreads();
+    if (k0 + KC < kend) fetch_w(k0 + KC);
 #pragma unroll 4
     for (int k = 0; k < KC; ++k) {
       const float4 w0 = *reinterpret_cast<const float4*>(&Ws[k][tr]);
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   __syncthreads();
   const int mcount = min(BM, a.M - m0);
   if (a.k_splits > 1) {
-    if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM)) return;
+    if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM, mcount)) return;
   }
   __shared__ EpiSmem esm;
   epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x, esm, nullptr, [] { __syncthreads(); });
