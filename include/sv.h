@@ -36,11 +36,9 @@
  *   - The library never aborts the process and never traps on the device.
  *     Device-side checks (token ids, page ids) record a status word that
  *     sv_model_sync_status() reads back; the offending rows are skipped.
- *   - Models, tensor maps and the static scratch of sv_linear_noalloc hold
- *     device addresses of the context they were made in. cudaDeviceReset
- *     ends that context: destroy every model before it, and do not use the
- *     library across it (sv_linear_noalloc keeps the scratch address it
- *     looked up, which a reset invalidates).
+ *   - Models and their tensor maps hold device addresses of the context they
+ *     were made in. cudaDeviceReset ends that context: destroy every model
+ *     before it.
  */
 #ifndef SV_H
 #define SV_H
@@ -395,20 +393,13 @@ sv_status sv_linear(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, co
  * CUDA-core (FMA) plan of the product, whatever the weight type: its result
  * equals sv_linear's within rounding (not bit for bit, since sv_linear takes
  * the tensor-core path for bf16/W12 weights), and for large bf16/W12 shapes it
- * is much slower. The split-K scratch (partial tiles and tile counters) lives
- * in a 16 MiB static device array inside the library, which every GPU that
- * loads the library keeps until the process exits.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current. Make that first call
- *     before any stream capture.
- *   - A shape whose scratch would exceed 16 MiB is rejected with
- *     SV_ERR_INVALID_ARG; sv_last_error() gives the bytes it would need.
- *   - Each call clears the tile counters (cudaMemsetAsync on `stream`)
- *     before its launch. No call allocates or frees memory.
- *   - All calls share the one array, and it keeps the last call's contents:
- *     calls whose work overlaps on the GPU (several streams, or several host
- *     threads) race on it and produce wrong results. Serialize them, for
- *     example on one stream.
+ * is much slower. That plan splits K over at most 8 CTAs of one thread-block
+ * cluster, which add their partial tiles in distributed shared memory, so the
+ * call needs no scratch: it allocates nothing, keeps no state between calls,
+ * and calls on several streams or host threads may overlap. It launches one
+ * kernel on `stream` and returns (asynchronous; capturable in a CUDA graph).
+ * Errors: SV_ERR_INVALID_ARG as for sv_linear; SV_ERR_CUDA when the launch
+ * fails (for example N beyond 65535 tiles of 128 rows).
  */
 sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32_t N, int32_t K, const void* x,
                             int32_t x_planes, int32_t M, float* y, void* stream);

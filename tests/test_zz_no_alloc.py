@@ -2,9 +2,9 @@
 
 Callers that must not allocate device memory while they run (cudaMalloc can
 synchronize the device; some hosts own every allocation) use this entry
-point. Its split-K scratch is a 16 MiB static device array in the library,
-shared by every call, so each case below calls it twice in a row to check
-that the second call is not disturbed by what the first left behind.
+point. Its K splits meet in distributed shared memory within one cluster, so
+it keeps no state between calls; each case below still calls it twice in a row
+to check that the second call gives the same result.
 """
 import ctypes
 
@@ -17,9 +17,6 @@ torch = pytest.importorskip("torch")
 import synth  # noqa: E402
 import synth.device as sd  # noqa: E402
 import verify_step_02_b300 as vs  # noqa: E402
-
-SCRATCH = 16 << 20
-
 
 def noalloc(wdtype, w, base, x, n, k):
     planes = 2 if x.dim() == 3 else 1
@@ -66,18 +63,26 @@ def test_noalloc_matches_linear_twice(kind, m, n, k):
         assert np.abs(got - want).max() / scale < 1e-5
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
-    m, k = 32, 64
-    for n_tiles in range(1, 4000):
-        n = n_tiles * 128
-        # the allocation-free product runs the CUDA-core plan for every weight type,
-        # whose scratch is what sv_linear_workspace_bytes reports for float32 weights
-        if vs.lib.sv_linear_workspace_bytes(vs.SV_F32, m, n, k) > SCRATCH:
-            break
-    else:
-        pytest.skip("no shape on this GPU needs more than the static scratch")
-    w = torch.zeros((n, k), dtype=torch.bfloat16, device="cuda")
-    x = torch.zeros((m, k), dtype=torch.bfloat16, device="cuda")
-    st, _ = noalloc(vs.SV_BF16, w, 0, x, n, k)
-    assert st == vs.SV_ERR_INVALID_ARG
-    assert b"static scratch" in vs.lib.sv_last_error()
+def test_noalloc_wide_shape_and_overlapping_streams():
+    # 65536 x 64 weights at 32 tokens: a shape whose split-K partials (2 splits x 512
+    # tiles x 16 KB) would not have fit a fixed scratch; two calls on two streams
+    # at once may overlap, since the calls share no state
+    m, n, k = 32, 65536, 64
+    rng = np.random.default_rng(65)
+    wd, w, base, x = make("bf16", m, n, k, rng)
+    want, _ = vs.linear(wd, w, x, n, k, base=base)
+    want = want.cpu().numpy().astype(np.float64)
+    scale = np.abs(want).max() + 1e-30
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ys = []
+    for s in (s1, s2):
+        with torch.cuda.stream(s):
+            st, y = noalloc(wd, w, base, x, n, k)
+            assert st == vs.SV_OK, vs.lib.sv_last_error()
+            ys.append(y)
+    torch.cuda.synchronize()
+    for y in ys:
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert np.abs(got - want).max() / scale < 1e-5

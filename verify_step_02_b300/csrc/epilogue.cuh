@@ -373,46 +373,4 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int nt, float* 
   }
 }
 
-// Split-K hand-off. Each split writes its partial tile; the last split to
-// arrive (per-tile counter, no waiting) sums the partials in split order —
-// a fixed order, so results do not depend on arrival order — resets the
-// counter and returns true with the sum in ys.
-__device__ __forceinline__ bool splitk_reduce(const GemmArgs& a, int tile_id, int split, const float* mine,
-                                              float* ys, int ldys, int rows, int cols, int live) {
-  __shared__ unsigned s_last;
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  float* base = a.partials + (long long)tile_id * a.k_splits * rows * cols;
-  float* dst = base + (long long)split * rows * cols;
-  // only the tile's live token columns (the rest is padding past the block)
-  const int n = rows * live;
-  for (int idx = tid; idx < n; idx += nthr) {
-    const int t = idx / live, c = idx - t * live;
-    __stcg(dst + t * cols + c, mine[t * ldys + c]);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.counters + tile_id, 1u) == (unsigned)(a.k_splits - 1);
-  __syncthreads();
-  if (!s_last) return false;
-  __threadfence();
-  constexpr int U = 8;  // partials whose loads are in flight together, summed in split order
-  const long long pstride = (long long)rows * cols;
-  for (int idx = tid; idx < n; idx += nthr) {
-    const int t = idx / live, c = idx - t * live;
-    const float* p = base + t * cols + c;
-    float s = 0.f;
-    for (int sp0 = 0; sp0 < a.k_splits; sp0 += U) {
-      float v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = sp0 + u < a.k_splits ? __ldcg(p + (sp0 + u) * pstride) : 0.f;
-#pragma unroll
-      for (int u = 0; u < U; ++u) s += v[u];
-    }
-    ys[t * ldys + c] = s;
-  }
-  if (tid == 0) a.counters[tile_id] = 0u;
-  __syncthreads();
-  return true;
-}
-
 }  // namespace sv

@@ -7,10 +7,14 @@
 // three nibble planes to bf16 on the way, SpecPilot digest, "Reasons") and
 // every thread then runs an 8 x 2 register-blocked FMA loop. Activations are
 // read as float32 (a hi/lo pair is summed on load). K is split
-// across CTAs until the grid covers the GPU; the last split of a tile reduces
-// the partials in a fixed order and runs the projection's epilogue.
+// across CTAs (at most 8 splits) until the grid covers the GPU. The splits of
+// a tile form one thread-block cluster: each rank sums a slice of the tile's
+// rows over every split's partial (distributed shared memory, in split order,
+// so results do not depend on timing) into rank 0, which runs the
+// projection's epilogue.
 #include "epilogue.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace sv {
 namespace {
@@ -90,12 +94,12 @@ __device__ __forceinline__ void load_w16(const GemmArgs& a, int row, int k, floa
   }
 }
 
-template <int WT>
+template <int WT, bool CL>
 __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   __shared__ __align__(16) float Ws[KC][WS_LD];
   __shared__ __align__(16) float Xs[KC][XS_LD];
   __shared__ __align__(16) float Ys[BN * YS_LD];
-  const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
+  const int ks = blockIdx.x, nt = blockIdx.y, mt = blockIdx.z;
   const int tid = threadIdx.x;
   const int tr = (tid & 15) * 8, tc = (tid >> 4) * 2;
   const int m0 = mt * BM;
@@ -162,11 +166,39 @@ __global__ void __launch_bounds__(256) gemm_fma_kernel(const GemmArgs a) {
   }
   __syncthreads();
   const int mcount = min(BM, a.M - m0);
-  if (a.k_splits > 1) {
-    if (!splitk_reduce(a, nt * a.m_tiles + mt, ks, Ys, Ys, YS_LD, BN, BM, mcount)) return;
+  if (CL) {
+    // the tile's splits are one cluster, rank = split: rank r sums rows
+    // [r rpr, (r + 1) rpr) of the live columns over every split, in split order
+    const int cs = a.k_splits, rank = static_cast<int>(tc::cluster_ctarank());
+    tc::cluster_sync();  // every split's partial is in its shared memory
+    const int rpr = (BN + cs - 1) / cs, r0 = rank * rpr, r1 = min(BN, r0 + rpr);
+    const int n = (r1 - r0) * mcount;
+    const uint32_t ys0 = tc::smem_u32(Ys);
+    for (int idx = tid; idx < n; idx += blockDim.x) {
+      const int tt = idx / mcount, c = idx - tt * mcount;
+      const uint32_t off = ys0 + 4u * static_cast<uint32_t>((r0 + tt) * YS_LD + c);
+      float v[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) v[p] = p < cs ? tc::ld_dsmem_f32(tc::mapa_shared(off, static_cast<uint32_t>(p))) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) sum += v[p];
+      tc::st_dsmem_f32(tc::mapa_shared(off, 0u), sum);
+    }
+    tc::cluster_sync();  // rank 0 holds the sums; no rank leaves while its partial may be read
+    if (rank != 0) return;
   }
   __shared__ EpiSmem esm;
   epilogue_tile(a, nt, Ys, YS_LD, m0, mcount, threadIdx.x, blockDim.x, esm, nullptr, [] { __syncthreads(); });
+}
+
+template <int WT>
+cudaError_t launch_wt(const GemmArgs& a, dim3 grid, cudaStream_t s) {
+  if (a.k_splits > 1) {
+    if (a.cl_size != a.k_splits || a.cl_size > kFmaMaxCluster) return cudaErrorInvalidValue;
+    return launch_k_cluster(gemm_fma_kernel<WT, true>, grid, dim3(256), 0, s, a.pdl != 0, a.cl_size, a);
+  }
+  return launch_k(gemm_fma_kernel<WT, false>, grid, dim3(256), 0, s, a.pdl != 0, a);
 }
 
 }  // namespace
@@ -182,22 +214,27 @@ void plan_gemm(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count) {
   const int ksteps = (K + KC - 1) / KC;
   int splits = (target + base - 1) / base;
   if (splits > ksteps) splits = ksteps;
+  if (splits > kFmaMaxCluster) splits = kFmaMaxCluster;
   if (splits < 1) splits = 1;
   const int steps_per = (ksteps + splits - 1) / splits;
   a.k_chunk = steps_per * KC;
   a.k_splits = (K + a.k_chunk - 1) / a.k_chunk;
+  a.cl_size = a.k_splits > 1 ? a.k_splits : 0;
 }
 
+// (the splits meet in distributed shared memory: no partial tiles in global memory)
 size_t gemm_partial_floats(const GemmArgs& a) {
-  return a.k_splits > 1 ? (size_t)a.n_tiles * a.m_tiles * a.k_splits * BN * BM : 0;
+  (void)a;
+  return 0;
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  const dim3 grid(a.n_tiles, a.m_tiles, a.k_splits);
+  if (a.n_tiles > 65535 || a.m_tiles > 65535) return cudaErrorInvalidValue;  // grid y / z limits
+  const dim3 grid(a.k_splits, a.n_tiles, a.m_tiles);  // a cluster spans one tile's splits (x)
   switch (a.wdtype) {
-    case SV_F32: return launch_k(gemm_fma_kernel<SV_F32>, grid, dim3(256), 0, s, a.pdl != 0, a);
-    case SV_BF16: return launch_k(gemm_fma_kernel<SV_BF16>, grid, dim3(256), 0, s, a.pdl != 0, a);
-    case SV_W12: return launch_k(gemm_fma_kernel<SV_W12>, grid, dim3(256), 0, s, a.pdl != 0, a);
+    case SV_F32: return launch_wt<SV_F32>(a, grid, s);
+    case SV_BF16: return launch_wt<SV_BF16>(a, grid, s);
+    case SV_W12: return launch_wt<SV_W12>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

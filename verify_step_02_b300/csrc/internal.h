@@ -15,6 +15,7 @@ constexpr int kMaxGamma = 255;        // largest block beyond the anchor (drafts
 constexpr int kGemmBN = 128;          // weight rows per GEMM tile (both GEMM paths)
 constexpr int kFmaBM = 32;            // tokens per FMA GEMM tile
 constexpr int kFmaKC = 32;            // K step of the FMA GEMM
+constexpr int kFmaMaxCluster = 8;     // FMA GEMM: K splits reduced within one cluster (portable size)
 
 // Device status word bits (sv_model_sync_status).
 // kStBadPos and kStNoPage mean the block does not fit the request's KV capacity

@@ -1,41 +1,13 @@
 // sv_linear_noalloc: the skinny weight-streaming product of sv_linear for
-// callers that cannot allocate device memory. Its split-K scratch (partial
-// tiles and tile counters) lives in one file-scope device array that every
-// GPU loading this library holds until the process exits.
-#include <cstdio>
+// callers that cannot allocate device memory. It runs the CUDA-core plan,
+// whose K splits meet in distributed shared memory within thread-block
+// clusters, so it needs no device scratch at all: no allocation, no shared
+// state between calls.
 #include <cstring>
-#include <mutex>
 
 #include "internal.h"
 
 namespace {
-
-constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB
-
-// Device-side scratch. In host code this name is only a host stand-in for the
-// symbol: kernels get the device address that cudaGetSymbolAddress returns.
-static __device__ __align__(256) unsigned char g_linear_scratch[kScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per device.
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_linear_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
-}
 
 sv_status reject(sv_status st, const char* msg) {
   sv::record_error(msg);
@@ -73,27 +45,13 @@ extern "C" sv_status sv_linear_noalloc(int32_t wdtype, const sv_matrix* w, int32
   a.x_kind = wdtype == SV_F32 ? kXF32 : (x_planes == 2 ? kXPair : kXBf16);
   a.x_plane = (long long)M * K;
   plan_gemm(a, M, N, K, kPairNone, sm);
-  const size_t cnt_bytes = ((size_t)a.n_tiles * a.m_tiles * sizeof(unsigned) + 255) & ~(size_t)255;
-  const size_t need = cnt_bytes + gemm_partial_floats(a) * sizeof(float);
-  if (need > kScratchBytes) {
-    char buf[160];
-    snprintf(buf, sizeof buf, "this shape needs %zu bytes of scratch, more than the %zu-byte static scratch", need,
-             kScratchBytes);
-    return reject(SV_ERR_INVALID_ARG, buf);
-  }
-  void* scratch = nullptr;
-  cudaError_t e = scratch_address(&scratch);
-  if (e != cudaSuccess) return reject(SV_ERR_CUDA, cudaGetErrorString(e));
+  a.counters = nullptr;  // (the plan keeps its splits within one cluster: no counters, no partials)
+  a.partials = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the tile counters must start at zero whatever an earlier call left behind
-  e = cudaMemsetAsync(scratch, 0, cnt_bytes, s);
-  if (e != cudaSuccess) return reject(SV_ERR_CUDA, cudaGetErrorString(e));
-  a.counters = static_cast<unsigned*>(scratch);
-  a.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + cnt_bytes);
   a.epi.kind = kEpiStore;
   a.epi.y = y;
   a.epi.ldy = N;
-  e = launch_gemm(a, s);
+  const cudaError_t e = launch_gemm(a, s);
   if (e != cudaSuccess) return reject(SV_ERR_CUDA, cudaGetErrorString(e));
   return SV_OK;
 }

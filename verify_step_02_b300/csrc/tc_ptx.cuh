@@ -98,6 +98,11 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
   return v;
 }
 
+// Store a float into distributed shared memory (a shared::cluster address).
+__device__ __forceinline__ void st_dsmem_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t caddr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
