@@ -146,10 +146,13 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
   a.cl_size = 0;
   a.cl_tiles = 0;
   // Small token tiles: the cluster split, when some (CTAs per cluster 2 .. 8, one tile
-  // per cluster) fits the device in one wave on at least 85% of the SMs (one SM
-  // streams only about its even share of HBM bandwidth with this pipeline depth)
-  // with per-CTA work within 1.2x of stream-K's: the fewest units per CTA wins,
-  // then the larger cluster (a smaller slice per rank, so more pipeline stages).
+  // per cluster) fits the device in one wave on at least 60% of the SMs with per-CTA
+  // work within 1.5x of stream-K's: the fewest units per CTA wins, then the larger
+  // cluster (a smaller slice per rank, so more pipeline stages). An SM streams about
+  // 50 GB/s with this pipeline depth, so 96 CTAs still draw 4.7 TB/s, and the cluster's
+  // hand-off through distributed shared memory ends about 5 us sooner than stream-K's
+  // through global memory (8B-class q|k|v, 48 tiles: 96 CTAs in 16.8 us, stream-K
+  // over 148 CTAs 19.7 us).
   if (a.tc_nt > kClusterMaxNT || a.m_tiles != 1 || a.tc_stages < 2) return;
   const long long ntt = static_cast<long long>(a.n_tiles) * a.m_tiles;
   const long long sk_work = (U + a.grid_p - 1) / a.grid_p;
@@ -165,7 +168,7 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
     // rank and the epilogue falls behind the MMAs (measured slower than stream-K)
     for (int tc = 1; tc <= 1; ++tc) {
       const long long ncl = (ntt + tc - 1) / tc;
-      if (ncl * cs > sm_count || ncl * cs * 20 < 17LL * sm_count) continue;
+      if (ncl * cs > sm_count || ncl * cs * 20 < 12LL * sm_count) continue;
       if (mc < 0) mc = max_clusters(a.tc_nt, pair2, w12, cs, st_cl);
       if (ncl > mc) continue;
       const long long work = static_cast<long long>(tc) * ((a.kb + cs - 1) / cs), ctas = ncl * cs;
@@ -178,7 +181,7 @@ void plan_gemm_tc(GemmArgs& a, int M, int n_units, int K, int pair, int sm_count
       }
     }
   }
-  if (best_cs == 0 || best_work * 5 > sk_work * 6) return;
+  if (best_cs == 0 || best_work * 2 > sk_work * 3) return;
   a.cl_size = best_cs;
   a.cl_tiles = best_tc;
   a.grid_p = static_cast<int>(best_ctas);
