@@ -930,8 +930,8 @@ SCHED_M = (8, 16, 24, 32, 40, 48, 64, 80, 96, 112, 136)
 def run_sweep_schedule(args, local):
     """The prefix scheduler on the device's own step costs (8B-class model, 8 requests at context 4096).
 
-    Measures T(M) for M = 8 .. 136 rows (the requests' lengths as even as possible), interpolates a
-    table for every M, draws per-draft confidences c ~ Beta(8, 2) (the 27B workload's draft model),
+    Measures T(M) for M = 8 .. 136 rows (the requests' lengths as even as possible), takes for every
+    M the cost of the next measured point at or above it, draws per-draft confidences c ~ Beta(8, 2) (the 27B workload's draft model),
     chooses the verify lengths with sv_schedule_prefix (with and without early stop), times the
     chosen lengths on the device and compares the expected throughput tau / T with two fixed
     rules: all 16 drafts, and drafts kept while the survival probability stays >= 0.3.
@@ -975,8 +975,9 @@ def run_sweep_schedule(args, local):
     for M in SCHED_M:
         lens = [M // B - 1 + (1 if r < M % B else 0) for r in range(B)]
         measured[M] = step_us(lens)
-    ms = np.array(SCHED_M, dtype=np.float64)
-    table_us = np.interp(np.arange(1, SCHED_M[-1] + 1), ms, [measured[m] for m in SCHED_M])
+    # T(M) between measured points: the cost of the next measured M at or above it (the step cost
+    # rises in steps at token-tile boundaries, so a straight line between points would understate it)
+    table_us = np.array([measured[min(m for m in SCHED_M if m >= M)] for M in range(1, SCHED_M[-1] + 1)])
     conf = synth.rng(31, 1).beta(8.0, 2.0, size=(B, G)).astype(np.float32)
     surv = np.cumprod(conf.astype(np.float64), axis=1)
 
