@@ -265,35 +265,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint64_t pol = policy_evict_first();
     int issued = 0;
     // sub-chunks whose keys all lie below C (cached before this step) go out
-    // before the dependency wait, up to the ring's depth
+    // before the dependency wait, up to the ring's depth; the block's own keys
+    // wait for the QKV product (the query tile is the MMA thread's to load)
     const int n_early = C - k0 >= kSub ? min(min(nsub, kStages), (C - k0) / kSub) : 0;
-    // the dependency wait, then the query tile (hi and lo planes)
-    auto load_q = [&]() {
+    auto dep_wait = [&]() {
       pdl_wait();
       pdl_trigger();
-      if (lane == 0) {
-        // QC copies of the tile's rows, at MMA rows 0, QL, ..
-        const uint32_t qbox = 128u * group * a.q_rows;
-        mbar_arrive_expect_tx(q_full, 2 * NH * qbox * QC);
-        const uint64_t polq = policy_evict_last();
-#pragma unroll
-        for (int cp = 0; cp < QC; ++cp)
-#pragma unroll
-          for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh)
-              tma_load_3d(smem + (pl * NH + hh) * kTile + cp * QL * 128, &tmq, hh * 64, h * group,
-                          pl * a.q_lo_row + row0 + j0, q_full, polq);
-      }
     };
-    if (n_early == nsub) load_q();  // (then every sub-chunk is early: the query first)
     for (int j = 0; j < nsub; ++j) {
       const int st = j % kStages;
       const int pj = j * (kSub / 16);  // the sub-chunk's first page in the range
-      if (j == n_early) load_q();
+      if (j == n_early) dep_wait();
       if (pj % kPageBlock == 0) load_pages(pj / kPageBlock);
       int ok = 1;
       if (lane == 0 && j >= kStages) ok = mbar_wait(kv_empty + st, (j / kStages - 1) & 1, abort_flag, kWaitNs);
+      // the first two sub-chunks go out alone: the rest wait until the first has
+      // landed, so that it is not served behind every CTA's whole ring
+      if (lane == 0 && j == 2) ok = mbar_wait(kv_full, 0, abort_flag, kWaitNs);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       // lane p < 4 takes page i = pj + p of the range, from lane i % 32,
       // register (i % kPageBlock) / 32 (the same register for the sub-chunk's four pages)
@@ -321,9 +309,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       ++issued;
     }
+    if (n_early == nsub) dep_wait();  // (every sub-chunk was early)
     if (lane == 0) {  // the copies land before the CTA can leave
       volatile int never = 0;
-      mbar_wait(q_full, 0, &never, kWaitNs);
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait(kv_full + j % kStages, (j / kStages) & 1, &never, kWaitNs);
     }
@@ -334,6 +322,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kSub);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);  // B (V) is N-major
       const uint32_t q = smem_u32(smem);
+      {
+        // the query tile (hi and lo planes), written by the QKV product (this warp has
+        // waited for it above): QC copies of the tile's rows, at MMA rows 0, QL, ..
+        const uint32_t qbox = 128u * group * a.q_rows;
+        mbar_arrive_expect_tx(q_full, 2 * NH * qbox * QC);
+        const uint64_t polq = policy_evict_last();
+#pragma unroll
+        for (int cp = 0; cp < QC; ++cp)
+#pragma unroll
+          for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh)
+              tma_load_3d(smem + (pl * NH + hh) * kTile + cp * QL * 128, &tmq, hh * 64, h * group,
+                          pl * a.q_lo_row + row0 + j0, q_full, polq);
+      }
       bool ok = mbar_wait(q_full, 0, abort_flag, kWaitNs);
       auto issue_s = [&](int j) {
         const int b = j & 1;
@@ -394,6 +397,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mma_commit(drain);
       volatile int never = 0;
       mbar_wait(drain, 0, &never, kDrainNs);
+      mbar_wait(q_full, 0, &never, kWaitNs);  // the query copy lands before the CTA can leave
     }
   } else {
     // ------------------------------------------------------------ rows: softmax, output
