@@ -125,3 +125,20 @@ def test_linear_projection_shapes(kind, m, n, k):
     # a second call on the same workspace gives the same bits (fixed-order split-K sums)
     y2, _ = vs.linear(wdtype, w_dev, torch.stack([hi, lo]), n, k, base=base, workspace=ws)
     assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("splits", range(1, 9))
+@pytest.mark.parametrize("m", [1, 5, 33])
+def test_fma_linear_cluster_splits(splits, m):
+    # one 128-row tile and K = 32 x splits: the CUDA-core product splits K into exactly
+    # `splits` CTAs of one cluster (1: no cluster), whose partials meet in distributed
+    # shared memory; against float64
+    rng = np.random.default_rng(100 * splits + m)
+    n, k = 128, 32 * splits
+    w = rng.standard_normal((n, k)).astype(np.float32)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    y, _ = vs.linear(vs.SV_F32, torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), n, k)
+    want = x.astype(np.float64) @ w.astype(np.float64).T
+    scale = np.sqrt((x.astype(np.float64) ** 2) @ (w.astype(np.float64) ** 2).T) + 1e-30
+    err = np.abs(y.cpu().numpy() - want) / scale
+    assert err.max() < 1e-5, err.max()
