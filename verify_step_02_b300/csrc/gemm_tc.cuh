@@ -10,14 +10,17 @@
 // Two ways to spread the K range of the tiles over the SMs:
 //   stream-K   P <= #SM CTAs share U = tiles x K blocks units; CTA c takes
 //              units [c U / P, (c+1) U / P), so every SM streams the same
-//              bytes. A tile whose K range is shared by several CTAs is
-//              finished by those of them whose ranges end inside it (the
-//              tile is their last work): once every contributor's partial
-//              tile is in global memory, each sums its own slice of the
-//              tile's tokens in CTA order and runs the slice's epilogue, so
-//              no single SM reads the whole tile's partials.
+//              bytes. With more tiles than CTAs, the first tiles - P tiles
+//              are shared this way and then every CTA takes one whole tile
+//              of its own, so that it ends on a local epilogue rather than
+//              on a hand-off. A tile whose K range is shared by several CTAs
+//              is finished by those of them whose shared ranges end inside
+//              it: once every contributor's partial tile is in global memory,
+//              each sums its own slice of the tile's tokens in CTA order and
+//              runs the slice's epilogue, so no single SM reads the whole
+//              tile's partials.
 //   cluster    (token tiles of at most 64 columns, one weight tile per cluster:
-//              the O and down projections) the CS CTAs of a cluster split the
+//              the q|k|v, O and down projections) the CS CTAs of a cluster split the
 //              tile's K blocks evenly. Each rank stores a 1/CS share of its
 //              partial tile's tokens straight into the shared memory of the
 //              rank that finishes those tokens (asynchronous stores counted on
@@ -68,10 +71,13 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long U, int P) {
 }
 
 // The units (tile, K block) of one CTA, in processing order: a contiguous
-// range of the tile-major order (stream-K), or every K block of the CTA's
-// slice [k0, k1) of each tile in [t0, t1) (cluster split).
+// range of the tile-major order of the stream-K tiles, then (with more tiles
+// than CTAs) one whole tile of its own (stream-K), or every K block of the
+// CTA's slice [k0, k1) of each tile in [t0, t1) (cluster split).
 struct CtaUnits {
   long long u0, n;   // stream-K: first unit; both: units of this CTA
+  long long nsk;     // stream-K: units of the shared range (then the whole tile tdp, if tdp >= 0)
+  long long tdp;
   long long t0;      // cluster: first tile
   int k0, nk;        // cluster: first K block and K blocks per tile
   int kb;            // K blocks of a whole tile
@@ -81,18 +87,22 @@ struct CtaUnits {
       const long long q = i / nk;
       t = t0 + q;
       kbi = k0 + static_cast<int>(i - q * nk);
-    } else {
+    } else if (i < nsk) {
       const long long u = u0 + i;
       t = u / kb;
       kbi = static_cast<int>(u - t * kb);
+    } else {
+      t = tdp;
+      kbi = static_cast<int>(i - nsk);
     }
   }
   // one past the last unit of the tile that unit i belongs to
   __device__ __forceinline__ long long seg_end(long long i) const {
     if (cl) return (i / nk + 1) * nk;
+    if (i >= nsk) return n;
     const long long t = (u0 + i) / kb;
     const long long e = (t + 1) * kb - u0;
-    return e < n ? e : n;
+    return e < nsk ? e : nsk;
   }
 };
 
@@ -166,7 +176,12 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = a.grid_p, c = blockIdx.x;
-  const long long U = static_cast<long long>(a.n_tiles) * a.m_tiles * a.kb;
+  // stream-K: with more tiles than CTAs (and at least one unit per CTA left to share),
+  // CTA c shares the first NTT - P tiles' units with the others, then takes tile
+  // NTT - P + c whole, so that it ends on a tile of its own, not on a hand-off
+  const long long NTT = static_cast<long long>(a.n_tiles) * a.m_tiles;
+  const long long TSK = NTT > P && (NTT - P) * a.kb >= P ? NTT - P : NTT;  // tiles shared by stream-K
+  const long long USK = TSK * a.kb;                                           // their units
   const int CS = CL ? a.cl_size : 1;
   const int rank = CL ? static_cast<int>(cluster_ctarank()) : 0;
   CtaUnits W;
@@ -180,9 +195,13 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
     W.nk = (rank + 1) * a.kb / CS - W.k0;
     W.u0 = 0;
     W.n = (t1 > W.t0 ? t1 - W.t0 : 0) * W.nk;
+    W.nsk = W.n;
+    W.tdp = -1;
   } else {
-    W.u0 = c * U / P;
-    W.n = (c + 1) * U / P - W.u0;
+    W.u0 = c * USK / P;
+    W.nsk = (c + 1) * USK / P - W.u0;
+    W.tdp = TSK < NTT ? TSK + c : -1;
+    W.n = W.nsk + (W.tdp >= 0 ? a.kb : 0);
     W.t0 = 0;
     W.k0 = 0;
     W.nk = a.kb;
@@ -609,7 +628,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
         }
       } else {
         // ---- stream-K: partials through global memory, summed in token slices
-        const int cf = cta_of_unit(t * a.kb, U, P), cl = cta_of_unit((t + 1) * a.kb - 1, U, P);
+        const bool own = t >= TSK;  // the CTA's own whole tile
+        const int cf = own ? c : cta_of_unit(t * a.kb, USK, P), cl = own ? c : cta_of_unit((t + 1) * a.kb - 1, USK, P);
         const bool alone = cf == cl;
         const int slot = t == slot0_tile ? 0 : 1;
         // partial tiles are column-major ([token][tile row]) so that a warp's
@@ -656,8 +676,8 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
           const bool share = mtot > 32;
           const int ncon = cl - cf + 1;
           const long long tend = (t + 1) * a.kb;
-          const int lp = static_cast<long long>(cl + 1) * U / P <= tend ? cl : cl - 1;
-          const bool part = share && static_cast<long long>(c + 1) * U / P <= tend;
+          const int lp = static_cast<long long>(cl + 1) * USK / P <= tend ? cl : cl - 1;
+          const bool part = share && static_cast<long long>(c + 1) * USK / P <= tend;
           const int npart = share ? lp - cf + 1 : 1;
           const int ws = ((mtot + npart - 1) / npart + 3) / 4 * 4;
           const int s0 = share ? (c - cf) * ws : 0, s1 = share ? (s0 + ws < mtot ? s0 + ws : mtot) : mtot;
@@ -682,7 +702,7 @@ __global__ void __launch_bounds__(W12 ? kTcThreadsW12 : kTcThreads, 1)
             // the contributors' slots, in CTA order (a fixed summation order): a
             // tile is the first tile (slot 0) of every contributor after cf, and of
             // cf when cf's range starts at the tile's first unit
-            const int sl_first = static_cast<long long>(cf) * U / P == t * a.kb ? 0 : 1;
+            const int sl_first = static_cast<long long>(cf) * USK / P == t * a.kb ? 0 : 1;
             constexpr int RW = 32 / (EPT / 128);  // columns of a chunk each warpgroup sums
             const int col0 = grpA ? 0 : RW;
             constexpr int NB = W12 ? 1 : 4;  // contributors whose loads are in flight together
