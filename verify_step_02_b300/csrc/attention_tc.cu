@@ -685,20 +685,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int it = tid; it < nrr * D4; it += kAttnThreads) {
           const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
           const size_t base = static_cast<size_t>(blockIdx.x) * CC;
+          // every cluster's (m, l) and partial O of this row and 4 dims, all loads in flight
+          float2 ml[kMaxCrossClusters];
+          float4 o[kMaxCrossClusters];
+#pragma unroll
+          for (int c = 0; c < kMaxCrossClusters; ++c)
+            if (c < CC) {
+              ml[c] = __ldcg(a.xml + (base + c) * 128 + rho);
+              o[c] = __ldcg(reinterpret_cast<const float4*>(a.xpart + ((base + c) * 128 + rho) * HD + d));
+            }
           float M = -INFINITY;
-          for (int c = 0; c < CC; ++c) M = fmaxf(M, __ldcg(a.xml + (base + c) * 128 + rho).x);
+#pragma unroll
+          for (int c = 0; c < kMaxCrossClusters; ++c)
+            if (c < CC) M = fmaxf(M, ml[c].x);
           float L = 0.f;
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c = 0; c < CC; ++c) {  // in cluster order: a fixed summation order
-            const float2 ml = __ldcg(a.xml + (base + c) * 128 + rho);
-            const float w = ml.x == -INFINITY ? 0.f : __expf(ml.x - M);
+#pragma unroll
+          for (int c = 0; c < kMaxCrossClusters; ++c) {  // in cluster order: a fixed summation order
+            const float w = c < CC && ml[c].x != -INFINITY ? __expf(ml[c].x - M) : 0.f;
             if (w == 0.f) continue;
-            const float4 o = __ldcg(reinterpret_cast<const float4*>(a.xpart + ((base + c) * 128 + rho) * HD + d));
-            L += ml.y * w;
-            acc.x += o.x * w;
-            acc.y += o.y * w;
-            acc.z += o.z * w;
-            acc.w += o.w * w;
+            L += ml[c].y * w;
+            acc.x += o[c].x * w;
+            acc.y += o[c].y * w;
+            acc.z += o[c].z * w;
+            acc.w += o[c].w * w;
           }
           const float inv = L > 0.f ? 1.0f / L : 0.f;
           acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
