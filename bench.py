@@ -203,8 +203,8 @@ LAYER_KERNELS = ("qkv", "attention", "o", "gate_up", "down")
 # trace words past the common ones (1 start, 2 wait, 3 first operands, 4 last MMA, 6 exit)
 GEMM_MARKS = (("t_acc", 7), ("t_x", 12), ("t_stored", 8), ("t_counted", 9), ("t_summed", 13), ("t_reduced", 10),
               ("t_epilogue", 11))
-ATTN_MARKS = (("s0_ready", 12), ("p0_ready", 13), ("kv_last", 10), ("p_last", 11), ("partial", 7),
-              ("cluster_synced", 8), ("merge_weights", 9))
+ATTN_MARKS = (("s0_ready", 12), ("p0_ready", 13), ("kv_last", 10), ("p_last", 11), ("pv_done", 14),
+              ("sets_merged", 15), ("partial", 7), ("cluster_synced", 8), ("merge_weights", 9))
 
 
 def trace_summary(records, launches, n_layers):

@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t PM_OFF = KV_OFF + kStages * KVB;  // partial row maxima, bf16 [set][hf][128]
   // once every MMA is done the K/V ring holds the CTA's partial (O, then (m, l)) and
   // the merge's scratch: the two sets' (m, l), then the cluster merge's weights
-  constexpr uint32_t XCH_OFF = KV_OFF + 128 * HD * 4 + 128 * 8;
+  // the partial's rows are HD + 4 floats apart: the lanes of a warp store consecutive
+  // rows, which a stride of HD floats (a multiple of 128 bytes) would put in one bank
+  constexpr int OLD = HD + 4;
+  constexpr uint32_t XCH_OFF = KV_OFF + 128 * OLD * 4 + 128 * 8;
   constexpr uint32_t WTS_OFF = XCH_OFF + 4 * 128 * 8;
   constexpr uint32_t MLS_OFF = WTS_OFF + 128 * 16 * 4;
   constexpr uint32_t MLR_OFF = MLS_OFF + 128 * 16 * 8;  // the cluster's merged (m, l) of this rank's rows
@@ -194,8 +197,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int nsub = nkeys > 0 ? (nkeys + kSub - 1) / kSub : 0;
   const int R = ntok * group;
   // the CTA's partial (m, l, O) of each row, in the K/V ring once every MMA is done
-  float* Os = reinterpret_cast<float*>(smem + KV_OFF);        // [128 rows][HD]
-  float2* ML = reinterpret_cast<float2*>(smem + KV_OFF + 128 * HD * 4);  // [128 rows]
+  float* Os = reinterpret_cast<float*>(smem + KV_OFF);        // [128 rows][OLD]
+  float2* ML = reinterpret_cast<float2*>(smem + KV_OFF + 128 * OLD * 4);  // [128 rows]
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -551,6 +554,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // merge the two sets' (m, l, O) of each row into the CTA's partial, in shared memory
     int okw = 0;
     if (lane == 0) okw = ok && mbar_wait(o_full, 0, abort_flag, kWaitNs) ? 1 : 0;
+    if (tid == 0) trace_mark(rec, 14);
     okw = __shfl_sync(0xffffffffu, okw, 0);
     float2* xch = reinterpret_cast<float2*>(smem + XCH_OFF);  // [set][hf][128]
     if (okw) xch[(set * 2 + hf) * 128 + rho] = make_float2(m, l);
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float o0[16], o1[16];
         tmem_ld16(tO + lane_base + col, o0);
         if (has1) tmem_ld16(tO + HD + lane_base + col, o1);
-        float4* po = reinterpret_cast<float4*>(Os + rho * HD + col);
+        float4* po = reinterpret_cast<float4*>(Os + rho * OLD + col);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float x[4];
@@ -585,7 +589,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else if (set == 0 && hf == 0) {
       ML[rho] = make_float2(-INFINITY, 0.f);
     }
-    if (tid == 0) trace_mark(rec, 5);
+    if (tid == 0) trace_mark(rec, 15);
   }
 
   tc_fence_before();
@@ -648,7 +652,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int kk = 0; kk < KB; ++kk) {
           const int p = p0 + kk;
           if (p < NP && wts[rr * NP + p] != 0.f)
-            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (((p % QC) * QL + rho) * HD + d),
+            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (((p % QC) * QL + rho) * OLD + d),
                                                static_cast<uint32_t>(p / QC)));
         }
 #pragma unroll

@@ -140,7 +140,7 @@ struct TokData {
 // the cluster shares summed. The attention adds 7 partial (m, l, O) in shared
 // memory, 8 the cluster's partials visible, 9 merge weights computed, 10 last
 // K/V stage landed, 11 last softmax done, 12 first scores ready, 13 first
-// softmax done.
+// softmax done, 14 every P·V product complete, 15 the two softmax sets merged.
 constexpr int kTraceWords = 16;
 enum TraceKind : int { kTrGemm = 1, kTrAttn = 2, kTrMerge = 3, kTrPrep = 4, kTrAccept = 5, kTrGemmFma = 6 };
 
