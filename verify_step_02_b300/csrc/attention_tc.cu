@@ -604,77 +604,130 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) trace_mark(rec, 8);
   {
     // rank i merges rows [i rpr, (i + 1) rpr) of the NP = CS QC partials (rank k,
-    // copy c: lane c QL + row of rank k): first each row's weights
-    // e^(m_p - M) / sum_p l_p e^(m_p - M) (one thread per row), then the output
-    // rows, 4 dims per item
+    // copy c: lane c QL + row of rank k) with the weights e^(m_p - M) / sum_p l_p
+    // e^(m_p - M), 4 output dims per item: with at most 8 partials each item forms
+    // its row's weights from loads issued with its O loads; with more, one thread
+    // per row forms them first
     constexpr int NPMAX = kMaxCluster * QC;
     const int NP = CS * QC;
     const int rpr = (R + CS - 1) / CS;
     const int rr0 = rank * rpr, rr1 = rr0 + rpr < R ? rr0 + rpr : R;
     const uint32_t os_addr = smem_u32(Os), ml_addr = smem_u32(ML);
-    float* wts = reinterpret_cast<float*>(smem + WTS_OFF);    // [rpr][NP]
-    float2* mls = reinterpret_cast<float2*>(smem + MLS_OFF);  // [rpr][NP]
     const int nrr = rr1 - rr0;
-    // every partial's (m, l) of this rank's rows, all loads in flight
-    for (int it = tid; it < nrr * NP; it += kAttnThreads) {
-      const int rr = it / NP, p = it - rr * NP;
-      const uint32_t ln = static_cast<uint32_t>((p % QC) * QL + rr0 + rr);
-      mls[rr * NP + p] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * ln, static_cast<uint32_t>(p / QC)));
-    }
-    __syncthreads();
-    for (int rr = tid; rr < nrr; rr += kAttnThreads) {
-      float M = -INFINITY;
-      for (int p = 0; p < NP; ++p) M = fmaxf(M, mls[rr * NP + p].x);
-      float L = 0.f;
-      for (int p = 0; p < NP; ++p) {
-        const float2 v = mls[rr * NP + p];
-        const float w = v.x == -INFINITY ? 0.f : __expf(v.x - M);
-        wts[rr * NP + p] = w;
-        L += v.y * w;
-      }
-      // L = 0 only for rows whose keys were all on bad pages (flagged): output 0. With
-      // several clusters the sum stays unnormalized until their partials meet.
-      const float inv = CC > 1 ? 1.f : (L > 0.f ? 1.0f / L : 0.f);
-      for (int p = 0; p < NP; ++p) wts[rr * NP + p] *= inv;
-      if (CC > 1) reinterpret_cast<float2*>(smem + MLR_OFF)[rr] = make_float2(M, L);
-    }
-    __syncthreads();
-    if (tid == 0) trace_mark(rec, 9);
     constexpr int D4 = HD / 4;
-    constexpr int KB = 8;  // partials whose O loads are in flight together
+    constexpr int KB = 8;  // partials whose loads are in flight together
     static_assert(NPMAX % KB == 0, "partials in groups of KB");
-    for (int it = tid; it < nrr * D4; it += kAttnThreads) {
-      const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p0 = 0; p0 < NP; p0 += KB) {
-        float4 o[KB];
-#pragma unroll
-        for (int kk = 0; kk < KB; ++kk) {
-          const int p = p0 + kk;
-          if (p < NP && wts[rr * NP + p] != 0.f)
-            o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (((p % QC) * QL + rho) * OLD + d),
-                                               static_cast<uint32_t>(p / QC)));
-        }
-#pragma unroll
-        for (int kk = 0; kk < KB; ++kk) {
-          const float w = p0 + kk < NP ? wts[rr * NP + p0 + kk] : 0.f;
-          if (w != 0.f) {
-            acc.x += o[kk].x * w;
-            acc.y += o[kk].y * w;
-            acc.z += o[kk].z * w;
-            acc.w += o[kk].w * w;
-          }
-        }
-      }
+    // the merged row: the output (one cluster), or with several clusters the row's
+    // unnormalized partial and (M, L) for the last of them to arrive
+    auto finish = [&](int rr, int d, float4 acc, float M, float L) {
+      const int rho = rr0 + rr;
       if (CC > 1) {
         const size_t slot = static_cast<size_t>(blockIdx.x) * CC + cc;
         __stcg(reinterpret_cast<float4*>(a.xpart + (slot * 128 + rho) * HD + d), acc);
-        if (d == 0) __stcg(a.xml + slot * 128 + rho, reinterpret_cast<const float2*>(smem + MLR_OFF)[rr]);
-        continue;
+        if (d == 0) __stcg(a.xml + slot * 128 + rho, make_float2(M, L));
+        return;
       }
       const int jrow = j0 + rho / group, g = rho % group;
       const long long orow = static_cast<long long>(row0 + jrow) * a.n_heads * HD + (h * group + g) * HD + d;
       store_x4(a.out, a.out_plane, orow, acc, a.x_pair);
+    };
+    if (NP <= KB) {
+      // few partials: every item loads its row's (m, l) and O of each partial in one
+      // round trip and forms the row's weights itself (the same arithmetic, in the
+      // same order, as the two-phase merge below)
+      if (tid == 0) trace_mark(rec, 9);
+      for (int it = tid; it < nrr * D4; it += kAttnThreads) {
+        const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
+        float2 ml[KB];
+        float4 o[KB];
+#pragma unroll
+        for (int p = 0; p < KB; ++p)
+          if (p < NP) {
+            const uint32_t ln = static_cast<uint32_t>((p % QC) * QL + rho), rk = static_cast<uint32_t>(p / QC);
+            ml[p] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * ln, rk));
+            o[p] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (ln * OLD + d), rk));
+          }
+        float M = -INFINITY;
+#pragma unroll
+        for (int p = 0; p < KB; ++p)
+          if (p < NP) M = fmaxf(M, ml[p].x);
+        float w[KB];
+        float L = 0.f;
+#pragma unroll
+        for (int p = 0; p < KB; ++p) {
+          w[p] = p < NP && ml[p].x != -INFINITY ? __expf(ml[p].x - M) : 0.f;
+          if (p < NP) L += ml[p].y * w[p];
+        }
+        // L = 0 only for rows whose keys were all on bad pages (flagged): output 0. With
+        // several clusters the sum stays unnormalized until their partials meet.
+        const float inv = CC > 1 ? 1.f : (L > 0.f ? 1.0f / L : 0.f);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < KB; ++p) {
+          const float wp = p < NP ? w[p] * inv : 0.f;
+          if (wp != 0.f) {
+            acc.x += o[p].x * wp;
+            acc.y += o[p].y * wp;
+            acc.z += o[p].z * wp;
+            acc.w += o[p].w * wp;
+          }
+        }
+        finish(rr, d, acc, M, L);
+      }
+    } else {
+      float* wts = reinterpret_cast<float*>(smem + WTS_OFF);    // [rpr][NP]
+      float2* mls = reinterpret_cast<float2*>(smem + MLS_OFF);  // [rpr][NP]
+      // every partial's (m, l) of this rank's rows, all loads in flight
+      for (int it = tid; it < nrr * NP; it += kAttnThreads) {
+        const int rr = it / NP, p = it - rr * NP;
+        const uint32_t ln = static_cast<uint32_t>((p % QC) * QL + rr0 + rr);
+        mls[rr * NP + p] = ld_dsmem_f32x2(mapa_shared(ml_addr + 8u * ln, static_cast<uint32_t>(p / QC)));
+      }
+      __syncthreads();
+      for (int rr = tid; rr < nrr; rr += kAttnThreads) {
+        float M = -INFINITY;
+        for (int p = 0; p < NP; ++p) M = fmaxf(M, mls[rr * NP + p].x);
+        float L = 0.f;
+        for (int p = 0; p < NP; ++p) {
+          const float2 v = mls[rr * NP + p];
+          const float w = v.x == -INFINITY ? 0.f : __expf(v.x - M);
+          wts[rr * NP + p] = w;
+          L += v.y * w;
+        }
+        // L = 0 only for rows whose keys were all on bad pages (flagged): output 0. With
+        // several clusters the sum stays unnormalized until their partials meet.
+        const float inv = CC > 1 ? 1.f : (L > 0.f ? 1.0f / L : 0.f);
+        for (int p = 0; p < NP; ++p) wts[rr * NP + p] *= inv;
+        if (CC > 1) reinterpret_cast<float2*>(smem + MLR_OFF)[rr] = make_float2(M, L);
+      }
+      __syncthreads();
+      if (tid == 0) trace_mark(rec, 9);
+      for (int it = tid; it < nrr * D4; it += kAttnThreads) {
+        const int rr = it / D4, rho = rr0 + rr, d = (it % D4) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p0 = 0; p0 < NP; p0 += KB) {
+          float4 o[KB];
+#pragma unroll
+          for (int kk = 0; kk < KB; ++kk) {
+            const int p = p0 + kk;
+            if (p < NP && wts[rr * NP + p] != 0.f)
+              o[kk] = ld_dsmem_f32x4(mapa_shared(os_addr + 4u * (((p % QC) * QL + rho) * OLD + d),
+                                                 static_cast<uint32_t>(p / QC)));
+          }
+#pragma unroll
+          for (int kk = 0; kk < KB; ++kk) {
+            const float w = p0 + kk < NP ? wts[rr * NP + p0 + kk] : 0.f;
+            if (w != 0.f) {
+              acc.x += o[kk].x * w;
+              acc.y += o[kk].y * w;
+              acc.z += o[kk].z * w;
+              acc.w += o[kk].w * w;
+            }
+          }
+        }
+        const float2 mlr = CC > 1 ? reinterpret_cast<const float2*>(smem + MLR_OFF)[rr] : make_float2(0.f, 0.f);
+        finish(rr, d, acc, mlr.x, mlr.y);
+      }
     }
     if (CC > 1) {
       // the last of the item's CC clusters to arrive for this rank's rows merges their partials
