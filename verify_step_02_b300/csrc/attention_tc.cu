@@ -109,12 +109,29 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
   else if constexpr (N == 16) tmem_ld16(taddr, v);
   else tmem_ld8(taddr, v);
 }
+// N consecutive 32-bit TMEM columns of this thread's lane, issued without the
+// completion wait (the registers are read at issue): tmem_wait_st() completes
+// every earlier store of the thread, so several stores share one wait.
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* v) {
-  if constexpr (N == 16) tmem_st16u(taddr, v);
-  else if constexpr (N == 8) tmem_st8u(taddr, v);
-  else tmem_st4u(taddr, v);
+  if constexpr (N == 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+  } else if constexpr (N == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+  }
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <int HD, int QC>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -520,6 +537,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         tmem_st_cols<NKW / 2>(tp + kk0 / 2, ph);
         tmem_st_cols<NKW / 2>(tp + 32 + kk0 / 2, pl);
+        tmem_wait_st();  // both halves in TMEM before the P-ready arrival below
       }
       if (j >= set + 2 && __any_sync(0xffffffffu, corr != 1.f)) {
         // this warp rescales O_set's dims hf * HD / 2 .. + HD / 2
